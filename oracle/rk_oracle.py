@@ -1,0 +1,284 @@
+"""fp64 CPU oracle for RoPE repositioning and SegPagedAttention.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's CPU
+baseline leg may import this module; the library path never does.  It shares no
+code with the CUDA library: it reads the same numpy inputs (bf16 as uint16 bit
+patterns) and recomputes everything in float64, slowly and plainly.
+
+What it computes, and where the pages state it:
+
+* RoPE repositioning ("RedKnot" article on is96.com, paragraphs on RoPE and on
+  the correction RedKnot applies): cached K was rotated at its offline
+  position; it is first rotated *back* at that offline position and then
+  rotated *forward* at the online position.  Both rotations are applied here,
+  one after the other, exactly as described.  The rotation itself (which
+  channels pair up, the frequency of each pair) is not printed on the pages;
+  the reading taken is the one of the Qwen/Llama families the pages evaluate:
+  channel i pairs with i + d/2 (or, as an option, 2i with 2i+1) and turns by
+  position * theta^(-2i/d).
+* Per-head page tables ("RedKnot" article, SegPagedAttention paragraph; "小红书
+  RedKnot" section 3, fourth component): each (sequence, KV head) segment lists
+  the pages it reads; token j of a segment lives in logical page j // P, slot
+  j % P, and the table maps the logical page to a physical page of the shared
+  pool ("PagedAttention & RadixAttention", "The Solution: Fixed-size blocks").
+* Head classes ("小红书 RedKnot", section 3, first component): global heads see
+  the whole (causal) context, local heads a window of recent tokens, retrieval
+  heads the pages their table lists, dense heads the whole context of freshly
+  computed K.  The visible set of the query at position p is materialised
+  explicitly:
+      V(p) = { j : page j // P is listed, j < seq_len, j <= p,
+               and, for a local head, j > p - W or j < S }.
+* Attention ("PagedAttention & RadixAttention": the attention math itself is
+  the standard dot-product softmax, only storage and gathering change):
+      o = sum_{j in V(p)} softmax_j(q . k_j * scale) v_j,   lse = log sum_j e^{q.k_j*scale}
+  with scale = 1/sqrt(d) and query head h reading KV head h // (Hq/Hkv).
+* Split combine (standard FlashAttention split-KV merge of partial (m, l, o)).
+
+Readings of silent points are listed in the repository's design notes; the
+pins that tie each function to something other than itself live in
+tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Iterable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+GLOBAL, LOCAL, RETRIEVAL, DENSE = 0, 1, 2, 3
+ROPE_HALF_SPLIT, ROPE_INTERLEAVED = 0, 1
+
+
+# ----------------------------------------------------------------------------- bf16
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 to the nearest bf16 (ties to even), returned as uint16 bits.
+
+    Rounds directly from float64 (no intermediate float32 rounding): write
+    |x| = m * 2^e with m in [0.5, 1); bf16 keeps 8 significant bits, so the
+    quantum is 2^(e-8), or 2^-133 below the normal range.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    quantum = np.ldexp(1.0, e - 8)
+    r = np.rint(x / quantum) * quantum          # np.rint rounds half to even; exact in fp64
+    # r has at most 8 significant bits, so the float32 conversion below is exact
+    return (np.asarray(r, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bf16_ordinal(bits: np.ndarray) -> np.ndarray:
+    """Monotone integer map of bf16 values, so that ordinal distance = ulp distance."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+# ----------------------------------------------------------------------------- RoPE
+def rope_inv_freq(theta: float, d: int) -> np.ndarray:
+    """Frequency of channel pair i: theta^(-2i/d), i < d/2, in float64."""
+    i = np.arange(d // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / d)
+
+
+def rope_pairs(d: int, style: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Channel indices (a_i, b_i) of pair i."""
+    i = np.arange(d // 2)
+    if style == ROPE_HALF_SPLIT:
+        return i, i + d // 2
+    if style == ROPE_INTERLEAVED:
+        return 2 * i, 2 * i + 1
+    raise ValueError("unknown RoPE style")
+
+
+def rope_rotate(x: np.ndarray, pos: np.ndarray, theta: float, style: int = ROPE_HALF_SPLIT,
+                inverse: bool = False) -> np.ndarray:
+    """Rotate each row x[t, :] by its position pos[t]: pair (a_i, b_i) turns by
+    angle pos * theta^(-2i/d) (clockwise when inverse)."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    a, b = rope_pairs(d, style)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * rope_inv_freq(theta, d)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    if inverse:
+        s = -s
+    y = np.empty_like(x)
+    y[:, a] = x[:, a] * c - x[:, b] * s
+    y[:, b] = x[:, a] * s + x[:, b] * c
+    return y
+
+
+def rope_reposition(k: np.ndarray, pos_off: np.ndarray, pos_on: np.ndarray, theta: float,
+                    style: int = ROPE_HALF_SPLIT) -> np.ndarray:
+    """Inverse rotation at the offline position, then forward rotation at the online one."""
+    back = rope_rotate(k, pos_off, theta, style, inverse=True)
+    return rope_rotate(back, pos_on, theta, style, inverse=False)
+
+
+def token_to_physical(table: Sequence[int], P: int, t: int) -> Tuple[int, int]:
+    """Logical token t -> (physical page, slot) through a dense block table."""
+    return int(table[t // P]), t % P
+
+
+def paged_rope_reposition(k_src: np.ndarray, src_tables: np.ndarray, dst_tables: np.ndarray,
+                          runs: np.ndarray, theta: float, P: int, style: int = ROPE_HALF_SPLIT):
+    """Apply every run; returns (dst_page, dst_slot, rows): the fp64 rows written and where.
+
+    Run fields: src_tab_off, src_tab_len, dst_tab_off, dst_tab_len, pos_off0, pos_on0, n_tok.
+    Token t of a run reads slot (pos_off0+t) of its src table and writes slot
+    (pos_on0+t) of its dst table.
+    """
+    pages, slots, rows = [], [], []
+    for r in np.asarray(runs):
+        s_off, s_len, d_off, d_len, p_off0, p_on0, n = (int(v) for v in r[:7])
+        if n == 0:
+            continue
+        t = np.arange(n, dtype=np.int64)
+        p_off = p_off0 + t
+        p_on = p_on0 + t
+        s_tab = np.asarray(src_tables[s_off:s_off + s_len], dtype=np.int64)
+        d_tab = np.asarray(dst_tables[d_off:d_off + d_len], dtype=np.int64)
+        x = bf16_to_f64(k_src[s_tab[p_off // P], p_off % P])
+        rows.append(rope_reposition(x, p_off, p_on, theta, style))
+        pages.append(d_tab[p_on // P])
+        slots.append(p_on % P)
+    if not rows:
+        d = k_src.shape[-1]
+        return np.zeros(0, np.int64), np.zeros(0, np.int64), np.zeros((0, d))
+    return np.concatenate(pages), np.concatenate(slots), np.concatenate(rows)
+
+
+def apply_rope_to_pool(k_pool: np.ndarray, written) -> np.ndarray:
+    """Store the oracle's repositioned rows into a copy of a bf16 pool (RNE to bf16:
+    the pool's storage type)."""
+    pages, slots, rows = written
+    out = np.array(k_pool, copy=True)
+    out[pages, slots] = f64_to_bf16(rows)
+    return out
+
+
+# ----------------------------------------------------------------------------- visibility
+def listed_positions(page_logical_row: np.ndarray, n_listed: int, P: int) -> np.ndarray:
+    """Logical token positions covered by the listed pages of one head segment."""
+    lp = np.asarray(page_logical_row[:n_listed], dtype=np.int64)
+    return (lp[:, None] * P + np.arange(P)[None, :]).reshape(-1)
+
+
+def visible_set(cls: int, window: int, sink: int, seq_len: int, p: int,
+                listed: np.ndarray) -> np.ndarray:
+    """Sorted logical key positions visible to the query at position p."""
+    j = np.asarray(listed, dtype=np.int64)
+    keep = (j < seq_len) & (j <= p)
+    if cls == LOCAL:
+        keep &= (j > p - window) | (j < sink)
+    elif cls not in (GLOBAL, RETRIEVAL, DENSE):
+        raise ValueError("unknown head class")
+    return np.sort(j[keep])
+
+
+def gather_rows(pool: np.ndarray, table_row: np.ndarray, logical_row: np.ndarray, n_listed: int,
+                P: int, positions: np.ndarray) -> np.ndarray:
+    """fp64 rows of the given logical positions, read through the head's page list."""
+    lp2phys = {int(logical_row[e]): int(table_row[e]) for e in range(n_listed)}
+    pg = np.array([lp2phys[int(p) // P] for p in positions], dtype=np.int64)
+    return bf16_to_f64(pool[pg, np.asarray(positions, dtype=np.int64) % P])
+
+
+# ----------------------------------------------------------------------------- attention
+def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
+    """Dense softmax attention of query rows q [G, d] over keys k/v [n, d] (fp64).
+    Returns (o [G, d], lse [G]); an empty key set gives o = 0, lse = -inf."""
+    if k.shape[0] == 0:
+        return np.zeros((q.shape[0], v.shape[1])), np.full(q.shape[0], -np.inf)
+    s = (q @ k.T) * scale
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=1, keepdims=True)
+    o = (e @ v) / l
+    return o, (m + np.log(l))[:, 0]
+
+
+def segpaged_attention(batch, rows: Optional[Iterable[Tuple[int, int]]] = None,
+                       scale: Optional[float] = None):
+    """Reference outputs of one SegPaged attention launch.
+
+    rows: iterable of (query token index into q, KV head) to compute; None = all.
+    Returns dict {(t, h_kv): (o [G, d], lse [G])} for the G query heads of group h_kv.
+    """
+    B, Hq, Hkv, d, P = batch.B, batch.Hq, batch.Hkv, batch.d, batch.P
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    cu = np.asarray(batch.cu_seqlens_q)
+    tok_seq = np.repeat(np.arange(B), np.diff(cu))
+    if rows is None:
+        rows = [(t, h) for t in range(int(cu[-1])) for h in range(Hkv)]
+    # group requested rows by head segment so each segment's keys are gathered once
+    by_seg: Dict[Tuple[int, int], List[int]] = {}
+    for t, h in rows:
+        by_seg.setdefault((int(tok_seq[t]), int(h)), []).append(int(t))
+    out = {}
+    for (b, h), toks in by_seg.items():
+        seg = b * Hkv + h
+        nl = int(batch.n_pages[seg])
+        listed = listed_positions(batch.page_logical[seg], nl, P)
+        L = int(batch.seq_len[b])
+        nq = int(cu[b + 1] - cu[b])
+        cls, W, S = int(batch.head_class[seg]), int(batch.window[seg]), int(batch.sink[seg])
+        cand = np.sort(listed[listed < L])
+        kk = gather_rows(batch.k_pool, batch.page_table[seg], batch.page_logical[seg], nl, P, cand)
+        vv = gather_rows(batch.v_pool, batch.page_table[seg], batch.page_logical[seg], nl, P, cand)
+        for t in toks:
+            p = L - nq + (t - int(cu[b]))
+            vis = visible_set(cls, W, S, L, p, cand)
+            idx = np.searchsorted(cand, vis)      # vis is a subset of the sorted cand
+            qg = bf16_to_f64(batch.q[t, h * G:(h + 1) * G])
+            out[(t, h)] = softmax_attention(qg, kk[idx], vv[idx], scale)
+    return out
+
+
+def split_partials(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, bounds: Sequence[int]):
+    """Unnormalised partial results (m, l, o) of attention over key ranges [bounds[i], bounds[i+1])."""
+    parts = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if b <= a:
+            parts.append((np.full(q.shape[0], -np.inf), np.zeros(q.shape[0]), np.zeros((q.shape[0], v.shape[1]))))
+            continue
+        s = (q @ k[a:b].T) * scale
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        parts.append((m, e.sum(axis=1), e @ v[a:b]))
+    return parts
+
+
+def combine_partials(parts):
+    """Merge split partials: m = max m_i, l = sum e^{m_i-m} l_i, o = sum e^{m_i-m} o_i / l."""
+    ms = np.stack([p[0] for p in parts])
+    m = ms.max(axis=0)
+    w = np.where(np.isfinite(ms), np.exp(ms - m[None, :]), 0.0)
+    l = sum(w[i] * parts[i][1] for i in range(len(parts)))
+    o = sum(w[i][:, None] * parts[i][2] for i in range(len(parts)))
+    return o / l[:, None], m + np.log(l)
+
+
+def attention_flops(batch) -> int:
+    """Algorithmic FLOPs: 4 * d * visible (query head, key) pairs, by explicit count."""
+    B, Hq, Hkv, d, P = batch.B, batch.Hq, batch.Hkv, batch.d, batch.P
+    G = Hq // Hkv
+    cu = np.asarray(batch.cu_seqlens_q)
+    pairs = 0
+    for b in range(B):
+        L = int(batch.seq_len[b])
+        nq = int(cu[b + 1] - cu[b])
+        for h in range(Hkv):
+            seg = b * Hkv + h
+            listed = listed_positions(batch.page_logical[seg], int(batch.n_pages[seg]), P)
+            cls, W, S = int(batch.head_class[seg]), int(batch.window[seg]), int(batch.sink[seg])
+            for i in range(nq):
+                pairs += len(visible_set(cls, W, S, L, L - nq + i, listed))
+    return 4 * d * G * pairs

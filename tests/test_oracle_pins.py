@@ -1,0 +1,254 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself:
+worked examples printed on the pages (tests/golden), closed forms, special cases
+that reduce to library routines, and invariants stated by the pages."""
+import dataclasses
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import rk_oracle as O
+from workloads import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ bf16 rounding
+def test_bf16_rounding_matches_torch_on_float32_values():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(100000).astype(np.float32) * s for s in (1e-3, 1.0, 1e3)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.f64_to_bf16(x.astype(np.float64)), ref)
+
+
+def test_bf16_rounding_ties_and_no_double_rounding():
+    one = 0x3F80
+    assert O.f64_to_bf16(np.array([1 + 2.0 ** -8]))[0] == one                     # tie -> even (1.0)
+    assert O.f64_to_bf16(np.array([1 + 3 * 2.0 ** -8]))[0] == one + 2             # tie -> even (1+2^-6)
+    # just above a tie: float32 would round it onto the tie first and then to 1.0
+    assert O.f64_to_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -30]))[0] == one + 1
+    assert O.f64_to_bf16(np.array([-2.5]))[0] == 0xC020
+    assert np.array_equal(O.bf16_to_f64(np.array([0x3F80, 0xC020], np.uint16)), [1.0, -2.5])
+
+
+def test_bf16_ordinal_is_ulp_distance():
+    b = np.array([0x3F80, 0x3F81, 0x0000, 0x8000, 0x8001, 0x0001], np.uint16)
+    o = O.bf16_ordinal(b)
+    assert o[1] - o[0] == 1 and o[2] == o[3] == 0 and o[5] - o[4] == 2
+
+
+# ------------------------------------------------------------------ RoPE
+@pytest.mark.parametrize("case", _load("rope_unit_vectors.json")["cases"])
+def test_rope_unit_vectors(case):
+    g = _load("rope_unit_vectors.json")
+    style = O.ROPE_HALF_SPLIT if case["style"] == "half_split" else O.ROPE_INTERLEAVED
+    y = O.rope_rotate(np.array([case["x"]], float), np.array([case["pos"]]), g["theta"], style)
+    assert np.allclose(y[0], case["y"], atol=1e-15)
+
+
+@pytest.mark.parametrize("style", [O.ROPE_HALF_SPLIT, O.ROPE_INTERLEAVED])
+def test_rope_equals_complex_multiplication(style):
+    # the same rotation written as multiplication by e^{i*angle} of the complex pair (a + i b)
+    rng = np.random.default_rng(1)
+    d, theta = 128, 1e6
+    x = rng.standard_normal((64, d))
+    pos = rng.integers(0, 200000, 64)
+    a, b = O.rope_pairs(d, style)
+    z = (x[:, a] + 1j * x[:, b]) * np.exp(1j * pos[:, None] * theta ** (-np.arange(0, d, 2) / d))
+    y = O.rope_rotate(x, pos, theta, style)
+    assert np.allclose(y[:, a], z.real, atol=1e-9) and np.allclose(y[:, b], z.imag, atol=1e-9)
+
+
+def test_rope_composition_closed_form():
+    # R(p2) R(p1)^-1 = R(p2 - p1), identity at equal positions, pair norms preserved
+    rng = np.random.default_rng(2)
+    d, theta = 128, 1e6
+    x = rng.standard_normal((256, d))
+    p1 = rng.integers(0, 5000, 256)
+    p2 = p1 + rng.integers(0, 30000, 256)
+    y = O.rope_reposition(x, p1, p2, theta)
+    assert np.allclose(y, O.rope_rotate(x, p2 - p1, theta), atol=1e-10)
+    assert np.allclose(O.rope_reposition(x, p1, p1, theta), x, atol=1e-12)
+    a, b = O.rope_pairs(d, 0)
+    assert np.allclose(y[:, a] ** 2 + y[:, b] ** 2, x[:, a] ** 2 + x[:, b] ** 2, atol=1e-10)
+
+
+def test_reposition_removes_position_offset_error():
+    """K cached at offline positions and repositioned to online positions equals K rotated
+    at the online positions directly, so attention scores only see relative positions."""
+    rng = np.random.default_rng(3)
+    d, theta = 64, 1e4
+    k_raw = rng.standard_normal((300, d))
+    q_raw = rng.standard_normal((5, d))
+    p_off = np.arange(300)
+    p_on = 7000 + np.arange(300)
+    cached = O.rope_rotate(k_raw, p_off, theta)
+    moved = O.rope_reposition(cached, p_off, p_on, theta)
+    direct = O.rope_rotate(k_raw, p_on, theta)
+    assert np.allclose(moved, direct, atol=1e-10)
+    qpos = np.array([7300, 7301, 7302, 7303, 7304])
+    q = O.rope_rotate(q_raw, qpos, theta)
+    # <R(a) q, R(b) k> = <q, R(b - a) k>
+    lhs = q @ moved.T
+    rhs = np.stack([q_raw[i] @ O.rope_rotate(k_raw, p_on - qpos[i], theta).T for i in range(5)])
+    assert np.allclose(lhs, rhs, atol=1e-9)
+
+
+def test_paged_rope_reposition_follows_tables():
+    w = synth.tiny_prefill()
+    r = w.rope
+    pages, slots, rows = O.paged_rope_reposition(r.k_src, r.src_tables, r.dst_tables, r.runs, w.theta, r.P)
+    assert len(pages) == r.total_tok
+    # every destination row is written once
+    assert len(set(zip(pages.tolist(), slots.tolist()))) == len(pages)
+    # the run with delta 0 (segment 0 stays at 0..255) gives back its source rows: to fp64
+    # rounding of the two rotations, and exactly once stored as bf16
+    run = r.runs[0]
+    assert run[4] == run[5] == 0
+    src_bits = r.k_src[r.src_tables[run[0] + np.arange(256) // 16], np.arange(256) % 16]
+    assert np.allclose(rows[:256], O.bf16_to_f64(src_bits), rtol=0, atol=1e-12)
+    assert np.array_equal(O.f64_to_bf16(rows[:256]), src_bits)
+
+
+# ------------------------------------------------------------------ page tables / visibility
+def test_vllm_worked_example_block_table():
+    g = _load("vllm_block_table.json")
+    for tok in g["tokens"]:
+        assert O.token_to_physical(g["block_table"], g["block_size"], tok["t"]) == (tok["physical"], tok["slot"])
+    used = set(g["block_table"])
+    assert sorted(set(range(g["n_physical_blocks"])) - used) == g["free_blocks"]
+
+
+@pytest.mark.parametrize("case", _load("visibility_cases.json")["cases"], ids=lambda c: c["name"])
+def test_visibility_hand_cases(case):
+    listed = O.listed_positions(np.array(case["listed_pages"]), len(case["listed_pages"]), case["P"])
+    got = O.visible_set(case["cls"], case["W"], case["S"], case["seq_len"], case["p"], listed)
+    assert got.tolist() == case["visible"]
+
+
+def _small_batch(cls_row, window_row, seed=7, P=16, ctx=300, suffix=37, Hq=4, Hkv=2, d=32):
+    rng = np.random.default_rng(seed)
+    return synth._build("t", rng, B=1, Hq=Hq, Hkv=Hkv, d=d, P=P, theta=1e4, ctx_len=[ctx],
+                        n_suffix=[suffix], classes=[cls_row], windows=[window_row],
+                        sinks=[[0] * Hkv], seg_tokens=[128]).attn
+
+
+def _outs(batch):
+    return O.segpaged_attention(batch)
+
+
+def test_local_with_huge_window_equals_global():
+    a = _small_batch([O.GLOBAL, O.LOCAL], [0, 10 ** 6])
+    res = _outs(a)
+    b = dataclasses.replace(a, head_class=np.array([O.GLOBAL, O.GLOBAL], np.int32))
+    res2 = _outs(b)
+    for key in res:
+        assert np.array_equal(res[key][0], res2[key][0])
+
+
+def test_retrieval_with_full_list_equals_global():
+    a = _small_batch([O.RETRIEVAL, O.GLOBAL], [0, 0])
+    res = _outs(a)
+    b = dataclasses.replace(a, head_class=np.array([O.GLOBAL, O.GLOBAL], np.int32))
+    for key, v in _outs(b).items():
+        assert np.array_equal(res[key][0], v[0])
+
+
+def test_physical_page_permutation_invariance():
+    a = _small_batch([O.GLOBAL, O.LOCAL], [0, 40])
+    res = _outs(a)
+    rng = np.random.default_rng(11)
+    n = a.k_pool.shape[0]
+    perm = rng.permutation(n)                       # new position of each old page
+    inv = np.empty(n, np.int64)
+    inv[perm] = np.arange(n)
+    k2 = a.k_pool[inv]
+    v2 = a.v_pool[inv]
+    tab2 = np.where(a.page_table >= 0, perm[np.maximum(a.page_table, 0)], -1).astype(np.int32)
+    b = dataclasses.replace(a, k_pool=k2, v_pool=v2, page_table=tab2)
+    for key, v in _outs(b).items():
+        assert np.array_equal(res[key][0], v[0]) and np.array_equal(res[key][1], v[1])
+
+
+# ------------------------------------------------------------------ attention
+def test_single_visible_key_returns_its_value():
+    rng = np.random.default_rng(4)
+    q, k, v = rng.standard_normal((3, 16)), rng.standard_normal((1, 16)), rng.standard_normal((1, 16))
+    o, lse = O.softmax_attention(q, k, v, 0.25)
+    assert np.allclose(o, np.repeat(v, 3, 0), atol=1e-15)
+    assert np.allclose(lse, (q @ k.T)[:, 0] * 0.25, atol=1e-15)
+
+
+def test_identical_keys_give_mean_of_values():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((4, 8))
+    k = np.repeat(rng.standard_normal((1, 8)), 10, 0)
+    v = rng.standard_normal((10, 8))
+    o, lse = O.softmax_attention(q, k, v, 1.0)
+    assert np.allclose(o, np.repeat(v.mean(0, keepdims=True), 4, 0), atol=1e-14)
+    assert np.allclose(lse, (q @ k[:1].T)[:, 0] + math.log(10), atol=1e-13)
+
+
+def test_zero_query_gives_mean_of_values():
+    rng = np.random.default_rng(6)
+    k, v = rng.standard_normal((50, 8)), rng.standard_normal((50, 8))
+    o, _ = O.softmax_attention(np.zeros((2, 8)), k, v, 0.3)
+    assert np.allclose(o, np.repeat(v.mean(0, keepdims=True), 2, 0), atol=1e-14)
+
+
+def test_two_scalar_keys_logistic_closed_form():
+    # d = 1, two keys: weight of key 0 is the logistic function of the score difference
+    q, k, v = np.array([[1.5]]), np.array([[2.0], [-1.0]]), np.array([[3.0], [5.0]])
+    o, lse = O.softmax_attention(q, k, v, 1.0)
+    w0 = 1.0 / (1.0 + math.exp(-(3.0 - (-1.5))))
+    assert abs(o[0, 0] - (w0 * 3.0 + (1 - w0) * 5.0)) < 1e-15
+    assert abs(lse[0] - math.log(math.exp(3.0) + math.exp(-1.5))) < 1e-15
+
+
+def test_segpaged_attention_matches_torch_sdpa_with_mask():
+    """Library cross-check: torch's scaled_dot_product_attention in float64 with an explicit
+    boolean mask (the masked path the pages say SegPagedAttention avoids) on the same keys."""
+    a = _small_batch([O.GLOBAL, O.LOCAL], [0, 50], suffix=41)
+    res = _outs(a)
+    G = a.Hq // a.Hkv
+    L = int(a.seq_len[0])
+    nq = a.total_q
+    for h in range(a.Hkv):
+        seg = h
+        pos = np.arange(L)
+        k = O.gather_rows(a.k_pool, a.page_table[seg], a.page_logical[seg], int(a.n_pages[seg]), a.P, pos)
+        v = O.gather_rows(a.v_pool, a.page_table[seg], a.page_logical[seg], int(a.n_pages[seg]), a.P, pos)
+        qpos = L - nq + np.arange(nq)
+        mask = pos[None, :] <= qpos[:, None]
+        if a.head_class[seg] == O.LOCAL:
+            mask &= pos[None, :] > qpos[:, None] - a.window[seg]
+        q = O.bf16_to_f64(a.q[:, h * G:(h + 1) * G])                       # [nq, G, d]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q).permute(1, 0, 2), torch.from_numpy(k)[None].expand(G, -1, -1),
+            torch.from_numpy(v)[None].expand(G, -1, -1), attn_mask=torch.from_numpy(mask)[None],
+            scale=1.0 / math.sqrt(a.d)).permute(1, 0, 2).numpy()
+        for t in range(nq):
+            assert np.allclose(res[(t, h)][0], ref[t], atol=1e-12)
+
+
+def test_split_combine_equals_unsplit():
+    rng = np.random.default_rng(8)
+    q, k, v = rng.standard_normal((4, 32)), rng.standard_normal((1000, 32)), rng.standard_normal((1000, 32))
+    o, lse = O.softmax_attention(q, k, v, 0.2)
+    for bounds in ([0, 1000], [0, 1, 999, 1000], [0, 300, 300, 650, 1000]):
+        oc, lc = O.combine_partials(O.split_partials(q, k, v, 0.2, bounds))
+        assert np.allclose(oc, o, atol=1e-13) and np.allclose(lc, lse, atol=1e-12)
+
+
+def test_attention_flops_tiny_hand_count():
+    # queries at 512..543; global head sees p+1 keys, local head (W=64) sees 64; 2 q heads per KV head
+    pairs = sum(p + 1 for p in range(512, 544)) + 32 * 64
+    assert O.attention_flops(synth.tiny_prefill().attn) == 4 * 64 * 2 * pairs == 9707520
