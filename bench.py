@@ -1,0 +1,485 @@
+#!/usr/bin/env python3
+"""Benchmark of the RoPE-repositioning + SegPagedAttention hot path on B300.
+
+Workload (default): the 128K long-context layer stack -- 8 layers of 64 query / 8 KV
+heads, head dim 128, page 16; context of 131072 tokens made of 32 reusable segments of
+4096 tokens whose cached K is repositioned (RoPE) to its online offsets; a 1024-token
+suffix prefill per layer; then 64 decode steps over all 8 layers.  (layer, KV head)
+classes: exactly 3 of 64 global, the rest local with window 512.  All inputs are seeded
+synthetic bf16 N(0, 1) data (workloads/synth.py).
+
+One step = for every layer: rk_rope_reposition, rk_segpaged_prefill; then 64 x 8
+rk_segpaged_decode.  The step is captured once in a CUDA graph and replayed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  See the design notes for the field definitions.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SegPaged prefill TFLOP/s & decode KV-read GB/s on 1 B300, % of roofline"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--decode-steps", type=int, default=64)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-queries", type=int, default=48)
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(args):
+    return {
+        "workload": "stack128k: %d layers x (64 q / 8 KV heads, d 128, page 16), context 131072 = 32 segments x 4096 "
+                    "repositioned, 1024-token suffix prefill, %d decode steps; 3 of 64 (layer, KV head) global, "
+                    "rest local window 512" % (args.layers, args.decode_steps),
+        "layers": args.layers, "context": 131072, "segments": 32, "segment_tokens": 4096, "suffix": 1024,
+        "decode_steps": args.decode_steps, "Hq": 64, "Hkv": 8, "head_dim": 128, "page": 16, "theta": 1e6,
+        "l2": "inputs larger than L2 (about 0.8 GB of pools per layer, re-read every step)",
+        "parallelism": "replicas",
+    }
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- reference arm
+def _oracle_sample(layer_wl, n_queries, seed):
+    """Rows (query token, KV head) sampled from a layer: n_queries spread tokens x all KV heads."""
+    a = layer_wl.attn
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(a.total_q, size=min(n_queries, a.total_q), replace=False))
+    return [(int(t), h) for t in toks for h in range(a.Hkv)]
+
+
+def _sample_flops(batch, rows):
+    from head_aware_paged_rope_b300 import roofline
+    import dataclasses
+    G = batch.Hq // batch.Hkv
+    tot = 0
+    cnt = roofline._visible_counts(batch, lambda b: [int(batch.seq_len[b]) - batch.total_q + t for t in range(batch.total_q)])
+    for t, h in rows:
+        tot += int(cnt[(0, h)][t])
+    return 4 * batch.d * G * tot
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def oracle_step(layer_wl, rows, n_rope_tok):
+    """One bounded oracle pass: RoPE of one run prefix plus attention of the sampled rows."""
+    from oracle import rk_oracle as O
+    r = layer_wl.rope
+    run = r.runs[:1].copy()
+    run[0, 6] = min(int(run[0, 6]), n_rope_tok)
+    t0 = time.perf_counter()
+    O.paged_rope_reposition(r.k_src, r.src_tables, r.dst_tables, run, layer_wl.theta, r.P, r.style)
+    O.segpaged_attention(layer_wl.attn, rows)
+    return time.perf_counter() - t0
+
+
+def reference_main(args, world, rank):
+    if rank != 0:
+        return 0
+    from workloads import synth
+    classes = synth.stack_classes(n_layers=args.layers)
+    layer = next((l for l, c in enumerate(classes) if 0 in c), 0)
+    wl = synth.stack_layer(layer, n_layers=args.layers, n_decode=0)
+    rows = _oracle_sample(wl, max(4, args.cpu_sample_queries // 6), 17)
+    flops = _sample_flops(wl.attn, rows)
+    for _ in range(args.warmup):
+        oracle_step(wl, rows, 256)
+    times = [oracle_step(wl, rows, 256) for _ in range(args.steps)]
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    cores = _blas_threads()
+    sample = (f"layer {layer} (holds a global head): attention of {len(rows) // wl.attn.Hkv} query tokens x 8 KV heads "
+              f"(x 8 query heads each) over their visible keys, plus RoPE of 256 tokens of one run, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+class LayerState:
+    """Device inputs, outputs and prebuilt C-ABI argument structs of one layer."""
+
+    def __init__(self, rk, wl, dev, n_dec, torch):
+        from workloads.device import attn_to_device, rope_to_device, to_device
+        self.wl = wl
+        a = wl.attn
+        self.rope = rope_to_device(wl.rope, dev)
+        self.attn = attn_to_device(a, dev)
+        self.rope_ws = torch.empty(rk.rope_workspace_size(wl.rope.n_runs, a.d), dtype=torch.uint8, device=dev)
+        rr = self.rope
+        self.rope_args = rk.RopeArgs(
+            k_src=rr.k_src.data_ptr(), n_src_pages=rr.k_src.shape[0], k_dst=self.attn.k_pool.data_ptr(),
+            n_dst_pages=self.attn.k_pool.shape[0], src_tables=rr.src_tables.data_ptr(),
+            n_src_entries=rr.src_tables.numel(), dst_tables=rr.dst_tables.data_ptr(),
+            n_dst_entries=rr.dst_tables.numel(), runs=rr.runs.data_ptr(), n_runs=rr.runs.shape[0],
+            max_tok=rr.max_tok, P=a.P, d=a.d, theta=rr.theta, style=rr.style, status=None)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.prefill_args = self.attn.args(rk, status=self.status)
+        self.prefill_ws = torch.empty(max(1, rk.segpaged_prefill_workspace_size(self.prefill_args)), dtype=torch.uint8,
+                                      device=dev)
+        # decode: one query per step at position seq_len + s
+        self.n_dec = n_dec
+        self.dec_q = to_device(wl.decode_q[:n_dec].reshape(n_dec, a.Hq, a.d), dev) if n_dec else None
+        self.dec_seq = torch.tensor([[int(a.seq_len[0]) + s + 1] for s in range(n_dec)], dtype=torch.int32, device=dev)
+        self.dec_out = torch.empty((n_dec, a.Hq, a.d), dtype=torch.bfloat16, device=dev)
+        self.dec_lse = torch.empty((n_dec, a.Hq), dtype=torch.float32, device=dev)
+        self.dec_args = []
+        for s in range(n_dec):
+            da = self.attn
+            self.dec_args.append(rk.AttnArgs(
+                q=self.dec_q[s].data_ptr(), cu_seqlens_q=None, seq_len=self.dec_seq[s].data_ptr(),
+                k_pool=da.k_pool.data_ptr(), v_pool=da.v_pool.data_ptr(), n_pool_pages=da.k_pool.shape[0],
+                page_table=da.page_table.data_ptr(), page_logical=da.page_logical.data_ptr(),
+                n_pages=da.n_pages.data_ptr(), head_class=da.head_class.data_ptr(), window=da.window.data_ptr(),
+                sink=da.sink.data_ptr(), B=1, Hq=a.Hq, Hkv=a.Hkv, d=a.d, P=a.P, max_pages=da.page_table.shape[1],
+                total_q=1, max_q=1, scale=0.0, out=self.dec_out[s].data_ptr(), lse=self.dec_lse[s].data_ptr(),
+                status=self.status.data_ptr()))
+        self.dec_ws = torch.empty(max(1, rk.segpaged_decode_workspace_size(self.dec_args[0])) if n_dec else 1,
+                                  dtype=torch.uint8, device=dev)
+
+    # host copies for the end-to-end leg: (device tensor, pinned host tensor) pairs
+    def host_inputs(self, torch):
+        pairs = []
+        d = self.attn
+        for t in (self.rope.k_src, self.rope.src_tables, self.rope.dst_tables, self.rope.runs, d.q, d.cu_seqlens_q,
+                  d.seq_len, d.k_pool, d.v_pool, d.page_table, d.page_logical, d.n_pages, d.head_class, d.window,
+                  d.sink, self.dec_q, self.dec_seq):
+            if t is None:
+                continue
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            pairs.append((t, h))
+        return pairs
+
+    def host_outputs(self, torch):
+        pairs = []
+        for t in (self.attn.out, self.attn.lse, self.dec_out, self.dec_lse):
+            pairs.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
+        return pairs
+
+
+def _call(fn, args_struct, ws, stream_handle):
+    code = fn(ctypes.byref(args_struct), ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(stream_handle))
+    if code != 0:
+        raise RuntimeError(f"librk call failed with status {code}")
+
+
+def enqueue(rk, layers, stream_handle, phase):
+    n = 0
+    if phase in ("step", "rope", "prefill"):
+        for L in layers:
+            if phase in ("step", "rope"):
+                _call(rk.LIB.rk_rope_reposition, L.rope_args, L.rope_ws, stream_handle)
+                n += 2
+            if phase in ("step", "prefill"):
+                _call(rk.LIB.rk_segpaged_prefill, L.prefill_args, L.prefill_ws, stream_handle)
+                n += 3
+    if phase in ("step", "decode"):
+        n_dec = layers[0].n_dec
+        for s in range(n_dec):
+            for L in layers:
+                _call(rk.LIB.rk_segpaged_decode, L.dec_args[s], L.dec_ws, stream_handle)
+                n += 3
+    return n
+
+
+def capture(torch, rk, layers, phase, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        enqueue(rk, layers, stream.cuda_stream, phase)           # eager warm-up (sets kernel attributes)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        n = enqueue(rk, layers, torch.cuda.current_stream().cuda_stream, phase)
+    torch.cuda.synchronize()
+    return g, n
+
+
+def time_graph(torch, g, stream, steps, warmup):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def ours_main(args, world, rank, local):
+    import torch
+    import head_aware_paged_rope_b300 as rk
+    from head_aware_paged_rope_b300 import roofline
+    from workloads import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peaks_src = load_peaks()
+
+    t_gen = time.time()
+    layers = []
+    flops_prefill = flops_decode = 0
+    bytes_rope = bytes_decode = 0
+    per_layer_prefill_flops = []
+    for l in range(args.layers):
+        wl = synth.stack_layer(l, n_layers=args.layers, n_decode=args.decode_steps)
+        fp = roofline.attention_flops(wl.attn)
+        per_layer_prefill_flops.append(fp)
+        flops_prefill += fp
+        bytes_rope += roofline.rope_bytes(wl.rope)
+        for s in range(args.decode_steps):
+            d = synth.decode_batch_from(wl, s)
+            flops_decode += roofline.attention_flops(d)
+            bytes_decode += roofline.decode_kv_bytes(d)
+        layers.append(LayerState(rk, wl, dev, args.decode_steps, torch))
+        del wl
+    torch.cuda.synchronize()
+    t_gen = time.time() - t_gen
+
+    stream = torch.cuda.Stream(device=dev)
+    g_step, launches_per_step = capture(torch, rk, layers, "step", stream)
+    for L in layers:
+        L.status.zero_()
+    # correctness guard: the device status word of every call must stay clear
+    g_step.replay()
+    torch.cuda.synchronize()
+    bad = [int(L.status.item()) for L in layers if int(L.status.item()) != 0]
+    if bad:
+        raise RuntimeError(f"device status {bad}")
+
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    ms_step = time_graph(torch, g_step, stream, args.steps, 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # per-phase timing (each phase captured alone and replayed)
+    parts = {}
+    for phase in ("rope", "prefill", "decode"):
+        g, n = capture(torch, rk, layers, phase, stream)
+        ms = time_graph(torch, g, stream, max(3, args.steps // 2), args.warmup)
+        parts[phase] = {"ms": ms, "launches": n}
+        del g
+    parts["rope"].update({"GB/s": bytes_rope / (parts["rope"]["ms"] * 1e-3) / 1e9, "bytes": bytes_rope,
+                          "calls": args.layers})
+    parts["prefill"].update({"TFLOP/s": flops_prefill / (parts["prefill"]["ms"] * 1e-3) / 1e12, "flops": flops_prefill,
+                             "calls": args.layers})
+    parts["decode"].update({"GB/s": bytes_decode / (parts["decode"]["ms"] * 1e-3) / 1e9, "bytes": bytes_decode,
+                            "TFLOP/s": flops_decode / (parts["decode"]["ms"] * 1e-3) / 1e12,
+                            "calls": args.layers * args.decode_steps})
+    parts["rope"]["frac_hbm"] = parts["rope"]["GB/s"] / peaks["hbm_gbs"]
+    parts["decode"]["frac_hbm"] = parts["decode"]["GB/s"] / peaks["hbm_gbs"]
+    parts["prefill"]["frac_bf16_burst"] = parts["prefill"]["TFLOP/s"] / peaks["bf16_tflops"]
+    parts["prefill"]["frac_bf16_sustained"] = parts["prefill"]["TFLOP/s"] / peaks["bf16_tflops_sustained"]
+
+    dom = max(("rope", "prefill", "decode"), key=lambda k: parts[k]["ms"])
+    if dom == "prefill":
+        roof = {"kernel": "rk_segpaged_prefill (plan + attention + combine)", "bound": "tensor",
+                "achieved": parts["prefill"]["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        key = "GB/s"
+        roof = {"kernel": {"rope": "rk_rope_reposition", "decode": "rk_segpaged_decode (plan + split-KV + combine)"}[dom],
+                "bound": "hbm", "achieved": parts[dom][key], "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = peaks_src + (" (burst)" if roof["bound"] == "tensor" else " (copy)")
+
+    step_flops = flops_prefill + flops_decode
+    value = step_flops * world / (ms_step * 1e-3) / 1e12
+
+    # end-to-end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        ins, outs = [], []
+        for L in layers:
+            ins += L.host_inputs(torch)
+            outs += L.host_outputs(torch)
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
+        d2h = sum(h.numel() * h.element_size() for _, h in outs)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for dt, ht in ins:
+                    dt.copy_(ht, non_blocking=True)
+            g_step.replay()
+            with torch.cuda.stream(stream):
+                for dt, ht in outs:
+                    ht.copy_(dt, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": step_flops * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": args.e2e_steps}
+        del ins, outs
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        classes = synth.stack_classes(n_layers=args.layers)
+        layer = next((l for l, c in enumerate(classes) if 0 in c), 0)
+        wl = synth.stack_layer(layer, n_layers=args.layers, n_decode=0)
+        rows = _oracle_sample(wl, args.cpu_sample_queries, 17)
+        fl = _sample_flops(wl.attn, rows)
+        secs = oracle_step(wl, rows, 4096)
+        cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+               "sample": f"layer {layer} (holds a global head): attention of {len(rows) // wl.attn.Hkv} query tokens "
+                         f"x 8 KV heads (x 8 query heads each) + RoPE of one 4096-token run; {secs:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1) K/V/q, seeded page "
+                "permutations and head classes; no dataset)", "config": workload_config(args),
+                "parts": parts, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+                "setup_s": round(t_gen, 1)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return reference_main(args, world, rank)
+    return ours_main(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

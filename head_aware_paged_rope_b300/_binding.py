@@ -1,0 +1,172 @@
+"""ctypes binding of librk (include/rk_api.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; this module only turns torch
+tensors into device pointers and sizes, allocates the caller-side workspace with torch
+and raises on a non-OK status.  The library must have been built
+(`python -m head_aware_paged_rope_b300.build`); importing this module without it fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librk.so")
+
+RK_OK, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED, RK_ERR_CUDA, RK_ERR_DEVICE_BOUNDS, RK_ERR_TIMEOUT, RK_ERR_WORKSPACE = range(7)
+RK_CLASS_GLOBAL, RK_CLASS_LOCAL, RK_CLASS_RETRIEVAL, RK_CLASS_DENSE = range(4)
+RK_ROPE_HALF_SPLIT, RK_ROPE_INTERLEAVED = 0, 1
+
+
+class RkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+class RopeRun(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("src_tab_off", "src_tab_len", "dst_tab_off", "dst_tab_len", "pos_off0", "pos_on0", "n_tok", "reserved")]
+
+
+class RopeArgs(ctypes.Structure):
+    _fields_ = [
+        ("k_src", ctypes.c_void_p), ("n_src_pages", ctypes.c_int64),
+        ("k_dst", ctypes.c_void_p), ("n_dst_pages", ctypes.c_int64),
+        ("src_tables", ctypes.c_void_p), ("n_src_entries", ctypes.c_int64),
+        ("dst_tables", ctypes.c_void_p), ("n_dst_entries", ctypes.c_int64),
+        ("runs", ctypes.c_void_p), ("n_runs", ctypes.c_int32), ("max_tok", ctypes.c_int32),
+        ("P", ctypes.c_int32), ("d", ctypes.c_int32), ("theta", ctypes.c_double),
+        ("style", ctypes.c_int32), ("status", ctypes.c_void_p),
+    ]
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p), ("seq_len", ctypes.c_void_p),
+        ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("n_pool_pages", ctypes.c_int64),
+        ("page_table", ctypes.c_void_p), ("page_logical", ctypes.c_void_p), ("n_pages", ctypes.c_void_p),
+        ("head_class", ctypes.c_void_p), ("window", ctypes.c_void_p), ("sink", ctypes.c_void_p),
+        ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("P", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
+def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"librk.so not built at {path}; run python -m head_aware_paged_rope_b300.build")
+    lib = ctypes.CDLL(path)
+    lib.rk_rope_workspace_size.restype = ctypes.c_size_t
+    lib.rk_rope_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    lib.rk_rope_reposition.restype = ctypes.c_int
+    lib.rk_rope_reposition.argtypes = [ctypes.POINTER(RopeArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    for name in ("rk_segpaged_prefill_workspace_size", "rk_segpaged_decode_workspace_size"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_size_t
+        f.argtypes = [ctypes.POINTER(AttnArgs)]
+    for name in ("rk_segpaged_prefill", "rk_segpaged_decode"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.rk_status_string.restype = ctypes.c_char_p
+    lib.rk_status_string.argtypes = [ctypes.c_int]
+    lib.rk_version.restype = ctypes.c_int32
+    lib.rk_version.argtypes = []
+    return lib
+
+
+LIB = load_library()
+
+
+def status_string(code: int) -> str:
+    return LIB.rk_status_string(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("librk takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("librk takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return workspace
+    if workspace is not None:
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _check(code: int, where: str) -> None:
+    if code != RK_OK:
+        raise RkError(code, where)
+
+
+def rope_workspace_size(n_runs: int, d: int) -> int:
+    return int(LIB.rk_rope_workspace_size(n_runs, d))
+
+
+def rope_reposition(k_src: torch.Tensor, k_dst: torch.Tensor, src_tables: torch.Tensor, dst_tables: torch.Tensor,
+                    runs: torch.Tensor, *, max_tok: int, theta: float, style: int = RK_ROPE_HALF_SPLIT,
+                    status: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None) -> None:
+    """k_src/k_dst: [pages][P][d] bf16 pools; src/dst_tables: int32; runs: int32 [n_runs][8]."""
+    n_pages_src, P, d = k_src.shape
+    a = RopeArgs(k_src=_ptr(k_src), n_src_pages=n_pages_src, k_dst=_ptr(k_dst), n_dst_pages=k_dst.shape[0],
+                 src_tables=_ptr(src_tables), n_src_entries=src_tables.numel(), dst_tables=_ptr(dst_tables),
+                 n_dst_entries=dst_tables.numel(), runs=_ptr(runs), n_runs=runs.shape[0], max_tok=int(max_tok),
+                 P=P, d=d, theta=float(theta), style=int(style), status=_ptr(status))
+    ws = _workspace(rope_workspace_size(runs.shape[0], d), k_src.device, workspace)
+    nbytes = ws.numel() if ws is not None else 0
+    _check(LIB.rk_rope_reposition(ctypes.byref(a), _ptr(ws), nbytes, _stream(stream)), "rk_rope_reposition")
+
+
+def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, head_class, window, sink, out,
+              *, cu_seqlens_q=None, lse=None, status=None, total_q: int, max_q: int, scale: float = 0.0) -> AttnArgs:
+    B = seq_len.shape[0]
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = n_pages.shape[0] // max(B, 1)
+    return AttnArgs(q=_ptr(q), cu_seqlens_q=_ptr(cu_seqlens_q), seq_len=_ptr(seq_len), k_pool=_ptr(k_pool),
+                    v_pool=_ptr(v_pool), n_pool_pages=k_pool.shape[0], page_table=_ptr(page_table),
+                    page_logical=_ptr(page_logical), n_pages=_ptr(n_pages), head_class=_ptr(head_class),
+                    window=_ptr(window), sink=_ptr(sink), B=B, Hq=Hq, Hkv=Hkv, d=d, P=k_pool.shape[1],
+                    max_pages=page_table.shape[1], total_q=int(total_q), max_q=int(max_q), scale=float(scale),
+                    out=_ptr(out), lse=_ptr(lse), status=_ptr(status))
+
+
+def segpaged_prefill_workspace_size(args: AttnArgs) -> int:
+    return int(LIB.rk_segpaged_prefill_workspace_size(ctypes.byref(args)))
+
+
+def segpaged_decode_workspace_size(args: AttnArgs) -> int:
+    return int(LIB.rk_segpaged_decode_workspace_size(ctypes.byref(args)))
+
+
+def segpaged_prefill(args: AttnArgs, *, device=None, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    n = segpaged_prefill_workspace_size(args)
+    ws = _workspace(n, device or torch.device("cuda"), workspace)
+    _check(LIB.rk_segpaged_prefill(ctypes.byref(args), _ptr(ws), ws.numel() if ws is not None else 0,
+                                   _stream(stream)), "rk_segpaged_prefill")
+
+
+def segpaged_decode(args: AttnArgs, *, device=None, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    n = segpaged_decode_workspace_size(args)
+    ws = _workspace(n, device or torch.device("cuda"), workspace)
+    _check(LIB.rk_segpaged_decode(ctypes.byref(args), _ptr(ws), ws.numel() if ws is not None else 0,
+                                  _stream(stream)), "rk_segpaged_decode")
+
+
+def version() -> int:
+    return int(LIB.rk_version())

@@ -1,0 +1,224 @@
+// C-ABI entry points of librk: argument validation, workspace layout, launches.
+// The computations themselves are described in include/rk_api.h and in the kernel files.
+#include "rk_internal.cuh"
+
+#include <algorithm>
+#include <cmath>
+
+namespace rk {
+
+int prefill_mma_rows();
+int prefill_mma_keys();
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+namespace {
+
+bool supported_dp(int d, int P) { return (d == 64 || d == 128) && (P == 16 || P == 32); }
+
+// Sizes shared by the workspace-size functions and the entry points.
+struct AttnLayout {
+  int rows;         // rows per unit (query tile rows, or G for decode)
+  int tok_per_unit;
+  int max_units;
+  int max_items;
+  size_t off_units, off_items, off_lse, off_o, off_prefix, total;
+};
+
+rk_status check_attn(const rk_attn_args* a, bool decode) {
+  if (!a) return RK_ERR_INVALID_ARG;
+  if (a->B < 0 || a->Hq <= 0 || a->Hkv <= 0 || a->max_pages < 0 || a->total_q < 0 || a->max_q < 0 ||
+      a->n_pool_pages < 0)
+    return RK_ERR_INVALID_ARG;
+  if (a->Hq % a->Hkv != 0) return RK_ERR_INVALID_ARG;
+  if (!supported_dp(a->d, a->P)) return RK_ERR_UNSUPPORTED;
+  const int G = a->Hq / a->Hkv;
+  if (G > 16 || (G & (G - 1)) != 0) return RK_ERR_UNSUPPORTED;
+  if (decode) {
+    if (a->total_q != a->B || (a->B > 0 && a->max_q != 1)) return RK_ERR_INVALID_ARG;
+  } else {
+    if (a->max_q > a->total_q) return RK_ERR_INVALID_ARG;
+    if (a->B > 0 && !a->cu_seqlens_q) return RK_ERR_INVALID_ARG;
+  }
+  if (a->B == 0 || a->total_q == 0) return RK_OK;
+  if (!a->q || !a->seq_len || !a->k_pool || !a->v_pool || !a->n_pages || !a->head_class ||
+      !a->window || !a->out)
+    return RK_ERR_INVALID_ARG;
+  if (a->max_pages > 0 && !a->page_table) return RK_ERR_INVALID_ARG;
+  if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
+  return RK_OK;
+}
+
+AttnLayout attn_layout(const rk_attn_args* a, bool decode) {
+  AttnLayout l{};
+  const int G = a->Hq / a->Hkv;
+  if (decode) {
+    l.rows = G;
+    l.tok_per_unit = 1;
+    l.max_units = a->B * a->Hkv;
+  } else {
+    l.rows = prefill_mma_rows();
+    l.tok_per_unit = l.rows / G;
+    const int64_t tiles = (int64_t(a->total_q) + l.tok_per_unit - 1) / l.tok_per_unit + a->B;
+    l.max_units = int(std::min<int64_t>(tiles * a->Hkv, int64_t(1) << 30));
+  }
+  l.max_items = l.max_units + kTargetItems;
+  size_t off = align256(sizeof(PlanHeader));
+  l.off_units = off;
+  off += align256(sizeof(Unit) * size_t(l.max_units));
+  l.off_items = off;
+  off += align256(sizeof(Item) * size_t(l.max_items));
+  l.off_lse = off;
+  off += align256(sizeof(float) * size_t(l.max_items) * l.rows);
+  l.off_o = off;
+  off += sizeof(float) * size_t(l.max_items) * l.rows * a->d;   // tile prefix follows directly
+  l.off_prefix = off;
+  off += align256(sizeof(int32_t) * size_t(a->B + 1));
+  l.total = off;
+  return l;
+}
+
+AttnParams make_params(const rk_attn_args* a, const AttnLayout& l) {
+  AttnParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.cu_seqlens_q = a->cu_seqlens_q;
+  p.seq_len = a->seq_len;
+  p.k_pool = static_cast<const __nv_bfloat16*>(a->k_pool);
+  p.v_pool = static_cast<const __nv_bfloat16*>(a->v_pool);
+  p.n_pool_pages = a->n_pool_pages;
+  p.page_table = a->page_table;
+  p.page_logical = a->page_logical;
+  p.n_pages = a->n_pages;
+  p.head_class = a->head_class;
+  p.window = a->window;
+  p.sink = a->sink;
+  p.B = a->B; p.Hq = a->Hq; p.Hkv = a->Hkv; p.d = a->d; p.P = a->P;
+  p.max_pages = a->max_pages; p.total_q = a->total_q; p.max_q = a->max_q;
+  p.G = a->Hq / a->Hkv;
+  p.tok_per_unit = l.tok_per_unit;
+  const float scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt(float(a->d));
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(a->out);
+  p.lse = a->lse;
+  p.status = a->status;
+  return p;
+}
+
+AttnWorkspace make_ws(void* base, const AttnLayout& l) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  AttnWorkspace ws;
+  ws.header = reinterpret_cast<PlanHeader*>(b);
+  ws.units = reinterpret_cast<Unit*>(b + l.off_units);
+  ws.items = reinterpret_cast<Item*>(b + l.off_items);
+  ws.part_lse = reinterpret_cast<float*>(b + l.off_lse);
+  ws.part_o = reinterpret_cast<float*>(b + l.off_o);
+  ws.max_units = l.max_units;
+  ws.max_items = l.max_items;
+  ws.rows = l.rows;
+  return ws;
+}
+
+rk_status check_ws(void* ws, size_t bytes, size_t need) {
+  if (need == 0) return RK_OK;
+  if (!ws || bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RK_ERR_WORKSPACE;
+  return RK_OK;
+}
+
+rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cudaStream_t stream, bool decode) {
+  rk_status st = check_attn(a, decode);
+  if (st != RK_OK) return st;
+  if (a->B == 0 || a->total_q == 0) return RK_OK;
+  const AttnLayout l = attn_layout(a, decode);
+  st = check_ws(workspace, bytes, l.total);
+  if (st != RK_OK) return st;
+  const AttnParams p = make_params(a, l);
+  const AttnWorkspace ws = make_ws(workspace, l);
+  const int sms = device_sm_count();
+  cudaError_t e;
+  if (decode) {
+    const int grid = std::max(1, std::min(l.max_items, sms * 4));
+    e = launch_plan(p, ws, 1, 1, std::min(kTargetItems, grid * 2), 4, true, stream);
+    if (e == cudaSuccess) e = launch_decode(p, ws, grid, stream);
+  } else {
+    const int grid = std::max(1, std::min(l.max_items, sms * 2));
+    const int ept = prefill_mma_keys() / a->P;
+    e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 4, false, stream);
+    if (e == cudaSuccess) e = launch_prefill_mma(p, ws, grid, stream);
+  }
+  if (e == cudaSuccess) e = launch_combine(p, ws, decode, stream);
+  return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace rk
+
+extern "C" {
+
+size_t rk_rope_workspace_size(int32_t n_runs, int32_t d) {
+  if (n_runs < 0 || d <= 0) return 0;
+  return rk::align256(sizeof(float4) * size_t(n_runs) * size_t(d / 2));
+}
+
+rk_status rk_rope_reposition(const rk_rope_args* a, void* workspace, size_t workspace_bytes, rk_stream_t stream) {
+  if (!a) return RK_ERR_INVALID_ARG;
+  if (a->n_runs < 0 || a->max_tok < 0 || a->n_src_pages < 0 || a->n_dst_pages < 0 || a->n_src_entries < 0 ||
+      a->n_dst_entries < 0)
+    return RK_ERR_INVALID_ARG;
+  if (!rk::supported_dp(a->d, a->P)) return RK_ERR_UNSUPPORTED;
+  if (a->style != RK_ROPE_HALF_SPLIT && a->style != RK_ROPE_INTERLEAVED) return RK_ERR_UNSUPPORTED;
+  if (!(a->theta > 1.0) || !std::isfinite(a->theta)) return RK_ERR_INVALID_ARG;
+  if (a->n_runs == 0 || a->max_tok == 0) return RK_OK;
+  if (!a->k_src || !a->k_dst || !a->src_tables || !a->dst_tables || !a->runs) return RK_ERR_INVALID_ARG;
+  if (a->max_tok > 65535 * 128) return RK_ERR_UNSUPPORTED;
+  const size_t need = rk_rope_workspace_size(a->n_runs, a->d);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return RK_ERR_WORKSPACE;
+  const cudaError_t e = rk::launch_rope(*a, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+}
+
+size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* a) {
+  if (rk::check_attn(a, false) != RK_OK) return 0;
+  if (a->B == 0 || a->total_q == 0) return 0;
+  return rk::attn_layout(a, false).total;
+}
+
+size_t rk_segpaged_decode_workspace_size(const rk_attn_args* a) {
+  if (rk::check_attn(a, true) != RK_OK) return 0;
+  if (a->B == 0 || a->total_q == 0) return 0;
+  return rk::attn_layout(a, true).total;
+}
+
+rk_status rk_segpaged_prefill(const rk_attn_args* a, void* ws, size_t bytes, rk_stream_t stream) {
+  return rk::run_attention(a, ws, bytes, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+rk_status rk_segpaged_decode(const rk_attn_args* a, void* ws, size_t bytes, rk_stream_t stream) {
+  return rk::run_attention(a, ws, bytes, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+const char* rk_status_string(rk_status s) {
+  switch (s) {
+    case RK_OK: return "ok";
+    case RK_ERR_INVALID_ARG: return "invalid argument";
+    case RK_ERR_UNSUPPORTED: return "unsupported configuration";
+    case RK_ERR_CUDA: return "CUDA error";
+    case RK_ERR_DEVICE_BOUNDS: return "device-side bounds check failed";
+    case RK_ERR_TIMEOUT: return "device-side wait timed out";
+    case RK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+int32_t rk_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// Internal declarations shared by the librk CUDA sources (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "rk_api.h"
+
+namespace rk {
+
+// ------------------------------------------------------------------ device error word
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------------ bf16 helpers
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ attention work list
+// A unit is one (head segment, query tile): the queries [tok0, tok0+ntok) of one sequence
+// against one KV head.  Its visible page-list entries form at most two ranges (sink pages
+// [0, e_sink) and window/causal pages [e_w, e_w + n_vis - e_sink)); a virtual index v in
+// [0, n_vis) walks both.  An item is a contiguous slice [v_begin, v_end) of one unit.
+struct Unit {
+  int32_t seg;        // b * Hkv + h
+  int32_t tok0;       // first query token (row of q)
+  int32_t ntok;       // queries in the tile
+  int32_t pos0;       // position of query tok0
+  int32_t e_sink;     // entries [0, e_sink) are the sink range
+  int32_t e_w;        // first entry of the second range
+  int32_t n_vis;      // entries to visit
+  int32_t n_splits;   // items of this unit
+  int32_t first_item; // index of its first item
+  int32_t b;          // sequence
+  int32_t pad[2];
+};
+
+struct Item {
+  int32_t unit;
+  int32_t v_begin;
+  int32_t v_end;
+  int32_t split;
+};
+
+struct PlanHeader {
+  int32_t n_units;
+  int32_t n_items;
+  int32_t chunk;      // entries per split
+  int32_t counter;    // dynamic work counter (reset by the planner)
+  int32_t pad[60];
+};
+
+__device__ __forceinline__ int32_t unit_entry(const Unit& u, int32_t v) {
+  return v < u.e_sink ? v : u.e_w + (v - u.e_sink);
+}
+
+// Parameters common to the attention kernels (copied from rk_attn_args + derived values).
+struct AttnParams {
+  const __nv_bfloat16* q;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_len;
+  const __nv_bfloat16* k_pool;
+  const __nv_bfloat16* v_pool;
+  int64_t n_pool_pages;
+  const int32_t* page_table;
+  const int32_t* page_logical;
+  const int32_t* n_pages;
+  const int32_t* head_class;
+  const int32_t* window;
+  const int32_t* sink;
+  int32_t B, Hq, Hkv, d, P, max_pages, total_q, max_q;
+  int32_t G;           // Hq / Hkv
+  int32_t tok_per_unit;
+  float scale_log2;    // softmax scale * log2(e)
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* status;
+};
+
+// Workspace carve-up for the attention calls.
+struct AttnWorkspace {
+  PlanHeader* header;
+  Unit* units;
+  Item* items;
+  float* part_lse;     // [max_items][rows]
+  float* part_o;       // [max_items][rows][d]
+  int32_t max_units;
+  int32_t max_items;
+  int32_t rows;        // rows per unit (query tile rows or G for decode)
+};
+
+constexpr int kTargetItems = 2048;   // upper bound on items beyond one per unit
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Launchers implemented in the .cu files.
+cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int rows_per_unit,
+                        int entries_per_tile, int target_items, int min_chunk_tiles,
+                        bool decode, cudaStream_t stream);
+cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, bool decode,
+                           cudaStream_t stream);
+cudaError_t launch_prefill_mma(const AttnParams& p, const AttnWorkspace& ws, int grid,
+                               cudaStream_t stream);
+cudaError_t launch_decode(const AttnParams& p, const AttnWorkspace& ws, int grid,
+                          cudaStream_t stream);
+cudaError_t launch_rope(const rk_rope_args& a, void* workspace, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace rk

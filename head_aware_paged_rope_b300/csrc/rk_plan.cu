@@ -1,0 +1,257 @@
+// Work planning and split-KV combine for SegPagedAttention.
+//
+// The visible key set of a query tile against one KV head is read straight off that
+// head's page list ("RedKnot" article, SegPagedAttention paragraph: the table records
+// which pages the head reads).  The planner turns every (query tile, KV head) unit into
+// at most two ranges of list entries -- sink pages and the causal / window pages -- by
+// binary search on the ascending logical page numbers, then cuts the units into items
+// of about equal size so that a persistent grid stays busy whatever the mix of head
+// classes.  Items of one unit are merged afterwards with the usual log-sum-exp rule.
+#include "rk_internal.cuh"
+
+#include <algorithm>
+
+namespace rk {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// first entry e in [0, n) with logical(e) >= x
+__device__ int lower_bound_lp(const int32_t* row, int n, int x) {
+  if (!row) return min(max(x, 0), n);
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(row + mid) < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// first entry e in [0, n) with logical(e) > x
+__device__ __forceinline__ int upper_bound_lp(const int32_t* row, int n, int x) {
+  return lower_bound_lp(row, n, x + 1);
+}
+
+// Block-wide exclusive scan of one int per thread; returns the prefix, writes the total.
+__device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;   // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  const int base = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWorkspace ws, int tok_per_unit,
+                                                            int entries_per_tile, int target_items,
+                                                            int min_chunk_tiles, int decode,
+                                                            int32_t* tile_prefix) {
+  __shared__ int s_warp[32];
+  __shared__ unsigned long long s_total_entries;
+  __shared__ int s_chunk;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_total_entries = 0ull;
+
+  // 1. query tiles per sequence and their prefix (units are enumerated as (tile, KV head))
+  int carry = 0;
+  for (int base = 0; base < p.B; base += kPlanThreads) {
+    const int b = base + tid;
+    int tiles = 0;
+    if (b < p.B) {
+      const int nq = decode ? 1 : (__ldg(p.cu_seqlens_q + b + 1) - __ldg(p.cu_seqlens_q + b));
+      tiles = nq > 0 ? (nq + tok_per_unit - 1) / tok_per_unit : 0;
+    }
+    int total;
+    const int pre = block_exclusive_scan(tiles, &total, s_warp);
+    if (b < p.B) tile_prefix[b] = carry + pre;
+    carry += total;
+  }
+  if (tid == 0) tile_prefix[p.B] = carry;
+  __syncthreads();
+  const int n_tiles = carry;
+  int n_units = n_tiles * p.Hkv;
+  if (n_units > ws.max_units) {  // cannot happen with the sizes the host validated
+    if (tid == 0) report(p.status, RK_ERR_DEVICE_BOUNDS);
+    n_units = ws.max_units;
+  }
+
+  // 2. visible entry ranges of every unit
+  unsigned long long my_entries = 0;
+  for (int u = tid; u < n_units; u += kPlanThreads) {
+    const int tile_g = u / p.Hkv, h = u - (u / p.Hkv) * p.Hkv;
+    int lo = 0, hi = p.B;   // last b with tile_prefix[b] <= tile_g
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_prefix[mid] <= tile_g) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int tile = tile_g - tile_prefix[b];
+    const int seg = b * p.Hkv + h;
+    const int q0 = decode ? b : __ldg(p.cu_seqlens_q + b);
+    const int nq = decode ? 1 : (__ldg(p.cu_seqlens_q + b + 1) - q0);
+    const int L = __ldg(p.seq_len + b);
+    Unit un;
+    un.seg = seg;
+    un.b = b;
+    un.tok0 = q0 + tile * tok_per_unit;
+    un.ntok = min(tok_per_unit, nq - tile * tok_per_unit);
+    un.pos0 = L - nq + tile * tok_per_unit;
+    un.e_sink = 0;
+    un.e_w = 0;
+    un.n_vis = 0;
+    int n = __ldg(p.n_pages + seg);
+    if (n < 0 || n > p.max_pages) { report(p.status, RK_ERR_DEVICE_BOUNDS); n = 0; }
+    if (q0 < 0 || nq < 0 || int64_t(q0) + nq > p.total_q) {   // queries outside q / out
+      report(p.status, RK_ERR_DEVICE_BOUNDS);
+      un.ntok = 0;
+      n = 0;
+    }
+    const int p_first = un.pos0, p_last = un.pos0 + un.ntok - 1;
+    if (L > 0 && p_last >= 0 && n > 0) {
+      const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
+      const int cap = min(p_last, L - 1);
+      const int e_hi = upper_bound_lp(lrow, n, cap / p.P);
+      const int cls = __ldg(p.head_class + seg);
+      if (cls == RK_CLASS_LOCAL) {
+        const int W = __ldg(p.window + seg);
+        const int S = p.sink ? __ldg(p.sink + seg) : 0;
+        const int start = max(0, p_first - W + 1);
+        int e_w = min(lower_bound_lp(lrow, n, start / p.P), e_hi);
+        int e_s = S > 0 ? min(upper_bound_lp(lrow, n, (S - 1) / p.P), e_hi) : 0;
+        if (e_s >= e_w) { e_s = 0; e_w = 0; }
+        un.e_sink = e_s;
+        un.e_w = e_w;
+        un.n_vis = e_s + (e_hi - e_w);
+      } else {
+        un.n_vis = e_hi;
+      }
+    }
+    ws.units[u] = un;
+    my_entries += (unsigned long long)un.n_vis;
+  }
+  atomicAdd(&s_total_entries, my_entries);
+  __syncthreads();
+
+  // 3. chunk size: about target_items items overall, whole key tiles, at least min_chunk_tiles
+  if (tid == 0) {
+    const unsigned long long total = s_total_entries;
+    long long c = (long long)((total + target_items - 1) / (unsigned long long)max(target_items, 1));
+    c = max(c, (long long)min_chunk_tiles * entries_per_tile);
+    c = ((c + entries_per_tile - 1) / entries_per_tile) * entries_per_tile;
+    s_chunk = (int)min(c, (long long)(1 << 30));
+  }
+  __syncthreads();
+  const int chunk = s_chunk;
+
+  // 4. items
+  carry = 0;
+  for (int base = 0; base < n_units; base += kPlanThreads) {
+    const int u = base + tid;
+    int ns = 0;
+    if (u < n_units) {
+      const int nv = ws.units[u].n_vis;
+      ns = nv > 0 ? (nv + chunk - 1) / chunk : 1;
+    }
+    int total;
+    const int pre = block_exclusive_scan(ns, &total, s_warp);
+    if (u < n_units) {
+      const int first = carry + pre;
+      ws.units[u].n_splits = ns;
+      ws.units[u].first_item = first;
+      const int nv = ws.units[u].n_vis;
+      for (int s = 0; s < ns; ++s) {
+        const int it = first + s;
+        if (it >= ws.max_items) { report(p.status, RK_ERR_DEVICE_BOUNDS); break; }
+        Item item;
+        item.unit = u;
+        item.v_begin = s * chunk;
+        item.v_end = min(nv, (s + 1) * chunk);
+        item.split = s;
+        ws.items[it] = item;
+      }
+    }
+    carry += total;
+  }
+  if (tid == 0) {
+    ws.header->n_units = n_units;
+    ws.header->n_items = min(carry, ws.max_items);
+    ws.header->chunk = chunk;
+    ws.header->counter = 0;
+  }
+}
+
+// Merge the split partials of each unit: lse = log sum_s e^{lse_s}, o = sum_s e^{lse_s - lse} o_s.
+// One warp per query row.
+__global__ __launch_bounds__(256) void combine_kernel(AttnParams p, AttnWorkspace ws) {
+  const int n_units = ws.header->n_units;
+  const int warps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const Unit un = ws.units[u];
+    if (un.n_splits <= 1 || un.first_item + un.n_splits > ws.max_items) continue;
+    const int rows = un.ntok * G;
+    const int h = un.seg % p.Hkv;
+    for (int r = warp; r < rows; r += warps) {
+      float m = -INFINITY;
+      for (int s = 0; s < un.n_splits; ++s)
+        m = fmaxf(m, ws.part_lse[int64_t(un.first_item + s) * ws.rows + r]);
+      float wsum = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int per_lane = p.d / 32;   // 2 or 4
+      for (int s = 0; s < un.n_splits; ++s) {
+        const int64_t it = un.first_item + s;
+        const float l = ws.part_lse[it * ws.rows + r];
+        const float w = (m == -INFINITY) ? 0.f : expf(l - m);
+        wsum += w;
+        const float* po = ws.part_o + (it * ws.rows + r) * p.d + lane * per_lane;
+        for (int c = 0; c < per_lane; ++c) acc[c] += w * po[c];
+      }
+      const int t = un.tok0 + r / G;
+      const int hq = h * G + (r % G);
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+      __nv_bfloat16* o = p.out + (int64_t(t) * p.Hq + hq) * p.d + lane * per_lane;
+      for (int c = 0; c < per_lane; ++c) o[c] = __float2bfloat16_rn(acc[c] * inv);
+      if (p.lse && lane == 0) p.lse[int64_t(t) * p.Hq + hq] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int tok_per_unit,
+                        int entries_per_tile, int target_items, int min_chunk_tiles, bool decode,
+                        cudaStream_t stream) {
+  // the tile prefix lives right after the partial outputs (sized by the host)
+  int32_t* tile_prefix = reinterpret_cast<int32_t*>(ws.part_o + int64_t(ws.max_items) * ws.rows * p.d);
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, ws, tok_per_unit, entries_per_tile, target_items,
+                                              min_chunk_tiles, decode ? 1 : 0, tile_prefix);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, bool decode, cudaStream_t stream) {
+  const int grid = std::max(1, std::min(ws.max_units, device_sm_count() * 4));
+  combine_kernel<<<grid, 256, 0, stream>>>(p, ws);
+  (void)decode;
+  return cudaGetLastError();
+}
+
+}  // namespace rk

@@ -1,0 +1,195 @@
+/*
+ * rk_api.h -- C ABI of librk: RoPE repositioning of cached K and SegPagedAttention
+ * (per-head paged attention without an attention mask) on NVIDIA B300 (sm_103a).
+ *
+ * What the calls compute, and where the RedKnot pages state it:
+ *
+ *  - rk_rope_reposition: "RedKnot" article (is96.com), paragraphs on RoPE and on the
+ *    correction RedKnot applies to reused KV: K of a reusable segment was cached with
+ *    the rotation of its offline position; the call turns it back by that rotation and
+ *    forward by the rotation of its online position.  "小红书 RedKnot" product page,
+ *    section 3, second component (offline KV reuse + RoPE repositioning).
+ *  - rk_segpaged_prefill / rk_segpaged_decode: "小红书 RedKnot", section 3, fourth
+ *    component (SegPagedAttention: an own page table per head, segmented KV storage, a
+ *    different visible window per head class, no attn_mask); "RedKnot" article,
+ *    SegPagedAttention paragraph (each head segment's table records which pages the
+ *    head reads); head classes from section 3, first component (global, local,
+ *    retrieval, dense); page pool and block tables from "PagedAttention &
+ *    RadixAttention", section "The Solution: Fixed-size blocks".
+ *
+ * Conventions common to every call
+ *  - bf16 tensors are passed as `void*` to 2-byte elements (IEEE bfloat16 bit patterns).
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, except the
+ *    argument struct itself, which is read on the host during the call only.
+ *  - The library never allocates device memory and never synchronises.  Work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).  Scratch
+ *    memory is the caller's `workspace`, sized by the matching *_workspace_size call;
+ *    its contents need no initialisation and are undefined afterwards.
+ *  - Host-side validation happens before anything is enqueued; on an error nothing is
+ *    enqueued.  Checks that need device data (page ids inside the pool, slots inside a
+ *    table) run in the kernels: a failing access is skipped and RK_ERR_DEVICE_BOUNDS
+ *    is written to `*status` (when `status` is non-NULL; the first error code wins, the
+ *    caller zeroes the word and reads it after synchronising).
+ *  - Page pools are [n_pages][P][d] bf16, d contiguous; page id p refers to the same
+ *    page index in the K pool and in the V pool.  P in {16, 32}; d in {64, 128}.
+ *  - A head segment is one (sequence b, KV head h) pair with index b*Hkv + h.
+ */
+#ifndef RK_API_H
+#define RK_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RK_API __attribute__((visibility("default")))
+#else
+#define RK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* rk_stream_t; /* same type as cudaStream_t */
+
+typedef enum rk_status {
+  RK_OK = 0,
+  RK_ERR_INVALID_ARG = 1,    /* host-side validation failed; nothing enqueued */
+  RK_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. d or P outside the sets above) */
+  RK_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
+  RK_ERR_DEVICE_BOUNDS = 4,  /* device-side check: page id / slot / table index out of range */
+  RK_ERR_TIMEOUT = 5,        /* device-side bounded wait gave up */
+  RK_ERR_WORKSPACE = 6       /* workspace NULL, misaligned (256 B) or smaller than required */
+} rk_status;
+
+/* Head classes ("小红书 RedKnot", section 3, first component). */
+enum { RK_CLASS_GLOBAL = 0, RK_CLASS_LOCAL = 1, RK_CLASS_RETRIEVAL = 2, RK_CLASS_DENSE = 3 };
+
+/* Channel pairing of the rotation: (i, i + d/2) or (2i, 2i + 1). */
+enum { RK_ROPE_HALF_SPLIT = 0, RK_ROPE_INTERLEAVED = 1 };
+
+/* ------------------------------------------------------------------------------------
+ * RoPE repositioning
+ *
+ * One run moves n_tok consecutive tokens of one head segment.  Token t (0 <= t < n_tok)
+ *   - is read from the offline store: logical slot s = pos_off0 + t of the run's source
+ *     table, i.e. row (src_tables[src_tab_off + s / P], s % P) of k_src;
+ *   - is written to the online pool: logical slot u = pos_on0 + t of the run's
+ *     destination table, i.e. row (dst_tables[dst_tab_off + u / P], u % P) of k_dst;
+ *   - is rotated, for every channel pair i < d/2, back by pos_off * w_i and forward by
+ *     pos_on * w_i, with w_i = theta^(-2i/d), pos_off = pos_off0 + t, pos_on = pos_on0 + t.
+ * Since both positions advance together the two rotations compose into one turn by
+ * (pos_on0 - pos_off0) * w_i, which is what the kernel applies; its cos/sin are taken
+ * in double precision and the product is formed in fp32 with a split (hi + lo)
+ * coefficient, so the bf16 result is within 1 bf16 ulp of the exact rotation.
+ * Output is rounded to bf16 (round to nearest even).
+ * ------------------------------------------------------------------------------------ */
+typedef struct rk_rope_run {
+  int32_t src_tab_off; /* first entry of this run's table inside src_tables */
+  int32_t src_tab_len; /* entries of that table (bounds: (pos_off0+n_tok-1)/P < len) */
+  int32_t dst_tab_off; /* first entry of this run's table inside dst_tables */
+  int32_t dst_tab_len;
+  int32_t pos_off0;    /* offline position of token 0, >= 0 */
+  int32_t pos_on0;     /* online position of token 0, >= 0 */
+  int32_t n_tok;       /* >= 0 */
+  int32_t reserved;    /* unused, set to 0 */
+} rk_rope_run;
+
+typedef struct rk_rope_args {
+  const void* k_src;          /* bf16 [n_src_pages][P][d], offline store (read only) */
+  int64_t n_src_pages;
+  void* k_dst;                /* bf16 [n_dst_pages][P][d], online pool (rows written) */
+  int64_t n_dst_pages;
+  const int32_t* src_tables;  /* int32 [n_src_entries] physical page ids */
+  int64_t n_src_entries;
+  const int32_t* dst_tables;  /* int32 [n_dst_entries] physical page ids */
+  int64_t n_dst_entries;
+  const rk_rope_run* runs;    /* [n_runs] run descriptors (device memory) */
+  int32_t n_runs;
+  int32_t max_tok;            /* host-known upper bound of runs[i].n_tok (sizes the grid) */
+  int32_t P;                  /* tokens per page: 16 or 32 */
+  int32_t d;                  /* head dim: 64 or 128 */
+  double theta;               /* RoPE base, > 1 */
+  int32_t style;              /* RK_ROPE_HALF_SPLIT or RK_ROPE_INTERLEAVED */
+  int32_t* status;            /* optional device int32 error word, may be NULL */
+} rk_rope_args;
+
+/* Bytes of workspace rk_rope_reposition needs (per-run rotation coefficients). */
+RK_API size_t rk_rope_workspace_size(int32_t n_runs, int32_t d);
+
+/* Enqueue the repositioning of every run.  Rows of different runs must not overlap in
+ * k_dst, and k_dst may alias k_src only when every token reads and writes the very same
+ * row (in-place update).  Errors: RK_ERR_INVALID_ARG (NULL pointers with n_runs > 0,
+ * negative sizes, theta <= 1 or not finite), RK_ERR_UNSUPPORTED (P, d, style, or max_tok
+ * above 8388480), RK_ERR_WORKSPACE, RK_ERR_CUDA.  On the device, a run with n_tok > max_tok
+ * or a negative position, a table slot beyond its run's table or the table array, or a
+ * page id outside its pool sets RK_ERR_DEVICE_BOUNDS and the affected rows are skipped. */
+RK_API rk_status rk_rope_reposition(const rk_rope_args* args, void* workspace, size_t workspace_bytes,
+                             rk_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * SegPagedAttention
+ *
+ * For query token t of sequence b (position p = seq_len[b] - nq_b + i for its i-th
+ * query, nq_b = cu_seqlens_q[b+1] - cu_seqlens_q[b]) and query head hq, read KV head
+ * h = hq / (Hq / Hkv) of head segment s = b*Hkv + h.  Its visible keys are
+ *     V = { j : logical page j / P is listed in page_logical[s][0 .. n_pages[s]),
+ *               j < seq_len[b], j <= p,
+ *               and, when head_class[s] == RK_CLASS_LOCAL, j > p - window[s] or j < sink[s] }
+ * (global, retrieval and dense heads differ only in which pages they list).  Key j is
+ * row (page_table[s][e], j % P) of k_pool / v_pool for the entry e listing page j / P.
+ *     out[t][hq][:] = sum_{j in V} softmax_j(scale * q[t][hq] . k_j) v_j      (bf16)
+ *     lse[t][hq]    = log sum_{j in V} exp(scale * q[t][hq] . k_j)             (fp32)
+ * An empty visible set gives out = 0 and lse = -inf.  Accumulation is fp32; the
+ * probabilities enter the value product as bf16.
+ * ------------------------------------------------------------------------------------ */
+typedef struct rk_attn_args {
+  const void* q;               /* bf16 [total_q][Hq][d] */
+  const int32_t* cu_seqlens_q; /* int32 [B+1], prefix sums of queries per sequence; decode: NULL (one query each) */
+  const int32_t* seq_len;      /* int32 [B], context length including the queries */
+  const void* k_pool;          /* bf16 [n_pool_pages][P][d] */
+  const void* v_pool;          /* bf16 [n_pool_pages][P][d] */
+  int64_t n_pool_pages;
+  const int32_t* page_table;   /* int32 [B*Hkv][max_pages] physical page of each listed entry */
+  const int32_t* page_logical; /* int32 [B*Hkv][max_pages] strictly ascending logical page of each
+                                  entry, or NULL: entry e is logical page e */
+  const int32_t* n_pages;      /* int32 [B*Hkv] listed entries, 0 <= n <= max_pages */
+  const int32_t* head_class;   /* int32 [B*Hkv] RK_CLASS_* */
+  const int32_t* window;       /* int32 [B*Hkv] local window W >= 1 (read for local heads) */
+  const int32_t* sink;         /* int32 [B*Hkv] sink length S >= 0, or NULL for all zero */
+  int32_t B, Hq, Hkv, d, P, max_pages;
+  int32_t total_q;             /* host-known: cu_seqlens_q[B] (decode: B) */
+  int32_t max_q;               /* host-known: max nq_b (decode: 1) */
+  float scale;                 /* softmax scale; <= 0 selects 1/sqrt(d) */
+  void* out;                   /* bf16 [total_q][Hq][d] */
+  float* lse;                  /* fp32 [total_q][Hq] or NULL */
+  int32_t* status;             /* optional device int32 error word, may be NULL */
+} rk_attn_args;
+
+/* Bytes of workspace rk_segpaged_prefill / rk_segpaged_decode need for these sizes
+ * (work list plus split-KV partial results).  Returns 0 for invalid sizes. */
+RK_API size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* args);
+RK_API size_t rk_segpaged_decode_workspace_size(const rk_attn_args* args);
+
+/* Prefill: any number of queries per sequence (a suffix at the end of the context).
+ * Errors: RK_ERR_INVALID_ARG (NULL pointers, B/Hq/Hkv/max_pages/total_q < 0, Hq % Hkv,
+ * max_q > total_q), RK_ERR_UNSUPPORTED (d, P, Hq/Hkv > 16), RK_ERR_WORKSPACE, RK_ERR_CUDA. */
+RK_API rk_status rk_segpaged_prefill(const rk_attn_args* args, void* workspace, size_t workspace_bytes,
+                              rk_stream_t stream);
+
+/* Decode: one query per sequence at position seq_len[b] - 1 (q is [B][Hq][d]); split-KV
+ * over each head's visible pages, partial results merged by log-sum-exp.  Same errors. */
+RK_API rk_status rk_segpaged_decode(const rk_attn_args* args, void* workspace, size_t workspace_bytes,
+                             rk_stream_t stream);
+
+/* Static text for a status code. */
+RK_API const char* rk_status_string(rk_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+RK_API int32_t rk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RK_API_H */

@@ -1,0 +1,106 @@
+"""CPU-side checks of the C ABI: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rk_api.h")
+LIB = os.path.join(ROOT, "head_aware_paged_rope_b300", "librk.so")
+
+
+@pytest.fixture(scope="module")
+def rk():
+    from head_aware_paged_rope_b300 import build as b
+    b.build()
+    import head_aware_paged_rope_b300 as m
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"RK_API\s+[\w\s\*]+?\b(rk_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("rk_rope_reposition", "rk_segpaged_prefill", "rk_segpaged_decode", "rk_rope_workspace_size",
+              "rk_segpaged_prefill_workspace_size", "rk_segpaged_decode_workspace_size", "rk_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(rk):
+    lib = ctypes.CDLL(LIB)
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(rk):
+    assert rk.status_string(0) == "ok"
+    assert "bounds" in rk.status_string(4)
+    assert rk.status_string(99) == "unknown status"
+
+
+def _rope_args(rk, **kw):
+    base = dict(k_src=1, n_src_pages=1, k_dst=1, n_dst_pages=1, src_tables=1, n_src_entries=1, dst_tables=1,
+                n_dst_entries=1, runs=1, n_runs=1, max_tok=16, P=16, d=128, theta=1e6, style=0, status=None)
+    base.update(kw)
+    return rk.RopeArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), 2), (dict(P=8), 2), (dict(style=3), 2), (dict(theta=1.0), 1), (dict(theta=float("nan")), 1),
+    (dict(n_runs=-1), 1), (dict(max_tok=-5), 1), (dict(k_src=None), 1), (dict(runs=None), 1),
+])
+def test_rope_host_validation(rk, kw, code):
+    a = _rope_args(rk, **kw)
+    assert rk.LIB.rk_rope_reposition(ctypes.byref(a), None, 0, None) == code
+
+
+def test_rope_nothing_to_do_and_workspace(rk):
+    a = _rope_args(rk, n_runs=0)
+    assert rk.LIB.rk_rope_reposition(ctypes.byref(a), None, 0, None) == 0
+    a = _rope_args(rk)
+    assert rk.LIB.rk_rope_reposition(ctypes.byref(a), None, 0, None) == 6          # workspace missing
+    assert rk.rope_workspace_size(48, 128) == 48 * 64 * 16
+    assert rk.rope_workspace_size(-1, 128) == 0
+
+
+def _attn_args(rk, **kw):
+    base = dict(q=1, cu_seqlens_q=1, seq_len=1, k_pool=1, v_pool=1, n_pool_pages=10, page_table=1, page_logical=None,
+                n_pages=1, head_class=1, window=1, sink=None, B=2, Hq=8, Hkv=2, d=128, P=16, max_pages=4,
+                total_q=10, max_q=5, scale=0.0, out=1, lse=None, status=None)
+    base.update(kw)
+    return rk.AttnArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=6, Hkv=4), 1), (dict(d=80), 2), (dict(P=64), 2), (dict(Hq=64, Hkv=2), 2), (dict(Hq=24, Hkv=8), 2),
+    (dict(B=-1), 1), (dict(max_q=11), 1), (dict(cu_seqlens_q=None), 1), (dict(q=None), 1), (dict(out=None), 1),
+    (dict(scale=float("inf")), 1),
+])
+def test_prefill_host_validation(rk, kw, code):
+    a = _attn_args(rk, **kw)
+    assert rk.LIB.rk_segpaged_prefill(ctypes.byref(a), None, 0, None) == code
+
+
+def test_decode_host_validation(rk):
+    a = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1)
+    assert rk.segpaged_decode_workspace_size(a) > 0
+    assert rk.LIB.rk_segpaged_decode(ctypes.byref(a), None, 0, None) == 6           # workspace missing
+    a = _attn_args(rk, cu_seqlens_q=None, total_q=3, max_q=1)                       # decode needs total_q == B
+    assert rk.LIB.rk_segpaged_decode(ctypes.byref(a), None, 0, None) == 1
+
+
+def test_attention_empty_batch_is_ok(rk):
+    a = _attn_args(rk, B=0, total_q=0, max_q=0)
+    assert rk.LIB.rk_segpaged_prefill(ctypes.byref(a), None, 0, None) == 0
+    assert rk.segpaged_prefill_workspace_size(a) == 0
+
+
+def test_workspace_size_grows_with_queries(rk):
+    small = rk.segpaged_prefill_workspace_size(_attn_args(rk, total_q=10))
+    big = rk.segpaged_prefill_workspace_size(_attn_args(rk, total_q=10000, max_q=5000))
+    assert 0 < small < big

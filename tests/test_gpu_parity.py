@@ -1,0 +1,296 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
+seeded inputs.
+
+Tolerances (stated for this path):
+  * RoPE-repositioned K: at most 1 bf16 ulp from the correctly rounded fp64 result.
+  * attention output (bf16): max-abs error <= 3e-2 and relative L2 error <= 5e-3 over the
+    compared rows; lse (fp32): abs error <= 1e-3 (fp32 accumulation of up to ~1.3e5
+    exponentials whose relative error is below 1e-6).
+  * everything that is index work (which rows are written, unchanged rows, page
+    permutations) is compared bit for bit.
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import rk_oracle as O
+from workloads import synth
+from workloads.device import attn_to_device, bf16_bits, rope_to_device, to_device
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL_L2, LSE_TOL = 3e-2, 5e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def rk():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from head_aware_paged_rope_b300 import build as b
+    b.build()
+    import head_aware_paged_rope_b300 as m
+    return m
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _gpu_rope(rk, w, k_pool_bits=None):
+    dr = rope_to_device(w.rope, "cuda")
+    kp = to_device(w.attn.k_pool if k_pool_bits is None else k_pool_bits, "cuda")
+    st = _status()
+    dr.run(rk, kp, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return kp
+
+
+def _check_rope(w, got_pool_bits):
+    r = w.rope
+    pages, slots, rows = O.paged_rope_reposition(r.k_src, r.src_tables, r.dst_tables, r.runs, w.theta, r.P, r.style)
+    ref = O.f64_to_bf16(rows)
+    got = got_pool_bits[pages, slots]
+    ulp = np.abs(O.bf16_ordinal(got) - O.bf16_ordinal(ref))
+    assert ulp.max() <= 1, f"max ulp {ulp.max()}"
+    assert (ulp == 0).mean() > 0.999
+    untouched = np.ones(got_pool_bits.shape[:2], dtype=bool)
+    untouched[pages, slots] = False
+    assert np.array_equal(got_pool_bits[untouched], w.attn.k_pool[untouched])
+    return O.apply_rope_to_pool(w.attn.k_pool, (pages, slots, rows))
+
+
+def _gpu_attn(rk, batch, decode=False, k_pool=None, use_logical=True):
+    da = attn_to_device(batch, "cuda", k_pool=k_pool)
+    st = _status()
+    args = da.args(rk, decode=decode, status=st, use_logical=use_logical)
+    (rk.segpaged_decode if decode else rk.segpaged_prefill)(args)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return da.out.float().cpu().numpy(), da.lse.cpu().numpy()
+
+
+def _compare(batch, out, lse, rows=None):
+    ref = O.segpaged_attention(batch, rows)
+    G = batch.Hq // batch.Hkv
+    got_o, ref_o, got_l, ref_l = [], [], [], []
+    for (t, h), (o, l) in ref.items():
+        got_o.append(out[t, h * G:(h + 1) * G])
+        ref_o.append(o)
+        got_l.append(lse[t, h * G:(h + 1) * G])
+        ref_l.append(l)
+    go, ro = np.concatenate(got_o), np.concatenate(ref_o)
+    gl, rl = np.concatenate(got_l), np.concatenate(ref_l)
+    err = np.abs(go - ro)
+    rel = np.linalg.norm(go - ro) / max(np.linalg.norm(ro), 1e-30)
+    assert err.max() <= ATOL, f"max abs {err.max()}"
+    assert rel <= RTOL_L2, f"rel L2 {rel}"
+    fin = np.isfinite(rl)
+    assert np.array_equal(fin, np.isfinite(gl))
+    assert np.abs(gl[fin] - rl[fin]).max(initial=0.0) <= LSE_TOL
+    return err.max(), rel
+
+
+def _sample_rows(batch, seed, per_head=64):
+    """All rows of one global and one local KV head, plus per_head random rows of every other head."""
+    rng = np.random.default_rng(seed)
+    T = batch.total_q
+    cls = batch.head_class.reshape(batch.B, batch.Hkv)[0]
+    full = set()
+    for c in (O.GLOBAL, O.LOCAL):
+        hs = np.nonzero(cls == c)[0]
+        if len(hs):
+            full.add(int(hs[0]))
+    rows = [(t, h) for h in full for t in range(T)]
+    for h in range(batch.Hkv):
+        if h not in full:
+            rows += [(int(t), h) for t in rng.choice(T, size=min(per_head, T), replace=False)]
+    return rows
+
+
+# ------------------------------------------------------------------------- RoPE
+@pytest.mark.parametrize("style", [0, 1])
+def test_rope_tiny(rk, style):
+    w = synth.tiny_prefill(style=style)
+    _check_rope(w, bf16_bits(_gpu_rope(rk, w)))
+
+
+def test_rope_delta_zero_is_bit_exact(rk):
+    w = synth.tiny_prefill()
+    got = bf16_bits(_gpu_rope(rk, w))
+    r = w.rope.runs[0]
+    assert r[4] == r[5] == 0
+    t = np.arange(int(r[6]))
+    src = w.rope.k_src[w.rope.src_tables[r[0] + t // 16], t % 16]
+    dst = got[w.rope.dst_tables[r[2] + t // 16], t % 16]
+    assert np.array_equal(src, dst)
+
+
+def test_rope_rag_full_size_unaligned(rk):
+    w = synth.rag_prefill()          # 6 x 5000 tokens: runs start mid-page online
+    _check_rope(w, bf16_bits(_gpu_rope(rk, w)))
+
+
+def test_rope_mixed_d64_interleaved(rk):
+    rng = np.random.default_rng(5)
+    w = synth._build("m", rng, B=2, Hq=4, Hkv=4, d=64, P=32, theta=5e5, ctx_len=[700, 1300], n_suffix=[5, 9],
+                     classes=[[0, 1, 2, 3]] * 2, windows=[[0, 64, 0, 0]] * 2, sinks=[[0] * 4] * 2,
+                     seg_tokens=[333, 400], style=1)
+    _check_rope(w, bf16_bits(_gpu_rope(rk, w)))
+
+
+# ------------------------------------------------------------------------- prefill
+def test_whole_path_tiny(rk):
+    """GPU RoPE then GPU attention vs oracle RoPE (stored as bf16) then oracle attention."""
+    w = synth.tiny_prefill()
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
+    _compare(dataclasses.replace(w.attn, k_pool=oracle_pool), out, lse)
+
+
+def test_prefill_rag_small_ragged(rk):
+    w = synth.rag_prefill(n_segments=3, seg_tokens=1000, n_suffix=77)
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
+    _compare(dataclasses.replace(w.attn, k_pool=oracle_pool), out, lse)
+
+
+def test_prefill_mixed_small(rk):
+    w = synth.mixed_classes(B=4, lengths=(1024, 2048), suffix_range=(50, 200), seg_tokens=512)
+    out, lse = _gpu_attn(rk, w.attn)
+    _compare(w.attn, out, lse)
+
+
+def test_prefill_local_sink_and_window_one(rk):
+    rng = np.random.default_rng(9)
+    w = synth._build("s", rng, B=2, Hq=8, Hkv=4, d=128, P=16, theta=1e6, ctx_len=[300, 517], n_suffix=[33, 64],
+                     classes=[[1, 1, 0, 2], [1, 3, 1, 1]], windows=[[1, 40, 0, 0], [17, 0, 256, 1000]],
+                     sinks=[[3, 0, 0, 0], [20, 0, 5, 0]], seg_tokens=[128, 128])
+    out, lse = _gpu_attn(rk, w.attn)
+    _compare(w.attn, out, lse)
+
+
+def test_prefill_without_logical_table(rk):
+    """page_logical = NULL means entry e is logical page e (full lists)."""
+    w = synth.rag_prefill(n_segments=2, seg_tokens=800, n_suffix=40, Hq=16, Hkv=4)
+    out, lse = _gpu_attn(rk, w.attn, use_logical=False)
+    _compare(w.attn, out, lse)
+
+
+def test_prefill_empty_sequence_and_empty_list(rk):
+    rng = np.random.default_rng(4)
+    w = synth._build("e", rng, B=3, Hq=4, Hkv=2, d=64, P=16, theta=1e4, ctx_len=[100, 50, 80], n_suffix=[10, 0, 7],
+                     classes=[[0, 1]] * 3, windows=[[0, 30]] * 3, sinks=[[0, 0]] * 3, seg_tokens=[64] * 3)
+    a = w.attn
+    n = a.n_pages.copy()
+    n[1] = 0                                            # sequence 0, KV head 1 lists nothing
+    a = dataclasses.replace(a, n_pages=n)
+    out, lse = _gpu_attn(rk, a)
+    _compare(a, out, lse)
+    assert np.all(out[:10, 2:4] == 0) and np.all(np.isneginf(lse[:10, 2:4]))
+
+
+def test_prefill_page_permutation_bit_identical(rk):
+    w = synth.mixed_classes(B=2, lengths=(1024,), suffix_range=(60, 100), seg_tokens=512)
+    a = w.attn
+    out1, lse1 = _gpu_attn(rk, a)
+    rng = np.random.default_rng(3)
+    n = a.k_pool.shape[0]
+    perm = rng.permutation(n)
+    inv = np.empty(n, np.int64)
+    inv[perm] = np.arange(n)
+    b = dataclasses.replace(a, k_pool=a.k_pool[inv], v_pool=a.v_pool[inv],
+                            page_table=np.where(a.page_table >= 0, perm[np.maximum(a.page_table, 0)], -1).astype(np.int32))
+    out2, lse2 = _gpu_attn(rk, b)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+def test_prefill_device_bounds_check(rk):
+    """A page id outside the pool is skipped and reported through the status word."""
+    w = synth.tiny_prefill()
+    a = w.attn
+    tab = a.page_table.copy()
+    tab[0, 3] = a.k_pool.shape[0] + 5
+    da = attn_to_device(dataclasses.replace(a, page_table=tab), "cuda")
+    st = _status()
+    rk.segpaged_prefill(da.args(rk, status=st))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 4
+
+
+# ------------------------------------------------------------------------- decode
+def test_decode_microbench_full_size(rk):
+    w = synth.decode_microbench()
+    out, lse = _gpu_attn(rk, w.attn, decode=True)
+    _compare(w.attn, out, lse)
+
+
+def test_decode_small_ragged_sink(rk):
+    w = synth.decode_microbench(B=5, ctx=2001, Hq=16, Hkv=4, window=100, sink=7)
+    out, lse = _gpu_attn(rk, w.attn, decode=True)
+    _compare(w.attn, out, lse)
+
+
+def test_decode_d64_gqa2(rk):
+    w = synth.tiny_prefill()
+    a = synth.decode_batch_from(dataclasses.replace(w, decode_q=np.stack([w.attn.q[:1]] * 2)), 0)
+    a = dataclasses.replace(a, seq_len=w.attn.seq_len.copy())
+    out, lse = _gpu_attn(rk, a, decode=True)
+    _compare(a, out, lse)
+
+
+def test_stack_small_prefill_then_decode(rk):
+    w = synth.stack_layer(0, n_segments=4, seg_tokens=1024, n_suffix=100, n_decode=4)
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    a = dataclasses.replace(w.attn, k_pool=oracle_pool)
+    out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
+    _compare(a, out, lse)
+    for step in (0, 3):
+        d = synth.decode_batch_from(dataclasses.replace(w, attn=a), step)
+        out, lse = _gpu_attn(rk, d, decode=True)
+        _compare(d, out, lse)
+
+
+# ------------------------------------------------------------------------- full sizes, sampled rows
+@pytest.mark.slow
+def test_rag_prefill_full_size_sampled(rk):
+    w = synth.rag_prefill()
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
+    a = dataclasses.replace(w.attn, k_pool=oracle_pool)
+    _compare(a, out, lse, rows=_sample_rows(a, 31))
+
+
+@pytest.mark.slow
+def test_mixed_full_size_sampled(rk):
+    w = synth.mixed_classes()
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
+    a = dataclasses.replace(w.attn, k_pool=oracle_pool)
+    rng = np.random.default_rng(41)
+    rows = [(int(t), h) for t in rng.choice(a.total_q, 300, replace=False) for h in range(a.Hkv)]
+    _compare(a, out, lse, rows=rows)
+
+
+@pytest.mark.slow
+def test_stack_layer_full_size_sampled(rk):
+    classes = synth.stack_classes()
+    layer = next(l for l, c in enumerate(classes) if 0 in c)     # a layer holding a global head
+    w = synth.stack_layer(layer)
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    a = dataclasses.replace(w.attn, k_pool=oracle_pool)
+    out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
+    _compare(a, out, lse, rows=_sample_rows(a, 7, per_head=16))
+    for step in (0, 31, 63):
+        d = synth.decode_batch_from(dataclasses.replace(w, attn=a), step)
+        out, lse = _gpu_attn(rk, d, decode=True)
+        _compare(d, out, lse)

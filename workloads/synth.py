@@ -34,7 +34,9 @@ Conventions shared by both sides (data layout only):
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 from typing import List, Optional
 
 import numpy as np
@@ -45,20 +47,42 @@ RUN_FIELDS = 8  # src_tab_off, src_tab_len, dst_tab_off, dst_tab_len, pos_off0, 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 (round-to-nearest-even), as uint16 bits."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    bias = ((u >> 16) & 1) + np.uint32(0x7FFF)
-    return ((u + bias) >> 16).astype(np.uint16)
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    t = u >> 16
+    t &= 1
+    t += np.uint32(0x7FFF)
+    u += t
+    u >>= 16
+    return u.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+_CHUNK = 1 << 22          # values per independently seeded chunk (fixed: results do not depend on threads)
+_POOL = concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1))
+
+
 def _normal_bf16(rng: np.random.Generator, shape, scale=None) -> np.ndarray:
-    x = rng.standard_normal(size=shape, dtype=np.float32)
+    """bf16 N(0,1) draws.  The draw is split into fixed-size chunks, each from its own
+    PCG64 stream spawned from one seed taken from `rng`, and filled on worker threads."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    if n == 0:
+        return out.reshape(shape)
+    seeds = np.random.SeedSequence(int(rng.integers(0, 2 ** 63))).spawn((n + _CHUNK - 1) // _CHUNK)
+
+    def fill(i):
+        lo, hi = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        x = np.random.Generator(np.random.PCG64(seeds[i])).standard_normal(hi - lo, dtype=np.float32)
+        out[lo:hi] = f32_to_bf16_bits(x)
+
+    list(_POOL.map(fill, range(len(seeds))))
+    out = out.reshape(shape)
     if scale is not None:
-        x *= scale
-    return f32_to_bf16_bits(x)
+        out = f32_to_bf16_bits(bf16_bits_to_f32(out) * scale)
+    return out
 
 
 @dataclasses.dataclass
