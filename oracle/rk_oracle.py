@@ -126,14 +126,16 @@ def token_to_physical(table: Sequence[int], P: int, t: int) -> Tuple[int, int]:
 
 
 def paged_rope_reposition(k_src: np.ndarray, src_tables: np.ndarray, dst_tables: np.ndarray,
-                          runs: np.ndarray, theta: float, P: int, style: int = ROPE_HALF_SPLIT):
-    """Apply every run; returns (dst_page, dst_slot, rows): the fp64 rows written and where.
+                          runs: np.ndarray, theta: float, P: int, style: int = ROPE_HALF_SPLIT,
+                          return_inputs: bool = False):
+    """Apply every run; returns (dst_page, dst_slot, rows): the fp64 rows written and where
+    (plus the fp64 input rows when return_inputs).
 
     Run fields: src_tab_off, src_tab_len, dst_tab_off, dst_tab_len, pos_off0, pos_on0, n_tok.
     Token t of a run reads slot (pos_off0+t) of its src table and writes slot
     (pos_on0+t) of its dst table.
     """
-    pages, slots, rows = [], [], []
+    pages, slots, rows, inputs = [], [], [], []
     for r in np.asarray(runs):
         s_off, s_len, d_off, d_len, p_off0, p_on0, n = (int(v) for v in r[:7])
         if n == 0:
@@ -144,13 +146,35 @@ def paged_rope_reposition(k_src: np.ndarray, src_tables: np.ndarray, dst_tables:
         s_tab = np.asarray(src_tables[s_off:s_off + s_len], dtype=np.int64)
         d_tab = np.asarray(dst_tables[d_off:d_off + d_len], dtype=np.int64)
         x = bf16_to_f64(k_src[s_tab[p_off // P], p_off % P])
+        inputs.append(x)
         rows.append(rope_reposition(x, p_off, p_on, theta, style))
         pages.append(d_tab[p_on // P])
         slots.append(p_on % P)
     if not rows:
         d = k_src.shape[-1]
-        return np.zeros(0, np.int64), np.zeros(0, np.int64), np.zeros((0, d))
-    return np.concatenate(pages), np.concatenate(slots), np.concatenate(rows)
+        out = (np.zeros(0, np.int64), np.zeros(0, np.int64), np.zeros((0, d)))
+        return out + (np.zeros((0, d)),) if return_inputs else out
+    out = (np.concatenate(pages), np.concatenate(slots), np.concatenate(rows))
+    return out + (np.concatenate(inputs),) if return_inputs else out
+
+
+def rope_within_one_ulp(got_bits: np.ndarray, exact: np.ndarray, inputs: np.ndarray, style: int,
+                        floor_rel: float = 1e-12) -> np.ndarray:
+    """Per element: is the bf16 value within 1 bf16 ulp of the fp64 result?
+
+    The fp64 result itself carries round-off of about 1e-16 of its pair's magnitude
+    (two rotations), which near zero is any number of bf16 ulps; so an element also
+    passes when it is within floor_rel * |pair| of the fp64 value (e.g. an exact zero
+    kept at zero by a zero turn)."""
+    d = exact.shape[-1]
+    a, b = rope_pairs(d, style)
+    pair = np.sqrt(inputs[:, a] ** 2 + inputs[:, b] ** 2)
+    mag = np.empty_like(exact)
+    mag[:, a] = pair
+    mag[:, b] = pair
+    ulp_ok = np.abs(bf16_ordinal(got_bits) - bf16_ordinal(f64_to_bf16(exact))) <= 1
+    abs_ok = np.abs(bf16_to_f64(got_bits) - exact) <= floor_rel * mag
+    return ulp_ok | abs_ok
 
 
 def apply_rope_to_pool(k_pool: np.ndarray, written) -> np.ndarray:

@@ -252,3 +252,18 @@ def test_attention_flops_tiny_hand_count():
     # queries at 512..543; global head sees p+1 keys, local head (W=64) sees 64; 2 q heads per KV head
     pairs = sum(p + 1 for p in range(512, 544)) + 32 * 64
     assert O.attention_flops(synth.tiny_prefill().attn) == 4 * 64 * 2 * pairs == 9707520
+
+
+def test_rope_tolerance_floor_only_covers_fp64_roundoff():
+    # an exact zero kept at zero passes although the fp64 two-step value is ~1e-17
+    x = np.zeros((1, 4))
+    x[0, 0] = 1.0
+    exact = np.array([[1.0, 0.0, 1.4e-17, 0.0]])
+    got = np.array([[0x3F80, 0, 0, 0]], np.uint16)
+    assert O.rope_within_one_ulp(got, exact, x, O.ROPE_HALF_SPLIT).all()
+    # a real error of 2 ulps is still caught
+    got2 = np.array([[0x3F82, 0, 0, 0]], np.uint16)
+    assert not O.rope_within_one_ulp(got2, exact, x, O.ROPE_HALF_SPLIT)[0, 0]
+    # and so is a small absolute error well above the fp64 round-off
+    got3 = np.array([[0x3F80, 0, 0x2F00, 0]], np.uint16)      # 1.2e-10 where 1.4e-17 is exact
+    assert not O.rope_within_one_ulp(got3, exact, x, O.ROPE_HALF_SPLIT)[0, 2]
