@@ -4,11 +4,27 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
+#include <string>
 
 namespace rk {
 
 int prefill_mma_rows();
 int prefill_mma_keys();
+int prefill_tc_rows();
+int prefill_tc_keys();
+cudaError_t launch_prefill_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cudaStream_t stream);
+
+// The prefill kernel: tcgen05 (default) or the mma.sync baseline, the latter kept only for
+// A/B measurement (RK_PREFILL_KERNEL=mma).
+static bool use_mma_prefill() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("RK_PREFILL_KERNEL");
+    v = (e && std::string(e) == "mma") ? 1 : 0;
+  }
+  return v == 1;
+}
 
 int device_sm_count() {
   static int cache[64] = {0};
@@ -54,6 +70,8 @@ rk_status check_attn(const rk_attn_args* a, bool decode) {
       !a->window || !a->out)
     return RK_ERR_INVALID_ARG;
   if (a->max_pages > 0 && !a->page_table) return RK_ERR_INVALID_ARG;
+  if (a->n_pool_pages * int64_t(a->P) >= (int64_t(1) << 31) || int64_t(a->total_q) * a->Hq >= (int64_t(1) << 31))
+    return RK_ERR_UNSUPPORTED;   // row coordinates of the tensor maps are int32
   if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
   return RK_OK;
 }
@@ -66,7 +84,7 @@ AttnLayout attn_layout(const rk_attn_args* a, bool decode) {
     l.tok_per_unit = 1;
     l.max_units = a->B * a->Hkv;
   } else {
-    l.rows = prefill_mma_rows();
+    l.rows = use_mma_prefill() ? prefill_mma_rows() : prefill_tc_rows();
     l.tok_per_unit = l.rows / G;
     const int64_t tiles = (int64_t(a->total_q) + l.tok_per_unit - 1) / l.tok_per_unit + a->B;
     l.max_units = int(std::min<int64_t>(tiles * a->Hkv, int64_t(1) << 30));
@@ -149,10 +167,17 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
     e = launch_plan(p, ws, 1, 1, std::min(kTargetItems, grid * 2), 4, true, stream);
     if (e == cudaSuccess) e = launch_decode(p, ws, grid, stream);
   } else {
-    const int grid = std::max(1, std::min(l.max_items, sms * 2));
-    const int ept = prefill_mma_keys() / a->P;
-    e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 4, false, stream);
-    if (e == cudaSuccess) e = launch_prefill_mma(p, ws, grid, stream);
+    if (use_mma_prefill()) {
+      const int grid = std::max(1, std::min(l.max_items, sms * 2));
+      const int ept = prefill_mma_keys() / a->P;
+      e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 4, false, stream);
+      if (e == cudaSuccess) e = launch_prefill_mma(p, ws, grid, stream);
+    } else {
+      const int grid = std::max(1, std::min(l.max_items, sms));
+      const int ept = prefill_tc_keys() / a->P;
+      e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 2, false, stream);
+      if (e == cudaSuccess) e = launch_prefill_tc(p, ws, grid, stream);
+    }
   }
   if (e == cudaSuccess) e = launch_combine(p, ws, decode, stream);
   return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
