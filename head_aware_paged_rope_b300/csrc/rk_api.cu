@@ -163,9 +163,11 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
   const int sms = device_sm_count();
   cudaError_t e;
   if (decode) {
-    const int grid = std::max(1, std::min(l.max_items, sms * 4));
-    e = launch_plan(p, ws, 1, 1, std::min(kTargetItems, grid * 2), 4, true, stream);
+    const int grid = std::max(1, std::min(l.max_items, sms * decode_ctas_per_sm(a->P)));
+    e = launch_plan(p, ws, 1, 1, std::min(kTargetItems, grid), 4, true, stream);
     if (e == cudaSuccess) e = launch_decode(p, ws, grid, stream);
+    if (e == cudaSuccess) e = launch_combine_decode(p, ws, stream);
+    return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
   } else {
     if (use_mma_prefill()) {
       const int grid = std::max(1, std::min(l.max_items, sms * 2));

@@ -122,6 +122,8 @@ cudaError_t launch_prefill_mma(const AttnParams& p, const AttnWorkspace& ws, int
                                cudaStream_t stream);
 cudaError_t launch_decode(const AttnParams& p, const AttnWorkspace& ws, int grid,
                           cudaStream_t stream);
+cudaError_t launch_combine_decode(const AttnParams& p, const AttnWorkspace& ws, cudaStream_t stream);
+int decode_ctas_per_sm(int P);
 cudaError_t launch_rope(const rk_rope_args& a, void* workspace, cudaStream_t stream);
 
 int device_sm_count();

@@ -20,6 +20,11 @@ constexpr int kPlanThreads = 1024;
 // first entry e in [0, n) with logical(e) >= x
 __device__ int lower_bound_lp(const int32_t* row, int n, int x) {
   if (!row) return min(max(x, 0), n);
+  if (n <= 0) return 0;
+  const int first = __ldg(row), last = __ldg(row + n - 1);
+  if (x <= first) return 0;
+  if (x > last) return n;
+  if (last - first == n - 1) return x - first;    // contiguous run of logical pages
   int lo = 0, hi = n;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
