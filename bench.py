@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import json
 import os
 import statistics
@@ -49,6 +50,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-queries", type=int, default=48)
+    ap.add_argument("--case", choices=["rag_prefill", "stack_prefill", "decode_microbench", "stack_decode", "rag_rope"],
+                    help="run one call of one workload --steps times (for profiling) instead of the step")
     return ap.parse_args()
 
 
@@ -473,9 +476,67 @@ def ours_main(args, world, rank, local):
     return 0
 
 
+def case_main(args):
+    """One library call of one workload, repeated: a small, self-contained target for ncu.
+    Prints the average time per call measured with CUDA events."""
+    import torch
+    import head_aware_paged_rope_b300 as rk
+    from head_aware_paged_rope_b300 import roofline
+    from workloads import synth
+    from workloads.device import attn_to_device, rope_to_device, to_device
+    dev = torch.device("cuda", 0)
+    if args.case == "rag_prefill":
+        wl = synth.rag_prefill()
+    elif args.case == "stack_prefill":
+        classes = synth.stack_classes()
+        wl = synth.stack_layer(next(l for l, c in enumerate(classes) if 0 in c), n_decode=0)
+    elif args.case == "decode_microbench":
+        wl = synth.decode_microbench()
+    elif args.case == "stack_decode":
+        classes = synth.stack_classes()
+        layer_wl = synth.stack_layer(next(l for l, c in enumerate(classes) if 0 in c), n_decode=1)
+        wl = dataclasses.replace(layer_wl, attn=synth.decode_batch_from(layer_wl, 0))
+    else:
+        wl = synth.rag_prefill()
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.case == "rag_rope":
+        dr = rope_to_device(wl.rope, dev)
+        kp = to_device(wl.attn.k_pool, dev)
+        ws = torch.empty(rk.rope_workspace_size(wl.rope.n_runs, wl.attn.d), dtype=torch.uint8, device=dev)
+        call = lambda: dr.run(rk, kp, status=st, workspace=ws)
+        work, unit = roofline.rope_bytes(wl.rope) / 1e9, "GB/s"
+    else:
+        decode = args.case in ("decode_microbench", "stack_decode")
+        da = attn_to_device(wl.attn, dev)
+        a = da.args(rk, decode=decode, status=st)
+        n = (rk.segpaged_decode_workspace_size if decode else rk.segpaged_prefill_workspace_size)(a)
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        fn = rk.segpaged_decode if decode else rk.segpaged_prefill
+        call = lambda: fn(a, workspace=ws)
+        if decode:
+            work, unit = roofline.decode_kv_bytes(wl.attn) / 1e9, "GB/s"
+        else:
+            work, unit = roofline.attention_flops(wl.attn) / 1e12, "TFLOP/s"
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    print(json.dumps({"case": args.case, "ms_per_call": ms, unit: work / (ms * 1e-3)}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_setup(args)
+    if args.case:
+        return case_main(args)
     if args.impl == "reference":
         return reference_main(args, world, rank)
     return ours_main(args, world, rank, local)
