@@ -182,6 +182,26 @@ RK_API rk_status rk_segpaged_prefill(const rk_attn_args* args, void* workspace, 
 RK_API rk_status rk_segpaged_decode(const rk_attn_args* args, void* workspace, size_t workspace_bytes,
                              rk_stream_t stream);
 
+/* Decode without a caller workspace, for callers that cannot allocate device memory:
+ * plugins whose host owns all device memory and hands them no allocator, and code on a
+ * latency-critical path that must not call cudaMalloc (which can synchronise the device).
+ * The pages describe no such call; it is a deployment convenience of this library.
+ *
+ * Same arguments, computation and errors as rk_segpaged_decode; the scratch memory is a
+ * fixed device array of RK_DECODE_NOALLOC_SCRATCH_BYTES inside the library (reserved on
+ * every GPU that loads the library, until the process exits).  Calls whose
+ * rk_segpaged_decode_workspace_size exceeds it return RK_ERR_UNSUPPORTED and enqueue
+ * nothing; use rk_segpaged_decode with a workspace for those.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, once per device,
+ * with that device current), so make that first call before any stream capture.  No call
+ * allocates memory.  Every call on a device shares the one array: calls that may overlap
+ * on the GPU (different streams, or different host threads) race and must be serialised
+ * by the caller; calls on one stream are ordered.  The array keeps the last call's
+ * contents; nothing in it needs to start at zero, because each call's planning kernel
+ * rewrites the work list and resets its item counter before the decode kernel reads them. */
+#define RK_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+RK_API rk_status rk_segpaged_decode_noalloc(const rk_attn_args* args, rk_stream_t stream);
+
 /* Static text for a status code. */
 RK_API const char* rk_status_string(rk_status status);
 
