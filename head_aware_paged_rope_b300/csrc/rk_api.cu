@@ -26,6 +26,17 @@ static bool use_mma_prefill() {
   return v == 1;
 }
 
+// The decode kernel: tcgen05 (default) or the CUDA-core split-KV kernel, the latter kept for
+// A/B measurement (RK_DECODE_KERNEL=simt).
+static bool use_simt_decode() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("RK_DECODE_KERNEL");
+    v = (e && std::string(e) == "simt") ? 1 : 0;
+  }
+  return v == 1;
+}
+
 int device_sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -74,6 +85,12 @@ rk_status check_attn(const rk_attn_args* a, bool decode) {
     return RK_ERR_UNSUPPORTED;   // row coordinates of the tensor maps are int32
   if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
   return RK_OK;
+}
+
+// q, the pools and out are read and written with 16-byte vectors and TMA.
+bool aligned16(const rk_attn_args* a) {
+  const auto ok = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  return ok(a->q) && ok(a->k_pool) && ok(a->v_pool) && ok(a->out);
 }
 
 AttnLayout attn_layout(const rk_attn_args* a, bool decode) {
@@ -145,6 +162,51 @@ AttnWorkspace make_ws(void* base, const AttnLayout& l) {
   return ws;
 }
 
+// Workspace of the tcgen05 decode path.
+struct DecLayoutHost {
+  int nseg, grid, max_slots;
+  size_t off_segs, off_ctas, off_split, off_lse, off_o, total;
+};
+
+DecLayoutHost dec_layout(const rk_attn_args* a) {
+  DecLayoutHost l{};
+  const int G = a->Hq / a->Hkv;
+  l.nseg = a->B * a->Hkv;
+  l.grid = device_sm_count();
+  l.max_slots = l.nseg + l.grid;   // every CTA boundary splits at most one more segment
+  size_t off = align256(sizeof(DecHeader));
+  l.off_segs = off;
+  off += align256(sizeof(DecSeg) * size_t(l.nseg));
+  l.off_ctas = off;
+  off += align256(sizeof(DecCta) * size_t(l.grid));
+  l.off_split = off;
+  off += align256(sizeof(int32_t) * size_t(l.nseg));
+  l.off_lse = off;
+  off += align256(sizeof(float) * size_t(l.max_slots) * G);
+  l.off_o = off;
+  off += align256(sizeof(float) * size_t(l.max_slots) * G * a->d);
+  l.total = off;
+  return l;
+}
+
+DecWorkspace make_dec_ws(void* base, const DecLayoutHost& l) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  DecWorkspace ws;
+  ws.header = reinterpret_cast<DecHeader*>(b);
+  ws.segs = reinterpret_cast<DecSeg*>(b + l.off_segs);
+  ws.ctas = reinterpret_cast<DecCta*>(b + l.off_ctas);
+  ws.split_segs = reinterpret_cast<int32_t*>(b + l.off_split);
+  ws.part_lse = reinterpret_cast<float*>(b + l.off_lse);
+  ws.part_o = reinterpret_cast<float*>(b + l.off_o);
+  ws.max_slots = l.max_slots;
+  ws.grid = l.grid;
+  return ws;
+}
+
+size_t decode_ws_bytes(const rk_attn_args* a) {
+  return use_simt_decode() ? attn_layout(a, true).total : dec_layout(a).total;
+}
+
 rk_status check_ws(void* ws, size_t bytes, size_t need) {
   if (need == 0) return RK_OK;
   if (!ws || bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RK_ERR_WORKSPACE;
@@ -155,12 +217,27 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
   rk_status st = check_attn(a, decode);
   if (st != RK_OK) return st;
   if (a->B == 0 || a->total_q == 0) return RK_OK;
+  const int sms = device_sm_count();
+  if (decode && !use_simt_decode()) {
+    const DecLayoutHost dl = dec_layout(a);
+    st = check_ws(workspace, bytes, dl.total);
+    if (st != RK_OK) return st;
+    if (!aligned16(a)) return RK_ERR_INVALID_ARG;
+    AttnLayout l{};
+    l.rows = a->Hq / a->Hkv;
+    l.tok_per_unit = 1;
+    const AttnParams p = make_params(a, l);
+    const DecWorkspace ws = make_dec_ws(workspace, dl);
+    cudaError_t e = launch_plan_decode(p, ws, stream);
+    if (e == cudaSuccess) e = launch_decode_tc(p, ws, stream);
+    return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+  }
   const AttnLayout l = attn_layout(a, decode);
   st = check_ws(workspace, bytes, l.total);
   if (st != RK_OK) return st;
+  if (!aligned16(a)) return RK_ERR_INVALID_ARG;
   const AttnParams p = make_params(a, l);
   const AttnWorkspace ws = make_ws(workspace, l);
-  const int sms = device_sm_count();
   cudaError_t e;
   if (decode) {
     const int grid = std::max(1, std::min(l.max_items, sms * decode_ctas_per_sm(a->P)));
@@ -222,7 +299,7 @@ size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* a) {
 size_t rk_segpaged_decode_workspace_size(const rk_attn_args* a) {
   if (rk::check_attn(a, true) != RK_OK) return 0;
   if (a->B == 0 || a->total_q == 0) return 0;
-  return rk::attn_layout(a, true).total;
+  return rk::decode_ws_bytes(a);
 }
 
 rk_status rk_segpaged_prefill(const rk_attn_args* a, void* ws, size_t bytes, rk_stream_t stream) {

@@ -1,0 +1,725 @@
+// SegPaged decode on the 5th-generation tensor cores (tcgen05 + TMEM), sm_103a.
+//
+// What it computes is stated in include/rk_api.h: one query per sequence at position
+// seq_len - 1 attends to the keys its KV head lists in its own page table, with the
+// window / sink edge applied as a predicate ("小红书 RedKnot" section 3, fourth component;
+// "RedKnot" article, SegPagedAttention paragraph).  Decode reads every visible K/V row
+// once and is bound by HBM bandwidth ("LLM 推理原理详解": decode is memory-bound).  All G
+// query heads of a KV head share each K/V row, so the contraction runs on the tensor
+// cores with the keys on the MMA's M side, which keeps the per-row arithmetic far below
+// the memory time:
+//   S^T[key][g]  = K[key][:] . q[g][:]           M = 128 keys, N = 16 (G heads, padded), K = d
+//   O^T[c][g]   += V^T[c][key] . P^T[key][g]     M = 128 channels, N = 16, K = 128 keys
+//
+// Schedule (rk_plan.cu, plan_decode_kernel): the 128-key tiles of all head segments form
+// one sequence and CTA c takes the equal share [c*T/gs, (c+1)*T/gs) of it (gs = the
+// smaller of the grid, one CTA per SM, and T).  A share is walked as "portions" (the part of one segment inside the share).
+//   warp 4   producer: walks the share, pushes each portion into a 2-entry ring, loads its
+//            G query rows (TMA) into one of two Q buffers, and gathers each tile page by
+//            page (one TMA box per page and 64 channels) from the shared K and V pools
+//            through the page table into a ring of kStages stages.  Segment records and
+//            page ids are requested one step ahead of their use.
+//   warp 5   MMA issuer (one thread): issues whichever of S^T(j) (data landed, S buffer
+//            free) or O^T += V^T P^T (P^T written) is ready, so neither waits on the other.
+//   warps 0-3 softmax: thread t owns key t of the tile (TMEM lane t): masks it, finds the
+//            tile maximum of every head (transposing shuffle reduction, one barrier),
+//            keeps a per-head running maximum that moves only when it grows by more than
+//            2^8 (then O^T is rescaled in TMEM), writes P^T = 2^(S - m) as bf16 into shared
+//            memory, and at the end of a portion normalises O^T and stores it -- the output
+//            itself, or, for a segment shared with other CTAs, a partial result that
+//            combine_decode_tc_kernel merges by log-sum-exp.
+// Every wait is bounded; a timeout sets RK_ERR_TIMEOUT and all roles leave.
+#include "rk_internal.cuh"
+#include "rk_sm100.cuh"
+
+#include <algorithm>
+
+namespace rk {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 192;
+constexpr int kKeys = kDecTileKeys;     // keys per tile (MMA M of S^T)
+constexpr int kN = 16;                  // MMA N: query heads of the group, padded
+constexpr int kRing = 2;                // portion ring depth
+constexpr float kRescale = 8.0f;        // log2 units
+constexpr uint32_t kTmemCols = 64;      // S buffers at 0 and 16, O^T at 32
+constexpr uint32_t kColO = 32;
+constexpr int kHalfBytes = kKeys * 128; // one [128 keys][64 channels] bf16 box column
+constexpr int kGrp = 32;                // list entries whose page ids the producer warp loads at once
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+template <int D>
+struct DecLayout {
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kStageBytes = (D / 64) * kHalfBytes;     // K (or V) of one tile
+  static constexpr int kQBuf = (D / 64) * 2048;                 // [16][D] bf16, SW128 K-major
+  static constexpr int kQ = 0;                                  // 2 Q buffers
+  static constexpr int kP = kQ + 2 * kQBuf;                     // 2 x [16][128 keys] bf16
+  static constexpr int kV = kP + 2 * 4096;                      // V stages, then K stages: for D = 64
+  static constexpr int kK = kV + kStages * kStageBytes;         // V^T's second M half reads past a V stage
+  static constexpr int kBytes = kK + kStages * kStageBytes;
+  static constexpr int kSmem = kBytes + 1024;
+};
+
+// One segment's part of a CTA's share, as the producer hands it to the other roles.
+struct Portion {
+  int32_t seg, v_begin, v_end, slot;    // slot < 0: write the output directly
+  int32_t n_kt, b, tok, pos;
+  int32_t cls, W, S, L;
+};
+
+struct DecShared {
+  uint64_t kv_full[6], kv_empty[6];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], p_empty[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t iq_full[kRing], iq_empty[kRing];
+  Portion ring[kRing];
+  int lp[6][8];             // logical page of each page slot of a stage (-1: none)
+  float red[2][4][kN];      // per-warp tile maxima (double-buffered by tile parity)
+  float redl[4][kN];        // per-warp denominators
+  float lse2[kN];
+  uint32_t tmem_slot;
+  int abort;
+};
+
+__device__ __forceinline__ bool aborted(DecShared& sh) { return *reinterpret_cast<volatile int*>(&sh.abort) != 0; }
+__device__ __forceinline__ void set_abort(DecShared& sh, int32_t* status) {
+  report(status, RK_ERR_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&sh.abort) = 1;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(DecShared& sh, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (aborted(sh)) return false;
+    if (globaltimer() - t0 > kWaitNs) return false;
+  }
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ int seg_entry(const DecSeg& s, int v) { return v < s.e_sink ? v : s.e_w + (v - s.e_sink); }
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" :: "r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Reduce NG per-lane values over the 32 lanes of a warp, transposing as it goes: returns
+// the reduction of column lane / (32 / NG) (every lane of that column group holds it).
+template <int NG, bool MAX>
+__device__ __forceinline__ float warp_reduce_cols(float (&v)[NG]) {
+  int cnt = NG;
+#pragma unroll
+  for (int lvl = 0; lvl < 5; ++lvl) {
+    const int off = 16 >> lvl;
+    if (cnt > 1) {
+      const int half = cnt >> 1;
+      const bool upper = (threadIdx.x & off) != 0;
+#pragma unroll
+      for (int i = 0; i < NG / 2; ++i) {
+        if (i < half) {
+          const float keep = upper ? v[i + half] : v[i];
+          const float send = upper ? v[i] : v[i + half];
+          const float got = __shfl_xor_sync(0xffffffffu, send, off);
+          v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+      }
+      cnt = half;
+    } else {
+      const float got = __shfl_xor_sync(0xffffffffu, v[0], off);
+      v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
+    }
+  }
+  return v[0];
+}
+
+template <int D, int NG>
+__global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                                 const __grid_constant__ CUtensorMap tmK,
+                                                                 const __grid_constant__ CUtensorMap tmV,
+                                                                 AttnParams p, DecWorkspace ws) {
+  using LY = DecLayout<D>;
+  constexpr int NS = LY::kStages;
+  constexpr int HALVES = D / 64;
+  constexpr uint32_t kIdescQK = idesc_bf16(kKeys, kN, 0, 0);
+  constexpr uint32_t kIdescPV = idesc_bf16(128, kN, 0, 1);
+  constexpr uint32_t kTileTx = 2 * HALVES * kKeys * 128;   // K + V bytes of one tile
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ DecShared sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t sQ = sbase + LY::kQ, sP = sbase + LY::kP, sV = sbase + LY::kV, sK = sbase + LY::kK;
+  const int P = p.P, EPT = kKeys / P;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_addr(&sh.kv_full[s]), 1);
+      mbar_init(smem_addr(&sh.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&sh.s_full[s]), 1);
+      mbar_init(smem_addr(&sh.s_empty[s]), 128);
+      mbar_init(smem_addr(&sh.p_full[s]), 128);
+      mbar_init(smem_addr(&sh.p_empty[s]), 1);
+      mbar_init(smem_addr(&sh.q_full[s]), 1);
+      mbar_init(smem_addr(&sh.q_empty[s]), 1);
+    }
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(smem_addr(&sh.iq_full[s]), 1);
+      mbar_init(smem_addr(&sh.iq_empty[s]), 129);
+    }
+    sh.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 4 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmQ) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmK) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmV) : "memory");
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(&sh.tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp < 4) {   // Q rows >= G and P^T rows >= G stay zero for the whole kernel
+    for (int i = tid; i < (LY::kV - LY::kQ) / 16; i += 128) st_shared_v4(sQ + i * 16, make_uint4(0, 0, 0, 0));
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_slot;
+  grid_dependency_wait();      // the plan (and everything before it in the stream) is complete
+  grid_launch_dependents();    // the combine kernel may be scheduled as CTAs of this one finish
+
+  const int G = p.G;
+  const int nseg = p.B * p.Hkv;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ producer
+    const int64_t oob_row = p.n_pool_pages * P;      // a row past the pool: TMA fills zeros
+    const DecCta my = ws.ctas[blockIdx.x];
+    int seg = my.seg0, t = my.tile_begin;
+    const int t_end = my.tile_end;
+    // raw page id / logical page of entry v_begin + grp*32 + lane of segment s (present: listed)
+    auto fetch = [&](int s, const DecSeg& sd, int v_begin, int v_end, int grp, int& raw_page, int& raw_lp,
+                     bool& present) {
+      const int v = v_begin + grp * kGrp + lane;
+      present = s < nseg && v < v_end;
+      raw_page = -1;
+      raw_lp = -1;
+      if (present) {
+        const int en = seg_entry(sd, v);
+        raw_page = __ldg(p.page_table + int64_t(s) * p.max_pages + en);
+        raw_lp = p.page_logical ? __ldg(p.page_logical + int64_t(s) * p.max_pages + en) : en;
+      }
+    };
+    auto load_seg = [&](int s) {
+      DecSeg d;
+      if (s < nseg) {
+        d = ws.segs[s];
+      } else {
+        d.n_tiles = 0;
+        d.tile0 = 0x7fffffff;
+        d.n_vis = 0;
+        d.e_sink = 0;
+        d.e_w = 0;
+      }
+      return d;
+    };
+    uint32_t gg = 0, qn = 0;
+    int last_stage = -1, last_q = -1;
+    uint32_t last_parity = 0, last_q_parity = 0;
+    bool ok = true;
+    DecSeg cur = load_seg(t < t_end ? seg : nseg);
+    while (t < t_end && cur.n_tiles == 0 && seg < nseg) cur = load_seg(++seg);
+    int raw_page, raw_lp;
+    bool present;
+    fetch(seg, cur, (t < t_end && seg < nseg) ? (t - cur.tile0) * EPT : 0, cur.n_vis, 0, raw_page, raw_lp, present);
+    for (int k = 0; ok; ++k) {
+      const int slot = k % kRing;
+      if (k >= kRing) {
+        bool got = true;
+        if (lane == 0) got = wait_or_abort(sh, smem_addr(&sh.iq_empty[slot]), ((k / kRing) - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+      }
+      const bool live = t < t_end && seg < nseg;
+      Portion po;
+      int lt1 = 0;
+      if (live) {
+        const int lt0 = t - cur.tile0;
+        lt1 = min(cur.n_tiles, t_end - cur.tile0);
+        po.seg = seg;
+        po.v_begin = lt0 * EPT;
+        po.v_end = min(cur.n_vis, lt1 * EPT);
+        po.n_kt = lt1 - lt0;
+        po.slot = cur.n_splits > 1 ? cur.slot0 + (int(blockIdx.x) - cur.cta0) : -1;
+        po.b = cur.b;
+        po.tok = cur.tok;
+        po.pos = cur.pos;
+        po.cls = cur.cls;
+        po.W = cur.W;
+        po.S = cur.S;
+        po.L = cur.L;
+      } else {
+        po.seg = -1;
+        po.n_kt = 0;
+      }
+      if (lane == 0) {
+        sh.ring[slot] = po;
+        mbar_arrive(smem_addr(&sh.iq_full[slot]));
+      }
+      if (!live) break;
+      // the next segment's record, used when this portion's last group is issued
+      const bool more = cur.tile0 + lt1 < t_end;
+      int nseg_idx = seg + 1;
+      DecSeg nxt = load_seg(more ? nseg_idx : nseg);
+      {   // Q rows of the group -> buffer qn & 1, free once the MMAs of portion qn - 2 are done
+        bool got = true;
+        if (lane == 0) {
+          const int b = qn & 1;
+          if (qn >= 2) got = wait_or_abort(sh, smem_addr(&sh.q_empty[b]), ((qn >> 1) - 1) & 1);
+          if (got) {
+            const uint32_t bar = smem_addr(&sh.q_full[b]);
+            mbar_arrive_expect_tx(bar, HALVES * G * 128);
+#pragma unroll
+            for (int hf = 0; hf < HALVES; ++hf)
+              tma_load_3d(sQ + b * LY::kQBuf + hf * 2048, &tmQ, hf * 64, (po.seg % p.Hkv) * G, po.tok, bar);
+            last_q = b;
+            last_q_parity = (qn >> 1) & 1;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        ++qn;
+      }
+      const int tpg = kGrp / EPT;                       // tiles per group
+      const int n_grp = (po.n_kt + tpg - 1) / tpg;
+      for (int grp = 0; ok && grp < n_grp; ++grp) {
+        int raw_page_n, raw_lp_n;
+        bool present_n;
+        if (grp + 1 < n_grp) {
+          fetch(seg, cur, po.v_begin, po.v_end, grp + 1, raw_page_n, raw_lp_n, present_n);
+        } else if (more) {
+          while (nxt.n_tiles == 0 && nseg_idx < nseg) nxt = load_seg(++nseg_idx);   // segments with nothing visible
+          fetch(nseg_idx, nxt, 0, nxt.n_vis, 0, raw_page_n, raw_lp_n, present_n);
+        } else {
+          raw_page_n = raw_lp_n = -1;
+          present_n = false;
+        }
+        // this group's rows
+        const bool page_ok = present && raw_page >= 0 && raw_page < p.n_pool_pages;
+        if (present && !page_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
+        const int64_t row = page_ok ? int64_t(raw_page) * P : oob_row;
+        const int lpv = page_ok ? raw_lp : -1;
+        const int tiles = min(tpg, po.n_kt - grp * tpg);
+        for (int jt = 0; jt < tiles; ++jt, ++gg) {
+          const int st = gg % NS;
+          int lps[8];
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg) lps[pg] = __shfl_sync(0xffffffffu, lpv, (jt * EPT + pg) & 31);
+          bool got = true;
+          if (lane == 0) {
+            if (gg >= NS) got = wait_or_abort(sh, smem_addr(&sh.kv_empty[st]), ((gg / NS) - 1) & 1);
+            if (got) {
+#pragma unroll
+              for (int pg = 0; pg < 8; ++pg)
+                if (pg < EPT) sh.lp[st][pg] = lps[pg];
+              mbar_arrive_expect_tx(smem_addr(&sh.kv_full[st]), kTileTx);
+              last_stage = st;
+              last_parity = (gg / NS) & 1;
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+          const int pg = lane - jt * EPT;
+          if (pg >= 0 && pg < EPT) {
+            const uint32_t full = smem_addr(&sh.kv_full[st]);
+#pragma unroll
+            for (int hf = 0; hf < HALVES; ++hf) {
+              const uint32_t off = st * LY::kStageBytes + hf * kHalfBytes + pg * P * 128;
+              tma_load_2d(sK + off, &tmK, hf * 64, int(row), full);
+              tma_load_2d(sV + off, &tmV, hf * 64, int(row), full);
+            }
+          }
+        }
+        raw_page = raw_page_n;
+        raw_lp = raw_lp_n;
+        present = present_n;
+      }
+      t = cur.tile0 + lt1;
+      seg = nseg_idx;
+      cur = nxt;
+    }
+    if (!ok && lane == 0) set_abort(sh, p.status);
+    // copies still in flight after an abort: let them land before the CTA exits (bounded)
+    if (lane == 0 && aborted(sh)) {
+      if (last_stage >= 0) mbar_wait(smem_addr(&sh.kv_full[last_stage]), last_parity);
+      if (last_q >= 0) mbar_wait(smem_addr(&sh.q_full[last_q]), last_q_parity);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t gg = 0, qn = 0;
+      bool ok = true, pending = false;
+      uint32_t pend_bar = 0, pend_parity = 0;
+      for (int k = 0; ok; ++k) {
+        const int slot = k % kRing;
+        if (!wait_or_abort(sh, smem_addr(&sh.iq_full[slot]), (k / kRing) & 1)) { ok = false; break; }
+        const Portion po = sh.ring[slot];
+        mbar_arrive(smem_addr(&sh.iq_empty[slot]));
+        if (po.seg < 0) break;
+        const int n_kt = po.n_kt;
+        const int qb = qn & 1;
+        if (!wait_or_abort(sh, smem_addr(&sh.q_full[qb]), (qn >> 1) & 1)) { ok = false; break; }
+        const uint32_t sQb = sQ + qb * LY::kQBuf;
+        tc_fence_after();
+        // issue S^T(j) and the value product of earlier tiles in whatever order they become ready
+        int qk = 0, pv = 0;
+        uint64_t t_idle = 0;
+        while (pv < n_kt) {
+          bool did = false;
+          if (qk < n_kt) {
+            const uint32_t g1 = gg + qk;
+            const int st = g1 % NS, sb = g1 & 1;
+            if (mbar_test(smem_addr(&sh.kv_full[st]), (g1 / NS) & 1) &&
+                (g1 < 2 || mbar_test(smem_addr(&sh.s_empty[sb]), ((g1 >> 1) - 1) & 1))) {
+              tc_fence_after();
+              const uint32_t kb = sK + st * LY::kStageBytes;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t a = desc_sw128(kb + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+                const uint64_t b = desc_sw128(sQb + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+                tc_mma_f16(tmem + sb * kN, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+              }
+              tc_commit(smem_addr(&sh.s_full[sb]));
+              if (qk == n_kt - 1) tc_commit(smem_addr(&sh.q_empty[qb]));   // last read of this Q buffer
+              ++qk;
+              did = true;
+            }
+          }
+          if (pv < qk) {
+            const uint32_t g1 = gg + pv;
+            const int st = g1 % NS, pb = g1 & 1;
+            if (mbar_test(smem_addr(&sh.p_full[pb]), (g1 >> 1) & 1)) {
+              tc_fence_after();
+              const uint32_t vb = sV + st * LY::kStageBytes, pbase = sP + pb * 4096;
+#pragma unroll
+              for (int kk = 0; kk < kKeys / 16; ++kk) {
+                const uint64_t a = desc_sw128(vb + kk * 2048, kHalfBytes, 1024);
+                const uint64_t b = desc_sw128(pbase + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+                tc_mma_f16(tmem + kColO, a, b, kIdescPV, (pv == 0 && kk == 0) ? 0u : 1u);
+              }
+              tc_commit(smem_addr(&sh.kv_empty[st]));
+              tc_commit(smem_addr(&sh.p_empty[pb]));
+              pending = true;
+              pend_bar = smem_addr(&sh.p_empty[pb]);
+              pend_parity = (g1 >> 1) & 1;
+              ++pv;
+              did = true;
+            }
+          }
+          if (did) {
+            t_idle = 0;
+          } else {
+            if (aborted(sh)) { ok = false; break; }
+            const uint64_t now = globaltimer();
+            if (t_idle == 0) t_idle = now;
+            else if (now - t_idle > kWaitNs) { ok = false; break; }
+            __nanosleep(32);
+          }
+        }
+        gg += n_kt;
+        ++qn;
+      }
+      if (!ok) set_abort(sh, p.status);
+      if (pending && aborted(sh)) mbar_wait(pend_bar, pend_parity);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    const int t = tid;                               // key of the tile = TMEM lane
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const float scale = p.scale_log2;
+    constexpr int LPC = 32 / NG;                     // lanes per column after the transposing reduction
+    const int my_col = lane / LPC;
+    uint32_t gg = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int slot = k % kRing;
+      const bool got_item = wait_or_abort(sh, smem_addr(&sh.iq_full[slot]), (k / kRing) & 1);
+      if (!named_bar_and(1, 128, got_item)) { ok = false; break; }
+      const Portion po = sh.ring[slot];
+      mbar_arrive(smem_addr(&sh.iq_empty[slot]));
+      if (po.seg < 0) break;
+      const int h = po.seg % p.Hkv;
+      const int n_kt = po.n_kt;
+      const bool local = po.cls == RK_CLASS_LOCAL;
+
+      float m[NG], l[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) { m[g] = -INFINITY; l[g] = 0.f; }
+      // waits whose failure is only acted on at the next barrier (so all 128 threads leave together)
+      bool good = true;
+      for (int j = 0; j < n_kt; ++j, ++gg) {
+        const int sb = gg & 1, st = gg % NS;
+        // visibility of key t (the producer published the tile's logical pages before its copies)
+        bool got = wait_or_abort(sh, smem_addr(&sh.kv_full[st]), (gg / NS) & 1);
+        const int lp = sh.lp[st][t / P];
+        const int jpos = lp * P + (t % P);
+        const bool vis = lp >= 0 && jpos < po.L && jpos <= po.pos && (!local || jpos > po.pos - po.W || jpos < po.S);
+
+        got &= wait_or_abort(sh, smem_addr(&sh.s_full[sb]), (gg >> 1) & 1);
+        tc_fence_after();
+        uint32_t sv[16];
+        tmem_ld16(tmem + lane_base + sb * kN, sv);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&sh.s_empty[sb]));
+        float x[NG], r[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          x[g] = (vis && g < G) ? __uint_as_float(sv[g]) * scale : -INFINITY;
+          r[g] = x[g];
+        }
+        const float wmax = warp_reduce_cols<NG, true>(r);
+        if (lane % LPC == 0) sh.red[gg & 1][warp][my_col] = wmax;
+        if (!named_bar_and(1, 128, got && good)) { ok = false; break; }
+        bool need = false;
+        float mt[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          mt[g] = fmaxf(fmaxf(sh.red[gg & 1][0][g], sh.red[gg & 1][1][g]),
+                        fmaxf(sh.red[gg & 1][2][g], sh.red[gg & 1][3][g]));
+          need |= mt[g] > m[g] + kRescale;
+        }
+        if (need) {   // uniform across the 128 threads
+          float alpha[NG];
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const float mn = mt[g] > m[g] + kRescale ? mt[g] : m[g];
+            alpha[g] = m[g] == -INFINITY ? 0.f : fast_exp2(m[g] - mn);
+            m[g] = mn;
+            l[g] *= alpha[g];
+          }
+          if (j > 0) {   // O^T holds earlier tiles of this portion: wait for the last PV, rescale
+            good &= wait_or_abort(sh, smem_addr(&sh.p_empty[(gg - 1) & 1]), ((gg - 1) >> 1) & 1);
+            tc_fence_after();
+            uint32_t ov[16];
+            tmem_ld16(tmem + lane_base + kColO, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < NG; ++g) ov[g] = __float_as_uint(__uint_as_float(ov[g]) * alpha[g]);
+            tmem_st16(tmem + lane_base + kColO, ov);
+            tmem_wait_st();
+          }
+        }
+        // P^T buffer (gg & 1) is free once the PV of tile gg - 2 has completed
+        if (gg >= 2) good &= wait_or_abort(sh, smem_addr(&sh.p_empty[gg & 1]), ((gg - 2) >> 1) & 1);
+        const uint32_t pb = sP + (gg & 1) * 4096 + (t >> 6) * 2048 + ((t & 7) << 1);
+        const int chunk = (t & 63) >> 3;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const float pv = fast_exp2(x[g] - (m[g] == -INFINITY ? 0.f : m[g]));
+          l[g] += pv;
+          const __nv_bfloat16 hb = __float2bfloat16_rn(pv);
+          st_shared_u16(pb + g * 128 + ((chunk ^ (g & 7)) << 4), *reinterpret_cast<const uint16_t*>(&hb));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&sh.p_full[gg & 1]));
+      }
+      if (!ok) break;
+
+      // ------------------------------------------------------------ epilogue
+      const bool got_o = wait_or_abort(sh, smem_addr(&sh.p_empty[(gg - 1) & 1]), ((gg - 1) >> 1) & 1);
+      tc_fence_after();
+      uint32_t ov[16];
+      tmem_ld16(tmem + lane_base + kColO, ov);
+      tmem_wait_ld();
+      tc_fence_before();
+      {
+        float r[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) r[g] = l[g];
+        const float wsum = warp_reduce_cols<NG, false>(r);
+        if (lane % LPC == 0) sh.redl[warp][my_col] = wsum;
+      }
+      if (!named_bar_and(1, 128, got_o && good)) { ok = false; break; }
+      float lt[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) lt[g] = sh.redl[0][g] + sh.redl[1][g] + sh.redl[2][g] + sh.redl[3][g];
+      if (t < NG) {   // per-head lse in log2 units
+        float mm = -INFINITY, ll = 0.f;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) if (g == t) { mm = m[g]; ll = lt[g]; }
+        sh.lse2[t] = ll > 0.f ? mm + fast_log2(ll) : -INFINITY;
+      }
+      named_bar_sync(1, 128);
+      const bool split = po.slot >= 0;
+      if (t < D) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          if (g < G) {
+            const float val = lt[g] > 0.f ? __uint_as_float(ov[g]) / lt[g] : 0.f;
+            if (!split) p.out[(int64_t(po.tok) * p.Hq + h * G + g) * D + t] = __float2bfloat16_rn(val);
+            else ws.part_o[(int64_t(po.slot) * G + g) * D + t] = val;
+          }
+        }
+      }
+      if (t < G) {
+        if (!split) {
+          if (p.lse) p.lse[int64_t(po.tok) * p.Hq + h * G + t] = sh.lse2[t] * 0.69314718055994531f;
+        } else {
+          ws.part_lse[int64_t(po.slot) * G + t] = sh.lse2[t];
+        }
+      }
+      named_bar_sync(1, 128);   // sh.redl / sh.lse2 are rewritten by the next portion
+    }
+    if (!ok && lane == 0) set_abort(sh, p.status);
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Merge the partial results of the split segments: one block per (segment, head) unit at a
+// time; lane l of every warp owns channels [4l, 4l+4) and warp w every 8th partial.
+template <int D>
+__global__ __launch_bounds__(256) void combine_decode_tc_kernel(AttnParams p, DecWorkspace ws) {
+  grid_dependency_wait();   // the decode kernel is complete
+  constexpr int C4 = D / 4;
+  __shared__ float s_m[8], s_den[8];
+  __shared__ float4 s_acc[8][C4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  const int units = ws.header->n_split * G;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int seg = ws.split_segs[u / G], g = u % G;
+    const DecSeg sd = ws.segs[seg];
+    const int n = sd.n_splits, s0 = sd.slot0;
+    float M = -INFINITY;
+    for (int s = threadIdx.x; s < n; s += 256) M = fmaxf(M, ws.part_lse[int64_t(s0 + s) * G + g]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) s_m[warp] = M;
+    __syncthreads();
+    M = s_m[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) M = fmaxf(M, s_m[w]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < C4) {
+#pragma unroll 4
+      for (int s = warp; s < n; s += 8) {
+        const float lv = ws.part_lse[int64_t(s0 + s) * G + g];
+        const float w = M == -INFINITY ? 0.f : fast_exp2(lv - M);
+        const float4 v = *reinterpret_cast<const float4*>(ws.part_o + (int64_t(s0 + s) * G + g) * D + lane * 4);
+        den += w;
+        acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+      }
+      s_acc[warp][lane] = acc;
+    }
+    if (lane == 0) s_den[warp] = den;
+    __syncthreads();
+    if (warp == 0 && lane < C4) {
+      float d = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        d += s_den[w];
+        a.x += s_acc[w][lane].x; a.y += s_acc[w][lane].y; a.z += s_acc[w][lane].z; a.w += s_acc[w][lane].w;
+      }
+      const float inv = d > 0.f ? 1.f / d : 0.f;
+      const int hq = (seg % p.Hkv) * G + g;
+      uint2 o;
+      o.x = pack_bf16(a.x * inv, a.y * inv);
+      o.y = pack_bf16(a.z * inv, a.w * inv);
+      *reinterpret_cast<uint2*>(p.out + (int64_t(sd.tok) * p.Hq + hq) * D + lane * 4) = o;
+      if (p.lse && lane == 0)
+        p.lse[int64_t(sd.tok) * p.Hq + hq] = d > 0.f ? (M + fast_log2(d)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+  }
+}
+
+cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int D, int NG>
+cudaError_t launch_t(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream) {
+  using LY = DecLayout<D>;
+  CUtensorMap mq, mk, mv;
+  const cuuint64_t qdims[3] = {cuuint64_t(D), cuuint64_t(p.Hq), cuuint64_t(p.total_q)};
+  const cuuint64_t qstr[2] = {cuuint64_t(D) * 2, cuuint64_t(p.Hq) * D * 2};
+  const cuuint32_t qbox[3] = {64, cuuint32_t(p.G), 1};
+  const cuuint64_t kdims[2] = {cuuint64_t(D), cuuint64_t(p.n_pool_pages) * p.P};
+  const cuuint64_t kstr[1] = {cuuint64_t(D) * 2};
+  const cuuint32_t kbox[2] = {64, cuuint32_t(p.P)};
+  if (!encode_tmap_bf16(&mq, p.q, 3, qdims, qstr, qbox) || !encode_tmap_bf16(&mk, p.k_pool, 2, kdims, kstr, kbox) ||
+      !encode_tmap_bf16(&mv, p.v_pool, 2, kdims, kstr, kbox))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         LY::kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(ws.grid), dim3(kThreads), LY::kSmem, stream, attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG>, mq, mk, mv, p, ws);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr2[1];
+  cudaLaunchConfig_t cfg2 = pdl_config(dim3(ws.grid), dim3(256), 0, stream, attr2);
+  return cudaLaunchKernelEx(&cfg2, combine_decode_tc_kernel<D>, p, ws);
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream) {
+  switch (p.G) {
+    case 1: case 2: case 4: return launch_t<D, 4>(p, ws, stream);
+    case 8: return launch_t<D, 8>(p, ws, stream);
+    case 16: return launch_t<D, 16>(p, ws, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream) {
+  return p.d == 128 ? launch_d<128>(p, ws, stream) : launch_d<64>(p, ws, stream);
+}
+
+}  // namespace rk

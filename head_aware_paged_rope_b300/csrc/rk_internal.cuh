@@ -1,6 +1,7 @@
 // Internal declarations shared by the librk CUDA sources (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -110,6 +111,47 @@ struct AttnWorkspace {
 
 constexpr int kTargetItems = 2048;   // upper bound on items beyond one per unit
 
+// ------------------------------------------------------------------ decode work list
+// Decode is scheduled stream-K style: the key tiles (128 keys) of all head segments are
+// concatenated, segment after segment, and CTA c of the decode grid takes the equal share
+// [c*T/gs, (c+1)*T/gs) of the T tiles (gs = min(grid, T); further CTAs get none).  A segment whose tiles fall to several CTAs is
+// "split": each CTA writes a normalised partial result into its slot and
+// combine_decode_tc_kernel merges them.  plan_decode_kernel (rk_plan.cu) writes:
+struct DecSeg {
+  int32_t e_sink, e_w, n_vis, n_tiles;      // visible entry ranges (see Unit) and key tiles
+  int32_t tile0;                            // first tile of the segment in the global sequence
+  int32_t slot0;                            // first partial slot (split segments only)
+  int32_t cta0;                             // first CTA whose share touches the segment
+  int32_t n_splits;                         // CTAs that touch it (1: written directly)
+  int32_t b, tok, pos, cls;                 // sequence, query row, query position, head class
+  int32_t W, S, L, pad;                     // window, sink, context length
+};
+
+struct DecCta {
+  int32_t seg0;          // segment holding the first tile of the share (B*Hkv if none)
+  int32_t tile_begin, tile_end, pad;
+};
+
+struct DecHeader {
+  int32_t total_tiles;
+  int32_t n_split;       // split segments, listed in DecWorkspace::split_segs
+  int32_t grid;          // CTAs of the decode kernel the shares were cut for
+  int32_t pad[61];
+};
+
+struct DecWorkspace {
+  DecHeader* header;
+  DecSeg* segs;          // [B*Hkv]
+  DecCta* ctas;          // [grid]
+  int32_t* split_segs;   // [B*Hkv]
+  float* part_lse;       // [max_slots][G], log2 domain
+  float* part_o;         // [max_slots][G][d], normalised partial outputs
+  int32_t max_slots;     // >= the slots any plan needs: B*Hkv + grid
+  int32_t grid;
+};
+
+constexpr int kDecTileKeys = 128;
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Launchers implemented in the .cu files.
@@ -123,6 +165,11 @@ cudaError_t launch_prefill_mma(const AttnParams& p, const AttnWorkspace& ws, int
 cudaError_t launch_decode(const AttnParams& p, const AttnWorkspace& ws, int grid,
                           cudaStream_t stream);
 cudaError_t launch_combine_decode(const AttnParams& p, const AttnWorkspace& ws, cudaStream_t stream);
+cudaError_t launch_plan_decode(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream);
+cudaError_t launch_decode_tc(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream);
+// bf16 2-D / 3-D tensor map with 128-byte swizzle (rk_prefill_tc.cu)
+bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                      const cuuint32_t* box);
 int decode_ctas_per_sm(int P);
 cudaError_t launch_rope(const rk_rope_args& a, void* workspace, cudaStream_t stream);
 

@@ -8,6 +8,7 @@
 // of about equal size so that a persistent grid stays busy whatever the mix of head
 // classes.  Items of one unit are merged afterwards with the usual log-sum-exp rule.
 #include "rk_internal.cuh"
+#include "rk_sm100.cuh"
 
 #include <algorithm>
 
@@ -25,6 +26,13 @@ __device__ int lower_bound_lp(const int32_t* row, int n, int x) {
   if (x <= first) return 0;
   if (x > last) return n;
   if (last - first == n - 1) return x - first;    // contiguous run of logical pages
+  // the list may end in a contiguous run (a window after sink pages): guess, then verify
+  const int guess = n - 1 - (last - x);
+  if (guess > 0 && guess < n) {
+    const int at = __ldg(row + guess);
+    if (at == x) return guess;
+    if (at < x && __ldg(row + guess + 1) > x) return guess + 1;
+  }
   int lo = 0, hi = n;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
@@ -240,7 +248,148 @@ __global__ __launch_bounds__(256) void combine_kernel(AttnParams p, AttnWorkspac
   }
 }
 
+// Decode plan: one query per sequence at position seq_len - 1.
+//  1. each head segment's visible entry ranges (as plan_kernel), its key tiles, and for a
+//     segment with nothing visible its output (zeros, lse = -inf), which no CTA writes;
+//  2. the tile prefix over segments: T tiles in all; with gs = min(grid, T), CTA c < gs of
+//     the decode grid takes tiles [c*T/gs, (c+1)*T/gs), so tile t belongs to CTA
+//     ((t+1)*gs + T - 1) / T - 1 (the others get no tiles);
+//  3. per segment the CTAs its tiles fall to; segments with more than one get consecutive
+//     partial slots and are listed for the combine kernel;
+//  4. per CTA the segment holding its first tile.
+__global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p, DecWorkspace ws) {
+  // the decode kernel may start its prologue now; it reads this plan after griddepcontrol.wait
+  sm100::grid_launch_dependents();
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x;
+  const int nseg = p.B * p.Hkv;
+  const int ept = kDecTileKeys / p.P;
+  const int grid = ws.grid;
+
+  // 1. visible ranges
+  for (int seg = tid; seg < nseg; seg += kPlanThreads) {
+    const int b = seg / p.Hkv;
+    const int L = __ldg(p.seq_len + b);
+    int n = __ldg(p.n_pages + seg);
+    const int cls = __ldg(p.head_class + seg);
+    const int W = cls == RK_CLASS_LOCAL ? __ldg(p.window + seg) : 0;
+    const int S = (cls == RK_CLASS_LOCAL && p.sink) ? __ldg(p.sink + seg) : 0;
+    if (n < 0 || n > p.max_pages) { report(p.status, RK_ERR_DEVICE_BOUNDS); n = 0; }
+    DecSeg ds{};
+    const int pos = L - 1;
+    if (L > 0 && n > 0) {
+      const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
+      const int e_hi = upper_bound_lp(lrow, n, pos / p.P);
+      if (cls == RK_CLASS_LOCAL) {
+        const int start = max(0, pos - W + 1);
+        int e_w = min(lower_bound_lp(lrow, n, start / p.P), e_hi);
+        int e_s = S > 0 ? min(upper_bound_lp(lrow, n, (S - 1) / p.P), e_hi) : 0;
+        if (e_s >= e_w) { e_s = 0; e_w = 0; }
+        ds.e_sink = e_s;
+        ds.e_w = e_w;
+        ds.n_vis = e_s + (e_hi - e_w);
+      } else {
+        ds.n_vis = e_hi;
+      }
+    }
+    ds.n_tiles = (ds.n_vis + ept - 1) / ept;
+    ds.b = b;
+    ds.tok = b;
+    ds.pos = pos;
+    ds.cls = cls;
+    ds.W = W;
+    ds.S = S;
+    ds.L = L;
+    ds.n_splits = 1;
+    ds.slot0 = -1;
+    ws.segs[seg] = ds;
+    if (ds.n_tiles == 0) {   // nothing visible: out = 0, lse = -inf
+      const int h = seg - b * p.Hkv;
+      uint4* o = reinterpret_cast<uint4*>(p.out + (int64_t(b) * p.Hq + h * p.G) * p.d);
+      for (int i = 0; i < p.G * p.d / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+      if (p.lse)
+        for (int g = 0; g < p.G; ++g) p.lse[int64_t(b) * p.Hq + h * p.G + g] = -INFINITY;
+    }
+  }
+  __syncthreads();
+
+  // 2. tile prefix
+  int carry = 0;
+  for (int base = 0; base < nseg; base += kPlanThreads) {
+    const int seg = base + tid;
+    const int nt = seg < nseg ? ws.segs[seg].n_tiles : 0;
+    int tot;
+    const int pre = block_exclusive_scan(nt, &tot, s_warp);
+    if (seg < nseg) ws.segs[seg].tile0 = carry + pre;
+    carry += tot;
+  }
+  const long long T = carry;
+  // shares are cut over at most T CTAs, so that every share holds at least one tile and
+  // the CTAs a segment's tiles fall to are exactly the ones that write its partials
+  const int gs = (int)min((long long)grid, T);
+  for (int c = tid; c < grid; c += kPlanThreads) {
+    DecCta dc;
+    dc.seg0 = nseg;
+    dc.tile_begin = c < gs ? (int)((long long)c * T / gs) : (int)T;
+    dc.tile_end = c < gs ? (int)((long long)(c + 1) * T / gs) : (int)T;
+    dc.pad = 0;
+    ws.ctas[c] = dc;
+  }
+  __syncthreads();
+
+  // 3. owners, splits and slots;  4. first segment of each CTA's share
+  auto owner = [&](long long t) { return (int)(((t + 1) * gs + T - 1) / T - 1); };
+  int carry_slot = 0, carry_split = 0;
+  for (int base = 0; base < nseg; base += kPlanThreads) {
+    const int seg = base + tid;
+    int ns = 0, t0 = 0, nt = 0, c0 = 0, c1 = -1;
+    if (seg < nseg) {
+      t0 = ws.segs[seg].tile0;
+      nt = ws.segs[seg].n_tiles;
+      if (nt > 0) {
+        c0 = owner(t0);
+        c1 = owner((long long)t0 + nt - 1);
+        ns = c1 - c0 + 1;
+      }
+    }
+    const int split = ns > 1 ? 1 : 0;
+    int tot_slot, tot_split;
+    const int pre_slot = block_exclusive_scan(split ? ns : 0, &tot_slot, s_warp);
+    const int pre_split = block_exclusive_scan(split, &tot_split, s_warp);
+    if (seg < nseg && nt > 0) {
+      DecSeg& ds = ws.segs[seg];
+      ds.cta0 = c0;
+      ds.n_splits = ns;
+      if (split) {
+        ds.slot0 = carry_slot + pre_slot;
+        ws.split_segs[carry_split + pre_split] = seg;
+      }
+      // CTAs whose share starts inside this segment: all of c0..c1 except c0 when its share
+      // began in an earlier segment
+      const int cs = ((long long)c0 * T / gs < t0) ? c0 + 1 : c0;
+      for (int c = cs; c <= c1; ++c) ws.ctas[c].seg0 = seg;
+    }
+    carry_slot += tot_slot;
+    carry_split += tot_split;
+  }
+  if (carry_slot > ws.max_slots) {   // cannot happen (slots <= segments + grid); nothing is scheduled
+    if (tid == 0) report(p.status, RK_ERR_DEVICE_BOUNDS);
+    for (int c = tid; c < grid; c += kPlanThreads) ws.ctas[c].tile_end = ws.ctas[c].tile_begin;
+    carry_split = 0;
+  }
+  if (tid == 0) {
+    ws.header->total_tiles = (int)T;
+    ws.header->n_split = carry_split;
+    ws.header->grid = grid;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_plan_decode(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream) {
+  plan_decode_kernel<<<1, kPlanThreads, 0, stream>>>(p, ws);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int tok_per_unit,
                         int entries_per_tile, int target_items, int min_chunk_tiles, bool decode,

@@ -393,28 +393,6 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-            const cuuint32_t* box) {
-  auto fn = get_encoder();
-  if (!fn) return false;
-  const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int P>
 cudaError_t launch_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cudaStream_t stream) {
   using LY = TcLayout<D>;
@@ -425,8 +403,8 @@ cudaError_t launch_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cu
   const cuuint64_t kdims[2] = {cuuint64_t(D), cuuint64_t(p.n_pool_pages) * P};
   const cuuint64_t kstr[1] = {cuuint64_t(D) * 2};
   const cuuint32_t kbox[2] = {64, cuuint32_t(P)};
-  if (!encode(&mq, p.q, 3, qdims, qstr, qbox) || !encode(&mk, p.k_pool, 2, kdims, kstr, kbox) ||
-      !encode(&mv, p.v_pool, 2, kdims, kstr, kbox))
+  if (!encode_tmap_bf16(&mq, p.q, 3, qdims, qstr, qbox) || !encode_tmap_bf16(&mk, p.k_pool, 2, kdims, kstr, kbox) ||
+      !encode_tmap_bf16(&mv, p.v_pool, 2, kdims, kstr, kbox))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -441,6 +419,29 @@ cudaError_t launch_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cu
 }
 
 }  // namespace
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+  auto fn = get_encoder();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int prefill_tc_rows() { return kRowsTc; }
 int prefill_tc_keys() { return kKeysTc; }

@@ -172,7 +172,8 @@ RK_API size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* args);
 RK_API size_t rk_segpaged_decode_workspace_size(const rk_attn_args* args);
 
 /* Prefill: any number of queries per sequence (a suffix at the end of the context).
- * Errors: RK_ERR_INVALID_ARG (NULL pointers, B/Hq/Hkv/max_pages/total_q < 0, Hq % Hkv,
+ * Errors: RK_ERR_INVALID_ARG (NULL pointers, q / k_pool / v_pool / out not 16-byte aligned,
+ * B/Hq/Hkv/max_pages/total_q < 0, Hq % Hkv,
  * max_q > total_q), RK_ERR_UNSUPPORTED (d, P, Hq/Hkv > 16), RK_ERR_WORKSPACE, RK_ERR_CUDA. */
 RK_API rk_status rk_segpaged_prefill(const rk_attn_args* args, void* workspace, size_t workspace_bytes,
                               rk_stream_t stream);
