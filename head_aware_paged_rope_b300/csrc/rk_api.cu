@@ -219,6 +219,7 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
   if (a->B == 0 || a->total_q == 0) return RK_OK;
   const int sms = device_sm_count();
   if (decode && !use_simt_decode()) {
+    if (int64_t(a->B) * a->Hkv > kDecMaxSegs) return RK_ERR_UNSUPPORTED;
     const DecLayoutHost dl = dec_layout(a);
     st = check_ws(workspace, bytes, dl.total);
     if (st != RK_OK) return st;

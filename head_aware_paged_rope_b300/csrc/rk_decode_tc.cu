@@ -601,12 +601,15 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
   }
 }
 
-// Merge the partial results of the split segments: one block per (segment, head) unit at a
-// time; lane l of every warp owns channels [4l, 4l+4) and warp w every 8th partial.
+// Merge the partial results of the split segments, one (segment, head) unit per block at
+// a time: warp w takes partials w, w+8, ... (64 per round, all loads of a round in flight)
+// and keeps a running log-sum-exp merge; lane l owns channels [4l, 4l+4).  The warps'
+// states are merged at the end.
 template <int D>
 __global__ __launch_bounds__(256) void combine_decode_tc_kernel(AttnParams p, DecWorkspace ws) {
   grid_dependency_wait();   // the decode kernel is complete
   constexpr int C4 = D / 4;
+  constexpr int PER = 8;    // partials per warp and round
   __shared__ float s_m[8], s_den[8];
   __shared__ float4 s_acc[8][C4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -616,38 +619,52 @@ __global__ __launch_bounds__(256) void combine_decode_tc_kernel(AttnParams p, De
     const int seg = ws.split_segs[u / G], g = u % G;
     const DecSeg sd = ws.segs[seg];
     const int n = sd.n_splits, s0 = sd.slot0;
-    float M = -INFINITY;
-    for (int s = threadIdx.x; s < n; s += 256) M = fmaxf(M, ws.part_lse[int64_t(s0 + s) * G + g]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0) s_m[warp] = M;
-    __syncthreads();
-    M = s_m[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) M = fmaxf(M, s_m[w]);
-    float den = 0.f;
+    float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < C4) {
-#pragma unroll 4
-      for (int s = warp; s < n; s += 8) {
-        const float lv = ws.part_lse[int64_t(s0 + s) * G + g];
-        const float w = M == -INFINITY ? 0.f : fast_exp2(lv - M);
-        const float4 v = *reinterpret_cast<const float4*>(ws.part_o + (int64_t(s0 + s) * G + g) * D + lane * 4);
-        den += w;
-        acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+    for (int base = 0; base < n; base += 8 * PER) {
+      float lv[PER];
+      float4 ov[PER];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int s = base + warp + 8 * k;
+        lv[k] = -INFINITY;
+        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < n) {
+          lv[k] = ws.part_lse[int64_t(s0 + s) * G + g];
+          if (lane < C4) ov[k] = *reinterpret_cast<const float4*>(ws.part_o + (int64_t(s0 + s) * G + g) * D + lane * 4);
+        }
       }
-      s_acc[warp][lane] = acc;
+      float mc = M;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) mc = fmaxf(mc, lv[k]);
+      if (mc == -INFINITY) continue;
+      const float f = M == -INFINITY ? 0.f : fast_exp2(M - mc);
+      den *= f;
+      acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+      M = mc;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const float w = lv[k] == -INFINITY ? 0.f : fast_exp2(lv[k] - M);
+        den += w;
+        acc.x = fmaf(w, ov[k].x, acc.x); acc.y = fmaf(w, ov[k].y, acc.y);
+        acc.z = fmaf(w, ov[k].z, acc.z); acc.w = fmaf(w, ov[k].w, acc.w);
+      }
     }
-    if (lane == 0) s_den[warp] = den;
+    if (lane == 0) { s_m[warp] = M; s_den[warp] = den; }
+    if (lane < C4) s_acc[warp][lane] = acc;
     __syncthreads();
     if (warp == 0 && lane < C4) {
+      float Mt = s_m[0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) Mt = fmaxf(Mt, s_m[w]);
       float d = 0.f;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
-        d += s_den[w];
-        a.x += s_acc[w][lane].x; a.y += s_acc[w][lane].y; a.z += s_acc[w][lane].z; a.w += s_acc[w][lane].w;
+        const float f = s_m[w] == -INFINITY ? 0.f : fast_exp2(s_m[w] - Mt);
+        d += f * s_den[w];
+        a.x = fmaf(f, s_acc[w][lane].x, a.x); a.y = fmaf(f, s_acc[w][lane].y, a.y);
+        a.z = fmaf(f, s_acc[w][lane].z, a.z); a.w = fmaf(f, s_acc[w][lane].w, a.w);
       }
       const float inv = d > 0.f ? 1.f / d : 0.f;
       const int hq = (seg % p.Hkv) * G + g;
@@ -656,7 +673,7 @@ __global__ __launch_bounds__(256) void combine_decode_tc_kernel(AttnParams p, De
       o.y = pack_bf16(a.z * inv, a.w * inv);
       *reinterpret_cast<uint2*>(p.out + (int64_t(sd.tok) * p.Hq + hq) * D + lane * 4) = o;
       if (p.lse && lane == 0)
-        p.lse[int64_t(sd.tok) * p.Hq + hq] = d > 0.f ? (M + fast_log2(d)) * 0.69314718055994531f : -INFINITY;
+        p.lse[int64_t(sd.tok) * p.Hq + hq] = d > 0.f ? (Mt + fast_log2(d)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
   }
@@ -702,7 +719,7 @@ cudaError_t launch_t(const AttnParams& p, const DecWorkspace& ws, cudaStream_t s
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG>, mq, mk, mv, p, ws);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[1];
-  cudaLaunchConfig_t cfg2 = pdl_config(dim3(ws.grid), dim3(256), 0, stream, attr2);
+  cudaLaunchConfig_t cfg2 = pdl_config(dim3(4 * ws.grid), dim3(256), 0, stream, attr2);
   return cudaLaunchKernelEx(&cfg2, combine_decode_tc_kernel<D>, p, ws);
 }
 

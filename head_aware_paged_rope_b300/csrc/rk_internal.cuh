@@ -151,6 +151,7 @@ struct DecWorkspace {
 };
 
 constexpr int kDecTileKeys = 128;
+constexpr int kDecMaxSegs = 16384;   // B * Hkv of one decode call (the planner keeps 8 bytes per segment on chip)
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

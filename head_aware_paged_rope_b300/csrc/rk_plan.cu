@@ -248,23 +248,54 @@ __global__ __launch_bounds__(256) void combine_kernel(AttnParams p, AttnWorkspac
   }
 }
 
+// Lower bound (first entry >= x) of an ascending logical-page list from its two ends: the
+// answer when the ends decide it, else -1 and a guess g (0 <= g <= n-2) to verify with
+// lb_verify after loading row[g] and row[g+1].  `hint` is where the answer lies if the
+// list is contiguous near it.
+__device__ __forceinline__ int lb_ends(const int32_t* row, int n, int first, int last, int x, int hint, int& g) {
+  g = -1;
+  if (!row) return min(max(x, 0), n);
+  if (n <= 0 || x <= first) return 0;
+  if (x > last) return n;
+  if (last - first == n - 1) return x - first;
+  g = min(max(hint, 0), n - 2);   // first < x <= last implies n >= 2
+  return -1;
+}
+
+__device__ __forceinline__ int lb_verify(const int32_t* row, int n, int x, int g, int at, int at1) {
+  if (at == x) return g;                    // strictly ascending: every earlier entry is < x
+  if (at < x && at1 >= x) return g + 1;
+  int lo = at < x ? g + 2 : 0, hi = at < x ? n : g;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(row + mid) < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
 // Decode plan: one query per sequence at position seq_len - 1.
-//  1. each head segment's visible entry ranges (as plan_kernel), its key tiles, and for a
-//     segment with nothing visible its output (zeros, lse = -inf), which no CTA writes;
+//  1. each head segment's visible entry ranges (as plan_kernel), in three rounds of loads:
+//     the segment's scalars, the two ends of its logical-page list, then one check of every
+//     bound the ends do not settle; its key tiles; and, for a segment with nothing visible,
+//     its output (zeros, lse = -inf), which no CTA writes;
 //  2. the tile prefix over segments: T tiles in all; with gs = min(grid, T), CTA c < gs of
 //     the decode grid takes tiles [c*T/gs, (c+1)*T/gs), so tile t belongs to CTA
 //     ((t+1)*gs + T - 1) / T - 1 (the others get no tiles);
 //  3. per segment the CTAs its tiles fall to; segments with more than one get consecutive
 //     partial slots and are listed for the combine kernel;
 //  4. per CTA the segment holding its first tile.
+// Per-segment tile counts and prefixes stay in shared memory (8 bytes per segment).
 __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p, DecWorkspace ws) {
   // the decode kernel may start its prologue now; it reads this plan after griddepcontrol.wait
   sm100::grid_launch_dependents();
+  extern __shared__ int s_seg[];            // [nseg] tiles, then [nseg] first tile
   __shared__ int s_warp[32];
   const int tid = threadIdx.x;
   const int nseg = p.B * p.Hkv;
   const int ept = kDecTileKeys / p.P;
   const int grid = ws.grid;
+  int* s_nt = s_seg;
+  int* s_t0 = s_seg + nseg;
 
   // 1. visible ranges
   for (int seg = tid; seg < nseg; seg += kPlanThreads) {
@@ -272,27 +303,51 @@ __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p,
     const int L = __ldg(p.seq_len + b);
     int n = __ldg(p.n_pages + seg);
     const int cls = __ldg(p.head_class + seg);
-    const int W = cls == RK_CLASS_LOCAL ? __ldg(p.window + seg) : 0;
-    const int S = (cls == RK_CLASS_LOCAL && p.sink) ? __ldg(p.sink + seg) : 0;
+    const int Wr = __ldg(p.window + seg);
+    const int Sr = p.sink ? __ldg(p.sink + seg) : 0;
+    const bool local = cls == RK_CLASS_LOCAL;
+    const int W = local ? Wr : 0, S = local ? Sr : 0;
     if (n < 0 || n > p.max_pages) { report(p.status, RK_ERR_DEVICE_BOUNDS); n = 0; }
-    DecSeg ds{};
     const int pos = L - 1;
+    const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
+    int first = 0, last = 0;
+    if (lrow && n > 0 && L > 0) {
+      first = __ldg(lrow);
+      last = __ldg(lrow + n - 1);
+    }
+    int n_vis = 0, e_sink = 0, e_w = 0;
     if (L > 0 && n > 0) {
-      const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
-      const int e_hi = upper_bound_lp(lrow, n, pos / p.P);
-      if (cls == RK_CLASS_LOCAL) {
-        const int start = max(0, pos - W + 1);
-        int e_w = min(lower_bound_lp(lrow, n, start / p.P), e_hi);
-        int e_s = S > 0 ? min(upper_bound_lp(lrow, n, (S - 1) / p.P), e_hi) : 0;
-        if (e_s >= e_w) { e_s = 0; e_w = 0; }
-        ds.e_sink = e_s;
-        ds.e_w = e_w;
-        ds.n_vis = e_s + (e_hi - e_w);
+      const int x_hi = pos / p.P + 1;                   // entries with logical page <= pos / P
+      const int x_w = max(0, pos - W + 1) / p.P;        // first window page
+      const int x_s = (S - 1) / p.P + 1;                // entries past the sink pages
+      int g_hi, g_w = -1, g_s = -1;
+      int r_hi = lb_ends(lrow, n, first, last, x_hi, n - 1 - (last - x_hi), g_hi);
+      int r_w = local ? lb_ends(lrow, n, first, last, x_w, n - 1 - (last - x_w), g_w) : 0;
+      int r_s = (local && S > 0) ? lb_ends(lrow, n, first, last, x_s, x_s - first, g_s) : 0;
+      int a_hi = 0, b_hi = 0, a_w = 0, b_w = 0, a_s = 0, b_s = 0;   // all checks in one round
+      if (g_hi >= 0) { a_hi = __ldg(lrow + g_hi); b_hi = __ldg(lrow + g_hi + 1); }
+      if (g_w >= 0) { a_w = __ldg(lrow + g_w); b_w = __ldg(lrow + g_w + 1); }
+      if (g_s >= 0) { a_s = __ldg(lrow + g_s); b_s = __ldg(lrow + g_s + 1); }
+      if (g_hi >= 0) r_hi = lb_verify(lrow, n, x_hi, g_hi, a_hi, b_hi);
+      if (g_w >= 0) r_w = lb_verify(lrow, n, x_w, g_w, a_w, b_w);
+      if (g_s >= 0) r_s = lb_verify(lrow, n, x_s, g_s, a_s, b_s);
+      const int e_hi = r_hi;
+      if (local) {
+        int ew = min(r_w, e_hi), es = S > 0 ? min(r_s, e_hi) : 0;
+        if (es >= ew) { es = 0; ew = 0; }
+        e_sink = es;
+        e_w = ew;
+        n_vis = es + (e_hi - ew);
       } else {
-        ds.n_vis = e_hi;
+        n_vis = e_hi;
       }
     }
-    ds.n_tiles = (ds.n_vis + ept - 1) / ept;
+    DecSeg& ds = ws.segs[seg];
+    ds.e_sink = e_sink;
+    ds.e_w = e_w;
+    ds.n_vis = n_vis;
+    const int nt = (n_vis + ept - 1) / ept;
+    ds.n_tiles = nt;
     ds.b = b;
     ds.tok = b;
     ds.pos = pos;
@@ -300,10 +355,8 @@ __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p,
     ds.W = W;
     ds.S = S;
     ds.L = L;
-    ds.n_splits = 1;
-    ds.slot0 = -1;
-    ws.segs[seg] = ds;
-    if (ds.n_tiles == 0) {   // nothing visible: out = 0, lse = -inf
+    s_nt[seg] = nt;
+    if (nt == 0) {   // nothing visible: out = 0, lse = -inf
       const int h = seg - b * p.Hkv;
       uint4* o = reinterpret_cast<uint4*>(p.out + (int64_t(b) * p.Hq + h * p.G) * p.d);
       for (int i = 0; i < p.G * p.d / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -317,10 +370,10 @@ __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p,
   int carry = 0;
   for (int base = 0; base < nseg; base += kPlanThreads) {
     const int seg = base + tid;
-    const int nt = seg < nseg ? ws.segs[seg].n_tiles : 0;
+    const int nt = seg < nseg ? s_nt[seg] : 0;
     int tot;
     const int pre = block_exclusive_scan(nt, &tot, s_warp);
-    if (seg < nseg) ws.segs[seg].tile0 = carry + pre;
+    if (seg < nseg) s_t0[seg] = carry + pre;
     carry += tot;
   }
   const long long T = carry;
@@ -344,8 +397,8 @@ __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p,
     const int seg = base + tid;
     int ns = 0, t0 = 0, nt = 0, c0 = 0, c1 = -1;
     if (seg < nseg) {
-      t0 = ws.segs[seg].tile0;
-      nt = ws.segs[seg].n_tiles;
+      t0 = s_t0[seg];
+      nt = s_nt[seg];
       if (nt > 0) {
         c0 = owner(t0);
         c1 = owner((long long)t0 + nt - 1);
@@ -356,18 +409,19 @@ __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p,
     int tot_slot, tot_split;
     const int pre_slot = block_exclusive_scan(split ? ns : 0, &tot_slot, s_warp);
     const int pre_split = block_exclusive_scan(split, &tot_split, s_warp);
-    if (seg < nseg && nt > 0) {
+    if (seg < nseg) {
       DecSeg& ds = ws.segs[seg];
+      ds.tile0 = t0;
       ds.cta0 = c0;
-      ds.n_splits = ns;
-      if (split) {
-        ds.slot0 = carry_slot + pre_slot;
-        ws.split_segs[carry_split + pre_split] = seg;
+      ds.n_splits = nt > 0 ? ns : 1;
+      ds.slot0 = split ? carry_slot + pre_slot : -1;
+      if (split) ws.split_segs[carry_split + pre_split] = seg;
+      if (nt > 0) {
+        // CTAs whose share starts inside this segment: all of c0..c1 except c0 when its share
+        // began in an earlier segment
+        const int cs = ((long long)c0 * T / gs < t0) ? c0 + 1 : c0;
+        for (int c = cs; c <= c1; ++c) ws.ctas[c].seg0 = seg;
       }
-      // CTAs whose share starts inside this segment: all of c0..c1 except c0 when its share
-      // began in an earlier segment
-      const int cs = ((long long)c0 * T / gs < t0) ? c0 + 1 : c0;
-      for (int c = cs; c <= c1; ++c) ws.ctas[c].seg0 = seg;
     }
     carry_slot += tot_slot;
     carry_split += tot_split;
@@ -387,7 +441,17 @@ __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p,
 }  // namespace
 
 cudaError_t launch_plan_decode(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream) {
-  plan_decode_kernel<<<1, kPlanThreads, 0, stream>>>(p, ws);
+  const size_t smem = size_t(8) * p.B * p.Hkv;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(plan_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         8 * kDecMaxSegs);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  plan_decode_kernel<<<1, kPlanThreads, smem, stream>>>(p, ws);
   return cudaGetLastError();
 }
 

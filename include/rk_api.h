@@ -179,7 +179,8 @@ RK_API rk_status rk_segpaged_prefill(const rk_attn_args* args, void* workspace, 
                               rk_stream_t stream);
 
 /* Decode: one query per sequence at position seq_len[b] - 1 (q is [B][Hq][d]); split-KV
- * over each head's visible pages, partial results merged by log-sum-exp.  Same errors. */
+ * over each head's visible pages, partial results merged by log-sum-exp.  Same errors, and
+ * RK_ERR_UNSUPPORTED when B * Hkv exceeds 16384. */
 RK_API rk_status rk_segpaged_decode(const rk_attn_args* args, void* workspace, size_t workspace_bytes,
                              rk_stream_t stream);
 
