@@ -320,11 +320,10 @@ __global__ __launch_bounds__(128) void combine_decode_kernel(AttnParams p, AttnW
   const int u = blockIdx.x, g = blockIdx.y;
   if (u >= ws.header->n_units) return;
   const Unit un = ws.units[u];
-  if (un.n_splits <= 1 || un.first_item + un.n_splits > ws.max_items) return;
+  if (un.n_splits <= 1) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t base = un.first_item;
   float M = -INFINITY;
-  for (int s = threadIdx.x; s < un.n_splits; s += 128) M = fmaxf(M, ws.part_lse[(base + s) * ws.rows + g]);
+  for (int s = threadIdx.x; s < un.n_splits; s += 128) M = fmaxf(M, ws.part_lse[int64_t(unit_item(un, s)) * ws.rows + g]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) s_m[warp] = M;
@@ -335,10 +334,11 @@ __global__ __launch_bounds__(128) void combine_decode_kernel(AttnParams p, AttnW
   for (int c = 0; c < CH; ++c) num[c] = 0.f;
 #pragma unroll 4
   for (int s = warp; s < un.n_splits; s += 4) {
-    const float l = ws.part_lse[(base + s) * ws.rows + g];
+    const int64_t it = unit_item(un, s);
+    const float l = ws.part_lse[it * ws.rows + g];
     const float w = (M == -INFINITY) ? 0.f : __expf(l - M);
     den += w;
-    const float* po = ws.part_o + ((base + s) * ws.rows + g) * D + lane * CH;
+    const float* po = ws.part_o + (it * ws.rows + g) * D + lane * CH;
 #pragma unroll
     for (int c = 0; c < CH; ++c) num[c] += w * po[c];
   }

@@ -30,6 +30,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -50,9 +56,10 @@ struct Unit {
   int32_t e_w;        // first entry of the second range
   int32_t n_vis;      // entries to visit
   int32_t n_splits;   // items of this unit
-  int32_t first_item; // index of its first item
+  int32_t first_item; // index of its first full-size item (they are consecutive)
   int32_t b;          // sequence
-  int32_t pad[2];
+  int32_t n_full;     // full-size items
+  int32_t rem_item;   // index of its shorter last item, or -1
 };
 
 struct Item {
@@ -69,6 +76,12 @@ struct PlanHeader {
   int32_t counter;    // dynamic work counter (reset by the planner)
   int32_t pad[60];
 };
+
+// Item index of split s of a unit (items are emitted longest first: every unit's full-size
+// chunks, then the shorter remainders).
+__device__ __forceinline__ int32_t unit_item(const Unit& u, int32_t s) {
+  return s < u.n_full ? u.first_item + s : u.rem_item;
+}
 
 __device__ __forceinline__ int32_t unit_entry(const Unit& u, int32_t v) {
   return v < u.e_sink ? v : u.e_w + (v - u.e_sink);

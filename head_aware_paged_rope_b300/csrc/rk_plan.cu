@@ -174,38 +174,49 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
   __syncthreads();
   const int chunk = s_chunk;
 
-  // 4. items
-  carry = 0;
+  // 4. items, longest first: the full-size chunks of every unit, then each unit's shorter
+  //    last chunk (or its only, empty, item)
+  int carry_full = 0, carry_rem = 0;
   for (int base = 0; base < n_units; base += kPlanThreads) {
     const int u = base + tid;
-    int ns = 0;
+    int nf = 0, rm = 0;
     if (u < n_units) {
       const int nv = ws.units[u].n_vis;
-      ns = nv > 0 ? (nv + chunk - 1) / chunk : 1;
+      nf = nv / chunk;
+      rm = (nv % chunk != 0 || nv == 0) ? 1 : 0;
     }
-    int total;
-    const int pre = block_exclusive_scan(ns, &total, s_warp);
+    int tot_f, tot_r;
+    const int pre_f = block_exclusive_scan(nf, &tot_f, s_warp);
+    const int pre_r = block_exclusive_scan(rm, &tot_r, s_warp);
     if (u < n_units) {
-      const int first = carry + pre;
-      ws.units[u].n_splits = ns;
-      ws.units[u].first_item = first;
-      const int nv = ws.units[u].n_vis;
-      for (int s = 0; s < ns; ++s) {
-        const int it = first + s;
-        if (it >= ws.max_items) { report(p.status, RK_ERR_DEVICE_BOUNDS); break; }
-        Item item;
-        item.unit = u;
-        item.v_begin = s * chunk;
-        item.v_end = min(nv, (s + 1) * chunk);
-        item.split = s;
-        ws.items[it] = item;
-      }
+      ws.units[u].n_full = nf;
+      ws.units[u].n_splits = nf + rm;
+      ws.units[u].first_item = carry_full + pre_f;
+      ws.units[u].rem_item = rm ? carry_rem + pre_r : -1;   // made absolute below
     }
-    carry += total;
+    carry_full += tot_f;
+    carry_rem += tot_r;
+  }
+  __syncthreads();
+  const int n_items_all = carry_full + carry_rem;
+  for (int u = tid; u < n_units; u += kPlanThreads) {
+    Unit& un = ws.units[u];
+    if (un.rem_item >= 0) un.rem_item += carry_full;
+    const int nv = un.n_vis;
+    for (int s = 0; s < un.n_splits; ++s) {
+      const int it = unit_item(un, s);
+      if (it >= ws.max_items) { report(p.status, RK_ERR_DEVICE_BOUNDS); break; }
+      Item item;
+      item.unit = u;
+      item.v_begin = s * chunk;
+      item.v_end = min(nv, (s + 1) * chunk);
+      item.split = s;
+      ws.items[it] = item;
+    }
   }
   if (tid == 0) {
     ws.header->n_units = n_units;
-    ws.header->n_items = min(carry, ws.max_items);
+    ws.header->n_items = min(n_items_all, ws.max_items);
     ws.header->chunk = chunk;
     ws.header->counter = 0;
   }
@@ -220,18 +231,18 @@ __global__ __launch_bounds__(256) void combine_kernel(AttnParams p, AttnWorkspac
   const int G = p.G;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit un = ws.units[u];
-    if (un.n_splits <= 1 || un.first_item + un.n_splits > ws.max_items) continue;
+    if (un.n_splits <= 1) continue;
     const int rows = un.ntok * G;
     const int h = un.seg % p.Hkv;
     for (int r = warp; r < rows; r += warps) {
       float m = -INFINITY;
       for (int s = 0; s < un.n_splits; ++s)
-        m = fmaxf(m, ws.part_lse[int64_t(un.first_item + s) * ws.rows + r]);
+        m = fmaxf(m, ws.part_lse[int64_t(unit_item(un, s)) * ws.rows + r]);
       float wsum = 0.f;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       const int per_lane = p.d / 32;   // 2 or 4
       for (int s = 0; s < un.n_splits; ++s) {
-        const int64_t it = un.first_item + s;
+        const int64_t it = unit_item(un, s);
         const float l = ws.part_lse[it * ws.rows + r];
         const float w = (m == -INFINITY) ? 0.f : expf(l - m);
         wsum += w;

@@ -5,19 +5,24 @@
 // predicate, never as an attn_mask tensor ("小红书 RedKnot" section 3, fourth component;
 // "RedKnot" article, SegPagedAttention paragraph).
 //
-// One CTA = 6 warps working on items (rk_plan.cu) of 128 query rows (GQA-packed: 128/G
-// tokens x the G query heads of one KV head) against a slice of that head's page list:
-//   warp 4   producer: TMA loads the Q tile once per item, then for every 128-key tile
-//            gathers its pages (8 of 16 tokens or 4 of 32) from the shared pool through the
-//            page table, each page as one or two 64-column boxes, into a 2-stage ring;
-//   warp 5   MMA issuer: S = Q K^T into one of two TMEM buffers (128 columns each), then
-//            O += P V into a third TMEM region, one elected thread issuing tcgen05.mma;
-//   warps 0-3 softmax: thread r owns query row r = TMEM lane r; loads its S row, masks the
-//            edge, keeps a running maximum that is only moved when it grows by more than
-//            2^8 (so O needs rescaling rarely; then the thread rescales its O row in TMEM),
-//            writes P = 2^(S - m) as bf16 into shared memory (SW128 K-major, the MMA's A
-//            operand), and finally normalises O and stores it.
-// S of tile j+1 is computed while the softmax of tile j runs.  All waits are bounded.
+// Work items (rk_plan.cu, longest first) are taken from a counter; they are slices of the
+// page list of one unit: 256 query rows of one
+// KV head (GQA-packed: 256/G tokens x the G query heads), processed as two 128-row tiles
+// A and B that share every K/V tile loaded, which halves the K/V traffic per FLOP.
+// One CTA per SM, 10 warps:
+//   warp 8   producer: TMA loads the two Q tiles once per item, then for every 128-key
+//            tile gathers its pages (8 of 16 tokens or 4 of 32) from the shared pools
+//            through the page table, one box per page and 64 channels, into separate K
+//            and V rings (a K stage is freed as soon as both S tiles are computed);
+//   warp 9   MMA issuer (one thread): S_A = Q_A K^T and S_B = Q_B K^T into TMEM, then
+//            O_A += P_A V and O_B += P_B V with P read straight from TMEM;
+//   warps 0-3 / 4-7  softmax of tile A / B: thread r owns row r (TMEM lane r), loads its S
+//            row, masks the edge, keeps a running maximum that moves only when it grows by
+//            more than 2^8 (then the row of O is rescaled in TMEM), writes P = 2^(S - m) as
+//            bf16 pairs over the first half of its S columns, and at the end of the item
+//            normalises its O row and stores it (or a split partial).
+// TMEM: S_A cols 0-127, S_B 128-255, O_A 256-383, O_B 384-511.  The two softmax groups
+// work on S_A and S_B while the tensor core computes the other tile.  All waits are bounded.
 #include "rk_internal.cuh"
 #include "rk_sm100.cuh"
 
@@ -30,42 +35,54 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcThreads = 192;
-constexpr int kRowsTc = 128;
+constexpr int kTcThreads = 320;
+constexpr int kTileRows = 128;
+constexpr int kUnitRows = 256;
 constexpr int kKeysTc = 128;
-constexpr int kStages = 2;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr int kHalf = kTileRows * 128;      // bytes of one [128 rows][64] bf16 block
+constexpr uint64_t kWaitNs = 1000000000ull;
 
 template <int D>
 struct TcLayout {
-  static constexpr int kHalf = kRowsTc * 128;          // bytes of one [128 rows][64] bf16 block
-  static constexpr int kTile = kRowsTc * D * 2;        // Q, K or V tile
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
-  static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kP = kV + kStages * kTile;
-  static constexpr int kBytes = kP + kRowsTc * kKeysTc * 2;
-  static constexpr int kSmem = kBytes + 1024;          // slack for 1024-byte alignment
+  static constexpr int kTile = (D / 64) * kHalf;      // Q, K or V tile
+  static constexpr int kNK = D == 128 ? 2 : 4;        // K stages (freed once both S are computed)
+  static constexpr int kNV = D == 128 ? 3 : 4;        // V stages (held until the second value product)
+  static constexpr int kQ = 0;                        // Q_A, Q_B
+  static constexpr int kK = kQ + 2 * kTile;
+  static constexpr int kV = kK + kNK * kTile;
+  static constexpr int kBytes = kV + kNV * kTile;
+  static constexpr int kSmem = kBytes + 1024;         // slack for 1024-byte alignment
 };
 
 struct TcBarriers {
-  uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2];
-  uint64_t s_empty[2];
-  uint64_t p_full;
-  uint64_t o_done;
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t iq_full[2], iq_empty[2];   // item ring: producer -> MMA issuer and softmax warps
+  int ring[2];
   uint32_t tmem_slot;
   int abort;
 };
 
+__device__ __forceinline__ bool aborted(TcBarriers& b) { return *reinterpret_cast<volatile int*>(&b.abort) != 0; }
 __device__ __forceinline__ void fail(TcBarriers& b, int32_t* status) {
   report(status, RK_ERR_TIMEOUT);
   *reinterpret_cast<volatile int*>(&b.abort) = 1;
 }
-
-__device__ __forceinline__ bool aborted(TcBarriers& b) { return *reinterpret_cast<volatile int*>(&b.abort) != 0; }
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(TcBarriers& b, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (aborted(b)) return false;
+    if (globaltimer() - t0 > kWaitNs) return false;
+  }
+}
 
 template <int D, int P>
 __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -75,9 +92,9 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
   using LY = TcLayout<D>;
   constexpr int EPT = kKeysTc / P;       // pages per key tile
   constexpr int HALVES = D / 64;
-  constexpr int KSTEPS = D / 16;         // MMA k-steps of Q.K^T
-  constexpr uint32_t kIdescQK = idesc_bf16(kRowsTc, kKeysTc, 0);
-  constexpr uint32_t kIdescPV = idesc_bf16(kRowsTc, D, 1);
+  constexpr int NK = LY::kNK, NV = LY::kNV;
+  constexpr uint32_t kIdescQK = idesc_bf16(kTileRows, kKeysTc, 0);
+  constexpr uint32_t kIdescPV = idesc_bf16(kTileRows, D, 1);
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kColO = 256;
 
@@ -87,25 +104,35 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t sQ = sbase + LY::kQ, sK = sbase + LY::kK, sV = sbase + LY::kV, sP = sbase + LY::kP;
-  const uint32_t b_q = smem_addr(&bars.q_full), b_p = smem_addr(&bars.p_full), b_o = smem_addr(&bars.o_done);
+  const uint32_t sQ = sbase + LY::kQ, sK = sbase + LY::kK, sV = sbase + LY::kV;
 
   if (tid == 0) {
-    mbar_init(b_q, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_addr(&bars.kv_full[s]), 1);
-      mbar_init(smem_addr(&bars.kv_empty[s]), 1);
+    mbar_init(smem_addr(&bars.q_full), 1);
+    mbar_init(smem_addr(&bars.q_empty), 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(smem_addr(&bars.k_full[s]), 1);
+      mbar_init(smem_addr(&bars.k_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&bars.s_full[s]), 1);
-      mbar_init(smem_addr(&bars.s_empty[s]), 128);
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(smem_addr(&bars.v_full[s]), 1);
+      mbar_init(smem_addr(&bars.v_empty[s]), 1);
     }
-    mbar_init(b_p, 128);
-    mbar_init(b_o, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_addr(&bars.s_full[x]), 1);
+      mbar_init(smem_addr(&bars.p_full[x]), 128);
+      mbar_init(smem_addr(&bars.o_done[x]), 1);
+      mbar_init(smem_addr(&bars.iq_full[x]), 1);
+      mbar_init(smem_addr(&bars.iq_empty[x]), 257);
+    }
     bars.abort = 0;
     mbar_fence_init();
   }
-  if (warp == 5) {
+  if (warp == 8 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmQ) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmK) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmV) : "memory");
+  }
+  if (warp == 9) {
     tmem_alloc(smem_addr(&bars.tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -116,228 +143,378 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
   const int G = p.G;
   const int n_items = ws.header->n_items;
   const int64_t oob_row = p.n_pool_pages * P;      // a row index past the pool: TMA fills zeros
-  uint32_t g = 0;            // tiles processed by this CTA so far (all roles count alike)
-  uint32_t q_uses = 0;       // items with at least one tile
-  // last phase each role may still have in flight (for the bounded teardown)
-  int last_kv_stage = -1;
-  uint32_t last_kv_parity = 0;
-  bool mma_pending = false;
-  uint32_t mma_pending_parity = 0;
 
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const Item item = ws.items[it];
-    const Unit un = ws.units[item.unit];
-    const int seg = un.seg;
-    const int h = seg % p.Hkv;
-    const int n_kt = (item.v_end - item.v_begin + EPT - 1) / EPT;
-    const int32_t* trow = p.page_table + int64_t(seg) * p.max_pages;
-    const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
-
-    if (warp == 4 && lane == 0 && n_kt > 0 && !aborted(bars)) {
-      // ---------------------------------------------------------------- producer
-      mbar_arrive_expect_tx(b_q, LY::kTile);
+  if (warp == 8) {
+    // ---------------------------------------------------------------- producer
+    uint32_t gg = 0, qn = 0;
+    int last_k = -1, last_v = -1;
+    uint32_t last_k_par = 0, last_v_par = 0, last_q_par = 0;
+    bool q_pending = false, ok = true;
+    // items: blockIdx.x first, then from the counter (the next ticket is requested one item
+    // ahead); each is handed to the other roles through the 2-entry ring
+    int it = blockIdx.x, ticket = 0;
+    for (int k = 0; ok; ++k) {
+      if (k > 0) it = int(gridDim.x) + __shfl_sync(0xffffffffu, ticket, 0);   // requested one item ago
+      const int slot = k & 1;
+      bool gotr = true;
+      if (lane == 0 && k >= 2) gotr = wait_or_abort(bars, smem_addr(&bars.iq_empty[slot]), ((k >> 1) - 1) & 1);
+      if (!__shfl_sync(0xffffffffu, gotr, 0)) { ok = false; break; }
+      const bool valid = it < n_items;
+      if (lane == 0) {
+        bars.ring[slot] = valid ? it : -1;
+        mbar_arrive(smem_addr(&bars.iq_full[slot]));
+        if (valid) ticket = atomicAdd(&ws.header->counter, 1);
+      }
+      if (!valid) break;
+      const Item item = ws.items[it];
+      const Unit un = ws.units[item.unit];
+      const int n_kt = (item.v_end - item.v_begin + EPT - 1) / EPT;
+      if (n_kt == 0) continue;
+      const int h = un.seg % p.Hkv;
+      const int32_t* trow = p.page_table + int64_t(un.seg) * p.max_pages;
+      bool got = true;
+      if (lane == 0) {   // both Q tiles; the buffer is free once the previous item's S are computed
+        if (qn > 0) got = wait_or_abort(bars, smem_addr(&bars.q_empty), (qn - 1) & 1);
+        if (got) {
+          const uint32_t bar = smem_addr(&bars.q_full);
+          mbar_arrive_expect_tx(bar, 2 * LY::kTile);
 #pragma unroll
-      for (int hf = 0; hf < HALVES; ++hf) tma_load_3d(sQ + hf * LY::kHalf, &tmQ, hf * 64, h * G, un.tok0, b_q);
-      for (int j = 0; j < n_kt; ++j) {
-        const uint32_t gg = g + j;
-        const int st = gg % kStages;
-        const uint32_t full = smem_addr(&bars.kv_full[st]), empty = smem_addr(&bars.kv_empty[st]);
-        if (gg >= kStages && !mbar_wait(empty, ((gg / kStages) - 1) & 1)) { fail(bars, p.status); break; }
-        mbar_arrive_expect_tx(full, 2 * LY::kTile);
-        last_kv_stage = st;
-        last_kv_parity = (gg / kStages) & 1;
-        const int v0 = item.v_begin + j * EPT;
+          for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int pg = 0; pg < EPT; ++pg) {
-          const int v = v0 + pg;
-          int64_t row = oob_row;
-          if (v < item.v_end) {
-            const int page = __ldg(trow + unit_entry(un, v));
-            if (page >= 0 && page < p.n_pool_pages) row = int64_t(page) * P;
-            else report(p.status, RK_ERR_DEVICE_BOUNDS);
-          }
-#pragma unroll
-          for (int hf = 0; hf < HALVES; ++hf) {
-            const uint32_t off = st * LY::kTile + hf * LY::kHalf + pg * P * 128;
-            tma_load_2d(sK + off, &tmK, hf * 64, int(row), full);
-            tma_load_2d(sV + off, &tmV, hf * 64, int(row), full);
-          }
+            for (int hf = 0; hf < HALVES; ++hf)
+              tma_load_3d(sQ + x * LY::kTile + hf * kHalf, &tmQ, hf * 64, h * G, un.tok0 + x * (kTileRows / G), bar);
+          q_pending = true;
+          last_q_par = qn & 1;
         }
       }
-    } else if (warp == 5 && lane == 0 && n_kt > 0 && !aborted(bars)) {
-      // ---------------------------------------------------------------- MMA issuer
-      bool ok = mbar_wait(b_q, q_uses & 1);
-      tc_fence_after();
-      auto issue_pv = [&](int jj) -> bool {
-        const uint32_t gg = g + jj;
-        const int st = gg % kStages;
-        if (!mbar_wait(b_p, gg & 1)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sV + st * LY::kTile;
-#pragma unroll
-        for (int k = 0; k < kKeysTc / 16; ++k) {
-          const uint64_t a = desc_sw128(sP + (k >> 2) * LY::kHalf + (k & 3) * 32, 16, 1024);
-          const uint64_t b = desc_sw128(vbase + k * 2048, LY::kHalf, 1024);
-          tc_mma_f16(tmem + kColO, a, b, kIdescPV, (jj > 0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(b_o);
-        tc_commit(smem_addr(&bars.kv_empty[st]));
-        mma_pending = true;
-        mma_pending_parity = gg & 1;
-        return true;
+      if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+      ++qn;
+      // page ids of 32 list entries at a time, the next group requested one group ahead
+      constexpr int TPG = 32 / EPT;
+      const int n_grp = (n_kt + TPG - 1) / TPG;
+      auto fetch = [&](int grp, int& raw, bool& present) {
+        const int v = item.v_begin + grp * 32 + lane;
+        present = v < item.v_end;
+        raw = present ? __ldg(trow + unit_entry(un, v)) : -1;
       };
-      for (int j = 0; ok && j < n_kt; ++j) {
-        const uint32_t gg = g + j;
-        const int st = gg % kStages, sb = gg & 1;
-        if (!mbar_wait(smem_addr(&bars.kv_full[st]), (gg / kStages) & 1)) { ok = false; break; }
-        if (gg >= 2 && !mbar_wait(smem_addr(&bars.s_empty[sb]), ((gg >> 1) - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kbase = sK + st * LY::kTile;
+      int raw;
+      bool present;
+      fetch(0, raw, present);
+      for (int grp = 0; ok && grp < n_grp; ++grp) {
+        int raw_n = -1;
+        bool present_n = false;
+        if (grp + 1 < n_grp) fetch(grp + 1, raw_n, present_n);
+        const bool page_ok = present && raw >= 0 && raw < p.n_pool_pages;
+        if (present && !page_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
+        const int64_t row = page_ok ? int64_t(raw) * P : oob_row;
+        const int tiles = min(TPG, n_kt - grp * TPG);
+        for (int jt = 0; jt < tiles; ++jt, ++gg) {
+          const int sk = gg % NK, sv = gg % NV;
+          const int pg = lane - jt * EPT;
+          got = true;
+          if (lane == 0) {
+            if (gg >= NK) got = wait_or_abort(bars, smem_addr(&bars.k_empty[sk]), ((gg / NK) - 1) & 1);
+            if (got) {
+              mbar_arrive_expect_tx(smem_addr(&bars.k_full[sk]), LY::kTile);
+              last_k = sk;
+              last_k_par = (gg / NK) & 1;
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+          if (pg >= 0 && pg < EPT)
 #pragma unroll
-        for (int k = 0; k < KSTEPS; ++k) {
-          const uint64_t a = desc_sw128(sQ + (k >> 2) * LY::kHalf + (k & 3) * 32, 16, 1024);
-          const uint64_t b = desc_sw128(kbase + (k >> 2) * LY::kHalf + (k & 3) * 32, 16, 1024);
-          tc_mma_f16(tmem + sb * kKeysTc, a, b, kIdescQK, k > 0 ? 1u : 0u);
+            for (int hf = 0; hf < HALVES; ++hf)
+              tma_load_2d(sK + sk * LY::kTile + hf * kHalf + pg * P * 128, &tmK, hf * 64, int(row),
+                          smem_addr(&bars.k_full[sk]));
+          if (lane == 0) {
+            if (gg >= NV) got = wait_or_abort(bars, smem_addr(&bars.v_empty[sv]), ((gg / NV) - 1) & 1);
+            if (got) {
+              mbar_arrive_expect_tx(smem_addr(&bars.v_full[sv]), LY::kTile);
+              last_v = sv;
+              last_v_par = (gg / NV) & 1;
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+          if (pg >= 0 && pg < EPT)
+#pragma unroll
+            for (int hf = 0; hf < HALVES; ++hf)
+              tma_load_2d(sV + sv * LY::kTile + hf * kHalf + pg * P * 128, &tmV, hf * 64, int(row),
+                          smem_addr(&bars.v_full[sv]));
         }
-        tc_commit(smem_addr(&bars.s_full[sb]));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        raw = raw_n;
+        present = present_n;
       }
-      if (ok) ok = issue_pv(n_kt - 1);
+    }
+    if (!ok && lane == 0) fail(bars, p.status);
+    // copies still in flight after an abort: let them land before the CTA exits (bounded)
+    if (lane == 0 && aborted(bars)) {
+      if (last_k >= 0) mbar_wait(smem_addr(&bars.k_full[last_k]), last_k_par);
+      if (last_v >= 0) mbar_wait(smem_addr(&bars.v_full[last_v]), last_v_par);
+      if (q_pending) mbar_wait(smem_addr(&bars.q_full), last_q_par);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t gg = 0, qn = 0;
+      bool ok = true, pending = false;
+      uint32_t pend_bar = 0, pend_par = 0;
+      for (int k = 0; ok; ++k) {
+        if (!wait_or_abort(bars, smem_addr(&bars.iq_full[k & 1]), (k >> 1) & 1)) { ok = false; break; }
+        const int it = bars.ring[k & 1];
+        mbar_arrive(smem_addr(&bars.iq_empty[k & 1]));
+        if (it < 0) break;
+        const Item item = ws.items[it];
+        const int n_kt = (item.v_end - item.v_begin + EPT - 1) / EPT;
+        if (n_kt == 0) continue;
+        if (!wait_or_abort(bars, smem_addr(&bars.q_full), qn & 1)) { ok = false; break; }
+        ++qn;
+        tc_fence_after();
+        // order per tile j: S_A(j), O_B += P_B V (j-1), S_B(j), O_A += P_A V (j): the softmax of
+        // one tile runs while the tensor core works for the other
+        auto qk = [&](int x, uint32_t g1, uint32_t kb) -> bool {
+          // S_x holds P_x of the previous tile until its value product has completed
+          if (g1 >= 1 && !wait_or_abort(bars, smem_addr(&bars.o_done[x]), (g1 - 1) & 1)) return false;
+          tc_fence_after();
+          const uint32_t qb = sQ + x * LY::kTile;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t a = desc_sw128(qb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+            const uint64_t b = desc_sw128(kb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+            tc_mma_f16(tmem + x * kKeysTc, a, b, kIdescQK, k > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_addr(&bars.s_full[x]));
+          return true;
+        };
+        auto pv = [&](int x, uint32_t g1, bool first) -> bool {
+          const int sv = g1 % NV;
+          if (!wait_or_abort(bars, smem_addr(&bars.v_full[sv]), (g1 / NV) & 1)) return false;
+          if (!wait_or_abort(bars, smem_addr(&bars.p_full[x]), g1 & 1)) return false;
+          tc_fence_after();
+          const uint32_t vb = sV + sv * LY::kTile;
+#pragma unroll
+          for (int k = 0; k < kKeysTc / 16; ++k) {
+            const uint64_t b = desc_sw128(vb + k * 2048, kHalf, 1024);
+            tc_mma_f16_ts(tmem + kColO + x * 128, tmem + x * kKeysTc + k * 8, b, kIdescPV, (!first || k > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_addr(&bars.o_done[x]));
+          if (x == 1) tc_commit(smem_addr(&bars.v_empty[sv]));   // both value products of tile g1 issued
+          pending = true;
+          pend_bar = smem_addr(&bars.o_done[x]);
+          pend_par = g1 & 1;
+          return true;
+        };
+        const uint32_t g_first = gg;
+        for (int j = 0; j < n_kt; ++j, ++gg) {
+          const int sk = gg % NK;
+          if (!wait_or_abort(bars, smem_addr(&bars.k_full[sk]), (gg / NK) & 1)) { ok = false; break; }
+          const uint32_t kb = sK + sk * LY::kTile;
+          if (!qk(0, gg, kb)) { ok = false; break; }
+          if (j >= 1 && !pv(1, gg - 1, gg - 1 == g_first)) { ok = false; break; }
+          if (!qk(1, gg, kb)) { ok = false; break; }
+          tc_commit(smem_addr(&bars.k_empty[sk]));
+          if (j == n_kt - 1) tc_commit(smem_addr(&bars.q_empty));
+          if (!pv(0, gg, j == 0)) { ok = false; break; }
+        }
+        if (ok && !pv(1, gg - 1, n_kt == 1)) ok = false;
+      }
       if (!ok) fail(bars, p.status);
-    } else if (warp < 4) {
-      // ---------------------------------------------------------------- softmax + epilogue
-      const int r = tid;                       // query row = TMEM lane
+      if (pending && aborted(bars)) mbar_wait(pend_bar, pend_par);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax + epilogue
+    const int x = warp >> 2;                 // tile A (warps 0-3) or B (warps 4-7)
+    const int r = tid & 127;                 // row of the tile = TMEM lane
+    const int R = x * kTileRows + r;         // row of the unit
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t colS = x * kKeysTc, colO = kColO + x * 128;
+    uint32_t gg = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const bool got_it = wait_or_abort(bars, smem_addr(&bars.iq_full[k & 1]), (k >> 1) & 1);
+      if (!__all_sync(0xffffffffu, got_it)) { ok = false; break; }
+      const int it = bars.ring[k & 1];
+      mbar_arrive(smem_addr(&bars.iq_empty[k & 1]));
+      if (it < 0) break;
+      const Item item = ws.items[it];
+      const Unit un = ws.units[item.unit];
+      const int n_kt = (item.v_end - item.v_begin + EPT - 1) / EPT;
+      const int seg = un.seg;
+      const int h = seg % p.Hkv;
+      const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
       const int rows_valid = un.ntok * G;
-      const int pos = un.pos0 + r / G;
+      const int pos = un.pos0 + R / G;
       const int L = __ldg(p.seq_len + un.b);
       const int cls = __ldg(p.head_class + seg);
       const bool local = cls == RK_CLASS_LOCAL;
       const int W = local ? __ldg(p.window + seg) : 0;
       const int S = (local && p.sink) ? __ldg(p.sink + seg) : 0;
-      const uint32_t lane_base = uint32_t(warp * 32) << 16;
       float m_ref = -INFINITY, l_sum = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n_kt; ++j) {
-        const uint32_t gg = g + j;
-        const int sb = gg & 1;
-        // waits are made warp-uniform: tcgen05.ld/st below are warp-collective
-        const bool got = !aborted(bars) && mbar_wait(smem_addr(&bars.s_full[sb]), (gg >> 1) & 1);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-        tc_fence_after();
-        float x[kKeysTc];
-#pragma unroll
-        for (int c = 0; c < kKeysTc / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + sb * kKeysTc + c * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(v[i]) * p.scale_log2;
-        }
-        tc_fence_before();
-        mbar_arrive(smem_addr(&bars.s_empty[sb]));
-
-        // visibility of this tile's keys for this row
+      // logical pages of the entries of tile j, requested one tile ahead
+      auto load_lp = [&](int j, int (&lp)[EPT]) {
         const int v0 = item.v_begin + j * EPT;
-        int lp[EPT];
-        bool all_valid = true;
 #pragma unroll
         for (int pg = 0; pg < EPT; ++pg) {
           const int v = v0 + pg;
-          if (v < item.v_end) {
+          lp[pg] = -1;
+          if (j < n_kt && v < item.v_end) {
             const int e = unit_entry(un, v);
             lp[pg] = lrow ? __ldg(lrow + e) : e;
-          } else {
-            lp[pg] = -1;
-            all_valid = false;
           }
         }
-        const int j_min = lp[0] * P;
-        int lp_last = lp[0];
+      };
+      int lp_next[EPT];
+      load_lp(0, lp_next);
+      for (int j = 0; j < n_kt; ++j, ++gg) {
+        int lp[EPT];
 #pragma unroll
-        for (int pg = 0; pg < EPT; ++pg) lp_last = lp[pg] >= 0 ? lp[pg] : lp_last;
-        const int j_max = lp_last * P + P - 1;
-        const bool full = all_valid && j_max <= pos && j_max < L && (!local || j_min > pos - W || j_max < S);
+        for (int pg = 0; pg < EPT; ++pg) lp[pg] = lp_next[pg];
+        load_lp(j + 1, lp_next);
+        const bool got = wait_or_abort(bars, smem_addr(&bars.s_full[x]), gg & 1);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after();
+        // visibility of the tile's keys for this row: the whole tile (the common case) is
+        // settled from its first and last page; otherwise one bit per slot of each page
+        constexpr uint32_t kAll = P == 32 ? 0xffffffffu : 0xffffu;
+        bool full;
+        {
+          bool all_listed = true;
+          int lp_last = lp[0];
+#pragma unroll
+          for (int pg = 0; pg < EPT; ++pg) {
+            all_listed &= lp[pg] >= 0;
+            lp_last = lp[pg] >= 0 ? lp[pg] : lp_last;
+          }
+          const int j_min = lp[0] * P, j_max = lp_last * P + P - 1;
+          full = all_listed && j_max <= pos && j_max < L && (!local || j_min > pos - W || j_max < S);
+        }
+        uint32_t pm[EPT];
         if (!full) {
 #pragma unroll
-          for (int c = 0; c < kKeysTc; ++c) {
-            const int lpc = lp[c / P];
-            const int jj = lpc * P + (c % P);
-            const bool vis = lpc >= 0 && jj < L && jj <= pos && (!local || jj > pos - W || jj < S);
-            if (!vis) x[c] = -INFINITY;
+          for (int pg = 0; pg < EPT; ++pg) {
+            uint32_t m = 0u;
+            if (lp[pg] >= 0) {
+              const int base = lp[pg] * P;
+              const int hi = min(pos, L - 1) - base;          // last visible slot (causal, length)
+              m = hi < 0 ? 0u : (hi >= P - 1 ? kAll : (2u << hi) - 1u);
+              if (local) {
+                const int lo = pos - W + 1 - base;            // first slot inside the window
+                const int sk = S - base;                      // slots before this are sink
+                const uint32_t wm = lo <= 0 ? kAll : (lo >= P ? 0u : kAll & ~((1u << lo) - 1u));
+                const uint32_t sm = sk <= 0 ? 0u : (sk >= P ? kAll : (1u << sk) - 1u);
+                m &= wm | sm;
+              }
+            }
+            pm[pg] = m;
           }
         }
-        float mx = x[0];
+        // pass 1 over S in TMEM: the row maximum (64 columns per load round, 3-input max)
+        const float sc = p.scale_log2;
+        float mx = -INFINITY;
 #pragma unroll
-        for (int c = 1; c < kKeysTc; ++c) mx = fmaxf(mx, x[c]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[64];
+          tmem_ld32(tmem + lane_base + colS + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tmem + lane_base + colS + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmax3(mx, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int c0 = h2 * 64 + 2 * i, c1 = c0 + 1;
+              const float a0 = (pm[c0 / P] >> (c0 % P)) & 1u ? __uint_as_float(v[2 * i]) : -INFINITY;
+              const float a1 = (pm[c1 / P] >> (c1 % P)) & 1u ? __uint_as_float(v[2 * i + 1]) : -INFINITY;
+              mx = fmax3(mx, a0, a1);
+            }
+          }
+        }
+        mx *= sc;
         const float m_new = fmaxf(m_ref, mx);
         const bool rescale = m_new > m_ref + kRescaleThreshold;   // false while both are -inf
-
-        if (j > 0) {
-          const bool got_o = mbar_wait(b_o, (gg - 1) & 1);
-          if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, rescale)) {
-            const float alpha = rescale ? fast_exp2(m_ref - m_new) : 1.f;
+        // O_x already holds earlier tiles of this item (their value products completed before
+        // this S was computed): rescale the rows whose maximum moved
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+          const float alpha = rescale ? fast_exp2(m_ref - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + colO + c * 32, v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_base + kColO + c * 32, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(tmem + lane_base + kColO + c * 32, v);
-            }
-            tmem_wait_st();
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tmem + lane_base + colO + c * 32, v);
           }
+          tmem_wait_st();
         }
         if (rescale) {
           l_sum = (m_ref == -INFINITY) ? 0.f : l_sum * fast_exp2(m_ref - m_new);
           m_ref = m_new;
         }
         const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-        // P row -> shared memory, SW128 K-major: 16-byte chunk c of row r at
-        // half (c / 8), row offset r * 128, chunk slot (c % 8) ^ (r % 8)
-        float psum = 0.f;
+        // pass 2: P = 2^(S - m) as bf16 pairs; the 32 scores of chunk c become packed columns
+        // 16c .. 16c+15, which only overwrite scores already read
+        const float nref = -ref;
+        float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kKeysTc / 8; ++c) {
-          float e[8];
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[64];
+          tmem_ld32(tmem + lane_base + colS + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tmem + lane_base + colS + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            e[i] = fast_exp2(x[c * 8 + i] - ref);
-            psum += e[i];
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = h2 * 2 + c2;
+            uint32_t w[16];
+            if (full) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float e0 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i]), sc, nref));
+                const float e1 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i + 1]), sc, nref));
+                ps0 += e0;
+                ps1 += e1;
+                w[i] = pack_bf16(e0, e1);
+              }
+            } else {
+              const uint32_t bits = pm[(c * 32) / P] >> ((c * 32) % P);
+              const uint32_t cm = P == 16 ? (bits & 0xffffu) | (pm[(c * 32) / P + 1] << 16) : bits;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float e0 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i]), sc, nref));
+                float e1 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i + 1]), sc, nref));
+                e0 = (cm >> (2 * i)) & 1u ? e0 : 0.f;
+                e1 = (cm >> (2 * i + 1)) & 1u ? e1 : 0.f;
+                ps0 += e0;
+                ps1 += e1;
+                w[i] = pack_bf16(e0, e1);
+              }
+            }
+            tmem_st16(tmem + lane_base + colS + c * 16, w);
           }
-          uint4 w;
-          w.x = pack_bf16(e[0], e[1]);
-          w.y = pack_bf16(e[2], e[3]);
-          w.z = pack_bf16(e[4], e[5]);
-          w.w = pack_bf16(e[6], e[7]);
-          const uint32_t addr = sP + (c >> 3) * LY::kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(w.x), "r"(w.y), "r"(w.z),
-                       "r"(w.w) : "memory");
         }
+        const float psum = ps0 + ps1;
         l_sum += psum;
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(b_p);
+        mbar_arrive(smem_addr(&bars.p_full[x]));
       }
-      // epilogue: O / l -> output (or split partial)
-      if (ok && n_kt > 0) {
-        const bool got_o = mbar_wait(b_o, (g + n_kt - 1) & 1);
-        if (!__all_sync(0xffffffffu, got_o)) ok = false;
+      if (!ok) break;
+      // epilogue: O / l -> output (or split partial), 32 columns at a time
+      if (n_kt > 0) {
+        const bool got_o = wait_or_abort(bars, smem_addr(&bars.o_done[x]), (gg - 1) & 1);
+        if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
         tc_fence_after();
       }
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) fail(bars, p.status);
       const bool split = un.n_splits > 1;
+      const bool row_ok = R < rows_valid;
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       const float lse = l_sum > 0.f ? (m_ref + fast_log2(l_sum)) * 0.69314718055994531f : -INFINITY;
-      const bool row_ok = r < rows_valid;
-      const int t = un.tok0 + r / G, hq = h * G + r % G;
+      const int t = un.tok0 + R / G, hq = h * G + R % G;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        if (ok && n_kt > 0) {
-          tmem_ld32(tmem + lane_base + kColO + c * 32, v);
+        if (n_kt > 0) {
+          tmem_ld32(tmem + lane_base + colO + c * 32, v);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -356,7 +533,7 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
             *reinterpret_cast<uint4*>(orow + i) = w;
           }
         } else {
-          float* prow = ws.part_o + (int64_t(it) * ws.rows + r) * D + c * 32;
+          float* prow = ws.part_o + (int64_t(it) * ws.rows + R) * D + c * 32;
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(prow + i) =
@@ -364,29 +541,20 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
                             __uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
         }
       }
+      tc_fence_before();
       if (row_ok) {
         if (!split) {
           if (p.lse) p.lse[int64_t(t) * p.Hq + hq] = lse;
         } else {
-          ws.part_lse[int64_t(it) * ws.rows + r] = lse;
+          ws.part_lse[int64_t(it) * ws.rows + R] = lse;
         }
       }
-      tc_fence_before();
     }
-    if (n_kt > 0) {
-      g += n_kt;
-      ++q_uses;
-    }
-    __syncthreads();
-    if (aborted(bars)) break;
+    if (!ok && lane == 0) fail(bars, p.status);
   }
 
-  // teardown: let this CTA's own copies and MMAs land (bounded), then free TMEM
-  if (warp == 4 && lane == 0 && last_kv_stage >= 0 && aborted(bars))
-    mbar_wait(smem_addr(&bars.kv_full[last_kv_stage]), last_kv_parity);
-  if (warp == 5 && lane == 0 && mma_pending && aborted(bars)) mbar_wait(b_o, mma_pending_parity);
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -399,7 +567,7 @@ cudaError_t launch_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cu
   CUtensorMap mq, mk, mv;
   const cuuint64_t qdims[3] = {cuuint64_t(D), cuuint64_t(p.Hq), cuuint64_t(p.total_q)};
   const cuuint64_t qstr[2] = {cuuint64_t(D) * 2, cuuint64_t(p.Hq) * D * 2};
-  const cuuint32_t qbox[3] = {64, cuuint32_t(p.G), cuuint32_t(kRowsTc / p.G)};
+  const cuuint32_t qbox[3] = {64, cuuint32_t(p.G), cuuint32_t(kTileRows / p.G)};
   const cuuint64_t kdims[2] = {cuuint64_t(D), cuuint64_t(p.n_pool_pages) * P};
   const cuuint64_t kstr[1] = {cuuint64_t(D) * 2};
   const cuuint32_t kbox[2] = {64, cuuint32_t(P)};
@@ -443,7 +611,7 @@ bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int prefill_tc_rows() { return kRowsTc; }
+int prefill_tc_rows() { return kUnitRows; }
 int prefill_tc_keys() { return kKeysTc; }
 
 cudaError_t launch_prefill_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cudaStream_t stream) {
