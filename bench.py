@@ -242,8 +242,8 @@ class LayerState:
                 n_pages=da.n_pages.data_ptr(), head_class=da.head_class.data_ptr(), window=da.window.data_ptr(),
                 sink=da.sink.data_ptr(), B=1, Hq=a.Hq, Hkv=a.Hkv, d=a.d, P=a.P, max_pages=da.page_table.shape[1],
                 total_q=1, max_q=1, scale=0.0, out=self.dec_out[s].data_ptr(), lse=self.dec_lse[s].data_ptr(),
-                status=self.status.data_ptr()))
-        self.dec_ws = torch.empty(max(1, rk.segpaged_decode_workspace_size(self.dec_args[0])) if n_dec else 1,
+                status=self.status.data_ptr(), flags=rk.RK_ATTN_METADATA_STABLE))
+        self.dec_ws = torch.zeros(max(1, rk.segpaged_decode_workspace_size(self.dec_args[0])) if n_dec else 1,
                                   dtype=torch.uint8, device=dev)
 
     # host copies for the end-to-end leg: (device tensor, pinned host tensor) pairs
@@ -288,7 +288,8 @@ def enqueue(rk, layers, stream_handle, phase):
         for s in range(n_dec):
             for L in layers:
                 _call(rk.LIB.rk_segpaged_decode, L.dec_args[s], L.dec_ws, stream_handle)
-                n += 3
+                # one kernel for up to 512 head segments (B * Hkv), else planner + attention + merge
+                n += 1 if L.dec_args[s].B * L.dec_args[s].Hkv <= 512 else 3
     return n
 
 
@@ -516,9 +517,9 @@ def case_main(args):
     else:
         decode = args.case in ("decode_microbench", "stack_decode")
         da = attn_to_device(wl.attn, dev)
-        base = da.args(rk, decode=decode, status=st)
+        base = da.args(rk, decode=decode, status=st, flags=rk.RK_ATTN_METADATA_STABLE if decode else 0)
         n = (rk.segpaged_decode_workspace_size if decode else rk.segpaged_prefill_workspace_size)(base)
-        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        ws = torch.zeros(n, dtype=torch.uint8, device=dev)
         fn = rk.segpaged_decode if decode else rk.segpaged_prefill
         if decode:
             work, unit = roofline.decode_kv_bytes(wl.attn) / 1e9, "GB/s"

@@ -18,6 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librk.so")
 RK_OK, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED, RK_ERR_CUDA, RK_ERR_DEVICE_BOUNDS, RK_ERR_TIMEOUT, RK_ERR_WORKSPACE = range(7)
 RK_CLASS_GLOBAL, RK_CLASS_LOCAL, RK_CLASS_RETRIEVAL, RK_CLASS_DENSE = range(4)
 RK_ROPE_HALF_SPLIT, RK_ROPE_INTERLEAVED = 0, 1
+RK_ATTN_METADATA_STABLE = 1
 
 
 class RkError(RuntimeError):
@@ -52,6 +53,7 @@ class AttnArgs(ctypes.Structure):
         ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32),
         ("P", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q", ctypes.c_int32),
         ("scale", ctypes.c_float), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("flags", ctypes.c_int32),
     ]
 
 
@@ -101,12 +103,12 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor], zeroed: bool = False) -> Optional[torch.Tensor]:
     if nbytes == 0:
         return workspace
     if workspace is not None:
         return workspace
-    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return (torch.zeros if zeroed else torch.empty)(nbytes, dtype=torch.uint8, device=device)
 
 
 def _check(code: int, where: str) -> None:
@@ -134,7 +136,8 @@ def rope_reposition(k_src: torch.Tensor, k_dst: torch.Tensor, src_tables: torch.
 
 
 def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, head_class, window, sink, out,
-              *, cu_seqlens_q=None, lse=None, status=None, total_q: int, max_q: int, scale: float = 0.0) -> AttnArgs:
+              *, cu_seqlens_q=None, lse=None, status=None, total_q: int, max_q: int, scale: float = 0.0,
+              flags: int = 0) -> AttnArgs:
     B = seq_len.shape[0]
     Hq, d = q.shape[1], q.shape[2]
     Hkv = n_pages.shape[0] // max(B, 1)
@@ -143,7 +146,7 @@ def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, hea
                     page_logical=_ptr(page_logical), n_pages=_ptr(n_pages), head_class=_ptr(head_class),
                     window=_ptr(window), sink=_ptr(sink), B=B, Hq=Hq, Hkv=Hkv, d=d, P=k_pool.shape[1],
                     max_pages=page_table.shape[1], total_q=int(total_q), max_q=int(max_q), scale=float(scale),
-                    out=_ptr(out), lse=_ptr(lse), status=_ptr(status))
+                    out=_ptr(out), lse=_ptr(lse), status=_ptr(status), flags=int(flags))
 
 
 def segpaged_prefill_workspace_size(args: AttnArgs) -> int:
@@ -162,8 +165,10 @@ def segpaged_prefill(args: AttnArgs, *, device=None, workspace: Optional[torch.T
 
 
 def segpaged_decode(args: AttnArgs, *, device=None, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """A caller-owned `workspace` must be zero-filled before its first decode call; each call
+    leaves its split counters at zero, so it can be reused by later decode calls."""
     n = segpaged_decode_workspace_size(args)
-    ws = _workspace(n, device or torch.device("cuda"), workspace)
+    ws = _workspace(n, device or torch.device("cuda"), workspace, zeroed=True)
     _check(LIB.rk_segpaged_decode(ctypes.byref(args), _ptr(ws), ws.numel() if ws is not None else 0,
                                   _stream(stream)), "rk_segpaged_decode")
 

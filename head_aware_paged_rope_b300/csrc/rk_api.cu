@@ -84,6 +84,7 @@ rk_status check_attn(const rk_attn_args* a, bool decode) {
   if (a->n_pool_pages * int64_t(a->P) >= (int64_t(1) << 31) || int64_t(a->total_q) * a->Hq >= (int64_t(1) << 31))
     return RK_ERR_UNSUPPORTED;   // row coordinates of the tensor maps are int32
   if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
+  if (a->flags & ~RK_ATTN_METADATA_STABLE) return RK_ERR_INVALID_ARG;
   return RK_OK;
 }
 
@@ -145,6 +146,7 @@ AttnParams make_params(const rk_attn_args* a, const AttnLayout& l) {
   p.out = static_cast<__nv_bfloat16*>(a->out);
   p.lse = a->lse;
   p.status = a->status;
+  p.flags = a->flags;
   return p;
 }
 
@@ -163,18 +165,25 @@ AttnWorkspace make_ws(void* base, const AttnLayout& l) {
 }
 
 // Workspace of the tcgen05 decode path.
+// The split counters sit at the same offset for every decode shape, so that one workspace
+// serves any sequence of decode calls.
 struct DecLayoutHost {
   int nseg, grid, max_slots;
-  size_t off_segs, off_ctas, off_split, off_lse, off_o, total;
+  size_t off_counters, off_segs, off_ctas, off_split, off_lse, off_o, off_glse, off_go, total;
 };
 
 DecLayoutHost dec_layout(const rk_attn_args* a) {
   DecLayoutHost l{};
   const int G = a->Hq / a->Hkv;
   l.nseg = a->B * a->Hkv;
-  l.grid = device_sm_count();
-  l.max_slots = l.nseg + l.grid;   // every CTA boundary splits at most one more segment
+  l.grid = std::min(device_sm_count(), kDecMaxGrid);
+  // separate planner: every CTA boundary splits at most one more segment;
+  // single launch: two slots per CTA (its first and its last portion)
+  l.max_slots = std::max(l.nseg + l.grid, 2 * l.grid);
+  static_assert(sizeof(DecHeader) == 256, "the split counters start at byte 256");
   size_t off = align256(sizeof(DecHeader));
+  l.off_counters = off;
+  off += align256(sizeof(int32_t) * size_t(3 * kDecMaxGrid));   // ends at kDecCounterBytes
   l.off_segs = off;
   off += align256(sizeof(DecSeg) * size_t(l.nseg));
   l.off_ctas = off;
@@ -185,6 +194,10 @@ DecLayoutHost dec_layout(const rk_attn_args* a) {
   off += align256(sizeof(float) * size_t(l.max_slots) * G);
   l.off_o = off;
   off += align256(sizeof(float) * size_t(l.max_slots) * G * a->d);
+  l.off_glse = off;
+  off += align256(sizeof(float) * size_t(2 * l.grid) * G);
+  l.off_go = off;
+  off += align256(sizeof(float) * size_t(2 * l.grid) * G * a->d);
   l.total = off;
   return l;
 }
@@ -193,11 +206,14 @@ DecWorkspace make_dec_ws(void* base, const DecLayoutHost& l) {
   uint8_t* b = static_cast<uint8_t*>(base);
   DecWorkspace ws;
   ws.header = reinterpret_cast<DecHeader*>(b);
+  ws.counters = reinterpret_cast<int32_t*>(b + l.off_counters);
   ws.segs = reinterpret_cast<DecSeg*>(b + l.off_segs);
   ws.ctas = reinterpret_cast<DecCta*>(b + l.off_ctas);
   ws.split_segs = reinterpret_cast<int32_t*>(b + l.off_split);
   ws.part_lse = reinterpret_cast<float*>(b + l.off_lse);
   ws.part_o = reinterpret_cast<float*>(b + l.off_o);
+  ws.grp_lse = reinterpret_cast<float*>(b + l.off_glse);
+  ws.grp_o = reinterpret_cast<float*>(b + l.off_go);
   ws.max_slots = l.max_slots;
   ws.grid = l.grid;
   return ws;
@@ -229,8 +245,7 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
     l.tok_per_unit = 1;
     const AttnParams p = make_params(a, l);
     const DecWorkspace ws = make_dec_ws(workspace, dl);
-    cudaError_t e = launch_plan_decode(p, ws, stream);
-    if (e == cudaSuccess) e = launch_decode_tc(p, ws, stream);
+    const cudaError_t e = launch_decode_tc(p, ws, stream);
     return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
   }
   const AttnLayout l = attn_layout(a, decode);

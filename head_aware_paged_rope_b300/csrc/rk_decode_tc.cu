@@ -60,7 +60,8 @@ struct DecLayout {
   static constexpr int kP = kQ + 2 * kQBuf;                     // 2 x [16][128 keys] bf16
   static constexpr int kV = kP + 2 * 4096;                      // V stages, then K stages: for D = 64
   static constexpr int kK = kV + kStages * kStageBytes;         // V^T's second M half reads past a V stage
-  static constexpr int kBytes = kK + kStages * kStageBytes;
+  static constexpr int kPlan = kK + kStages * kStageBytes;      // single-launch path: per-segment ranges
+  static constexpr int kBytes = kPlan + kDecFusedSegs * 16;
   static constexpr int kSmem = kBytes + 1024;
 };
 
@@ -69,6 +70,7 @@ struct Portion {
   int32_t seg, v_begin, v_end, slot;    // slot < 0: write the output directly
   int32_t n_kt, b, tok, pos;
   int32_t cls, W, S, L;
+  int32_t n_splits, cta0, tile0, pad;   // CTAs sharing the segment, the first of them, its first tile
 };
 
 struct DecShared {
@@ -84,6 +86,9 @@ struct DecShared {
   float lse2[kN];
   uint32_t tmem_slot;
   int abort;
+  int T, gs, seg_first, last;   // single-launch path: the schedule, and "this CTA merges the splits"
+  int tb, te, aligned, max_nt;
+  int s_warp[32];
 };
 
 __device__ __forceinline__ bool aborted(DecShared& sh) { return *reinterpret_cast<volatile int*>(&sh.abort) != 0; }
@@ -150,7 +155,102 @@ __device__ __forceinline__ float warp_reduce_cols(float (&v)[NG]) {
   return v[0];
 }
 
-template <int D, int NG>
+constexpr int kMergeFan = 12;   // partials one CTA merges at a time (single-launch path)
+constexpr int kStreamTiles = 32;  // segments of at least 4096 keys are streamed past L2 (evict-first)
+constexpr int kAlignTiles = 2;  // segments this short are never split when there are enough CTAs
+
+// Partial slot of CTA c for a split segment (two per CTA: its first and its last portion):
+// c's portion of the segment is its first one unless c = cta0 and c's share began in an
+// earlier segment.
+__device__ __forceinline__ int split_slot(int c, int cta0, int tile0, long long T, long long gs) {
+  return (c == cta0 && (long long)c * T / gs < tile0) ? 2 * c + 1 : 2 * c;
+}
+
+// One arrival at a counter that `need` arrivals complete: true for the last one, which also
+// returns the counter to zero.  Called by one thread after a barrier of the threads that
+// wrote the partial: the release publishes their stores (cumulativity through the barrier),
+// the acquire makes the other CTAs' partials visible to the last arrival.
+__device__ __forceinline__ int arrive_last(int32_t* cnt, int need) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+  if (old != need - 1) return 0;
+  asm volatile("st.relaxed.gpu.s32 [%0], 0;" :: "l"(cnt) : "memory");
+  return 1;
+}
+
+// Log-sum-exp merge of n normalised partials (lse in log2 units) of one segment, whose slots
+// belong to CTAs c_first, c_first + stride, ...: into the bf16 output rows (and lse, natural
+// log) or into one partial slot.  The 128 softmax threads each take (head, 4 channels)
+// columns, two at a time, eight partials' loads in flight.
+template <int D>
+__device__ __forceinline__ void merge_splits(int n, int c_first, int stride, int cta0, int tile0, long long T,
+                                             long long gs, const float* src_lse, const float* src_o, int G,
+                                             __nv_bfloat16* out_row, float* lse_row, float* dst_lse, float* dst_o,
+                                             int t) {
+  constexpr int C4 = D / 4;
+  const int NU = G * C4;
+  for (int ub = 0; ub < NU; ub += 256) {
+    const int u[2] = {ub + t, ub + 128 + t};
+    float M[2] = {-INFINITY, -INFINITY}, den[2] = {0.f, 0.f};
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int k0 = 0; k0 < n; k0 += 8) {
+      float lv[2][8];
+      float4 ov[2][8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int slot = k0 + k < n ? split_slot(c_first + (k0 + k) * stride, cta0, tile0, T, gs) : -1;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          lv[x][k] = -INFINITY;
+          ov[x][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (slot >= 0 && u[x] < NU) {
+            const int g = u[x] / C4, c4 = u[x] - g * C4;
+            lv[x][k] = __ldcg(src_lse + int64_t(slot) * G + g);
+            ov[x][k] = __ldcg(reinterpret_cast<const float4*>(src_o + (int64_t(slot) * G + g) * D) + c4);
+          }
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        float mc = M[x];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mc = fmaxf(mc, lv[x][k]);
+        if (mc == -INFINITY) continue;
+        const float f = fast_exp2(M[x] - mc);   // 0 while M is -inf
+        den[x] *= f;
+        acc[x].x *= f; acc[x].y *= f; acc[x].z *= f; acc[x].w *= f;
+        M[x] = mc;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float w = fast_exp2(lv[x][k] - mc);
+          den[x] += w;
+          acc[x].x = fmaf(w, ov[x][k].x, acc[x].x); acc[x].y = fmaf(w, ov[x][k].y, acc[x].y);
+          acc[x].z = fmaf(w, ov[x][k].z, acc[x].z); acc[x].w = fmaf(w, ov[x][k].w, acc[x].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      if (u[x] >= NU) continue;
+      const int g = u[x] / C4, c4 = u[x] - g * C4;
+      const float inv = den[x] > 0.f ? 1.f / den[x] : 0.f;
+      const float l2 = den[x] > 0.f ? M[x] + fast_log2(den[x]) : -INFINITY;
+      if (out_row) {
+        uint2 o;
+        o.x = pack_bf16(acc[x].x * inv, acc[x].y * inv);
+        o.y = pack_bf16(acc[x].z * inv, acc[x].w * inv);
+        *reinterpret_cast<uint2*>(out_row + g * D + c4 * 4) = o;
+        if (lse_row && c4 == 0) lse_row[g] = l2 * 0.69314718055994531f;
+      } else {
+        *reinterpret_cast<float4*>(dst_o + g * D + c4 * 4) =
+            make_float4(acc[x].x * inv, acc[x].y * inv, acc[x].z * inv, acc[x].w * inv);
+        if (c4 == 0) dst_lse[g] = l2;
+      }
+    }
+  }
+}
+
+template <int D, int NG, bool FUSED>
 __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                  const __grid_constant__ CUtensorMap tmK,
                                                                  const __grid_constant__ CUtensorMap tmV,
@@ -189,6 +289,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       mbar_init(smem_addr(&sh.iq_empty[s]), 129);
     }
     sh.abort = 0;
+    sh.seg_first = p.B * p.Hkv;
+    sh.max_nt = 0;
     mbar_fence_init();
   }
   if (warp == 4 && lane == 0) {
@@ -207,16 +309,95 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_slot;
-  grid_dependency_wait();      // the plan (and everything before it in the stream) is complete
-  grid_launch_dependents();    // the combine kernel may be scheduled as CTAs of this one finish
+  // Stable metadata (single-launch path): plan and page ids are read while the preceding
+  // kernel finishes; each role waits for it before touching q, the pools or any output.
+  const bool early = FUSED && (p.flags & RK_ATTN_METADATA_STABLE) != 0;
+  if (!early) grid_dependency_wait();   // the plan (and everything before it in the stream) is complete
+  grid_launch_dependents();             // the next kernel may be scheduled as CTAs of this one finish
 
   const int G = p.G;
   const int nseg = p.B * p.Hkv;
+  const int4* s_plan = reinterpret_cast<const int4*>(smem + LY::kPlan);
+
+  if constexpr (FUSED) {
+    // ---------------------------------------------------------------- plan (every CTA alike)
+    // Thread i takes segments [i*per, i*per + per) (per <= 3), finds their visible ranges in
+    // three interleaved rounds of loads, and a block scan of their tile counts gives each
+    // segment's first tile; the share of this CTA follows as in the separate planner.
+    int4* plan = reinterpret_cast<int4*>(smem + LY::kPlan);
+    constexpr int kPer = (kDecFusedSegs + kThreads - 1) / kThreads;
+    const int per = (nseg + kThreads - 1) / kThreads;
+    const int s0 = tid * per;
+    DecRange rr[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) if (i < per && s0 + i < nseg) rr[i].load1(p, s0 + i);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) if (i < per && s0 + i < nseg) rr[i].load2();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) if (i < per && s0 + i < nseg) rr[i].load3(p);
+    int nt[kPer], sum = 0, mx = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      nt[i] = 0;
+      if (i < per && s0 + i < nseg) {
+        rr[i].finish();
+        nt[i] = (rr[i].n_vis + EPT - 1) / EPT;
+      }
+      sum += nt[i];
+      mx = max(mx, nt[i]);
+    }
+    if (mx > 0) atomicMax(&sh.max_nt, mx);   // read after the scan's barriers
+    int T;
+    int t0 = block_exclusive_scan(sum, &T, sh.s_warp);
+    // Few, short segments (at most kAlignTiles tiles each, no more segments than CTAs): CTA c
+    // takes segment c whole, so nothing is split.  Otherwise the equal shares.
+    const bool aligned = sh.max_nt <= kAlignTiles && nseg <= int(gridDim.x);
+    const int gs = min(int(gridDim.x), T);
+    const int c = blockIdx.x;
+    const int tb = c < gs ? int((long long)c * T / gs) : T;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int seg = s0 + i;
+      if (i < per && seg < nseg) {
+        plan[seg] = make_int4(rr[i].e_sink, rr[i].e_w, rr[i].n_vis, t0);
+        if (aligned) {
+          if (seg == c) {
+            sh.tb = nt[i] > 0 ? t0 : T;
+            sh.te = nt[i] > 0 ? t0 + nt[i] : T;
+            sh.seg_first = seg;
+          }
+        } else if (nt[i] > 0 && t0 <= tb && tb < t0 + nt[i]) {
+          sh.seg_first = seg;
+        }
+        t0 += nt[i];
+      }
+    }
+    if (tid == 0) {
+      sh.T = T;
+      sh.gs = gs;
+      sh.aligned = aligned;
+      if (!aligned) {
+        sh.tb = tb;
+        sh.te = c < gs ? int((long long)(c + 1) * T / gs) : T;
+      } else if (c >= nseg) {
+        sh.tb = sh.te = T;
+      }
+    }
+    __syncthreads();
+  }
 
   if (warp == 4) {
     // ------------------------------------------------------------------ producer
     const int64_t oob_row = p.n_pool_pages * P;      // a row past the pool: TMA fills zeros
-    const DecCta my = ws.ctas[blockIdx.x];
+    const uint64_t evict_first = l2_policy_evict_first();
+    DecCta my;
+    if constexpr (FUSED) {
+      my.seg0 = sh.seg_first;
+      my.tile_begin = sh.tb;
+      my.tile_end = sh.te;
+    } else {
+      my = ws.ctas[blockIdx.x];
+    }
     int seg = my.seg0, t = my.tile_begin;
     const int t_end = my.tile_end;
     // raw page id / logical page of entry v_begin + grp*32 + lane of segment s (present: listed)
@@ -235,7 +416,31 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     auto load_seg = [&](int s) {
       DecSeg d;
       if (s < nseg) {
-        d = ws.segs[s];
+        if constexpr (FUSED) {
+          const int4 r = s_plan[s];
+          d.e_sink = r.x;
+          d.e_w = r.y;
+          d.n_vis = r.z;
+          d.tile0 = r.w;
+          d.n_tiles = (r.z + EPT - 1) / EPT;
+          d.b = s / p.Hkv;
+          d.tok = d.b;
+          d.L = __ldg(p.seq_len + d.b);
+          d.pos = d.L - 1;
+          d.cls = __ldg(p.head_class + s);
+          const bool local = d.cls == RK_CLASS_LOCAL;
+          d.W = local ? __ldg(p.window + s) : 0;
+          d.S = local && p.sink ? __ldg(p.sink + s) : 0;
+          const long long T = sh.T, gs = sh.gs;
+          const bool cut = d.n_tiles > 0 && !sh.aligned;
+          const int c0 = cut ? int((((long long)d.tile0 + 1) * gs + T - 1) / T) - 1 : s;
+          const int c1 = cut ? int((((long long)d.tile0 + d.n_tiles) * gs + T - 1) / T) - 1 : s;
+          d.cta0 = c0;
+          d.n_splits = c1 - c0 + 1;
+          d.slot0 = -1;
+        } else {
+          d = ws.segs[s];
+        }
       } else {
         d.n_tiles = 0;
         d.tile0 = 0x7fffffff;
@@ -254,6 +459,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     int raw_page, raw_lp;
     bool present;
     fetch(seg, cur, (t < t_end && seg < nseg) ? (t - cur.tile0) * EPT : 0, cur.n_vis, 0, raw_page, raw_lp, present);
+    if (early) grid_dependency_wait();
     for (int k = 0; ok; ++k) {
       const int slot = k % kRing;
       if (k >= kRing) {
@@ -271,7 +477,13 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         po.v_begin = lt0 * EPT;
         po.v_end = min(cur.n_vis, lt1 * EPT);
         po.n_kt = lt1 - lt0;
-        po.slot = cur.n_splits > 1 ? cur.slot0 + (int(blockIdx.x) - cur.cta0) : -1;
+        if constexpr (FUSED)   // two slots per CTA: its first portion and its last one
+          po.slot = cur.n_splits > 1 ? 2 * int(blockIdx.x) + (t == my.tile_begin ? 0 : 1) : -1;
+        else
+          po.slot = cur.n_splits > 1 ? cur.slot0 + (int(blockIdx.x) - cur.cta0) : -1;
+        po.n_splits = cur.n_splits;
+        po.cta0 = cur.cta0;
+        po.tile0 = cur.tile0;
         po.b = cur.b;
         po.tok = cur.tok;
         po.pos = cur.pos;
@@ -312,6 +524,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       }
       const int tpg = kGrp / EPT;                       // tiles per group
       const int n_grp = (po.n_kt + tpg - 1) / tpg;
+      const bool streaming = cur.n_tiles >= kStreamTiles;
       for (int grp = 0; ok && grp < n_grp; ++grp) {
         int raw_page_n, raw_lp_n;
         bool present_n;
@@ -351,11 +564,20 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           const int pg = lane - jt * EPT;
           if (pg >= 0 && pg < EPT) {
             const uint32_t full = smem_addr(&sh.kv_full[st]);
+            if (streaming) {   // long segments: read once per call, keep them from evicting hot data
 #pragma unroll
-            for (int hf = 0; hf < HALVES; ++hf) {
-              const uint32_t off = st * LY::kStageBytes + hf * kHalfBytes + pg * P * 128;
-              tma_load_2d(sK + off, &tmK, hf * 64, int(row), full);
-              tma_load_2d(sV + off, &tmV, hf * 64, int(row), full);
+              for (int hf = 0; hf < HALVES; ++hf) {
+                const uint32_t off = st * LY::kStageBytes + hf * kHalfBytes + pg * P * 128;
+                tma_load_2d_hint(sK + off, &tmK, hf * 64, int(row), full, evict_first);
+                tma_load_2d_hint(sV + off, &tmV, hf * 64, int(row), full, evict_first);
+              }
+            } else {
+#pragma unroll
+              for (int hf = 0; hf < HALVES; ++hf) {
+                const uint32_t off = st * LY::kStageBytes + hf * kHalfBytes + pg * P * 128;
+                tma_load_2d(sK + off, &tmK, hf * 64, int(row), full);
+                tma_load_2d(sV + off, &tmV, hf * 64, int(row), full);
+              }
             }
           }
         }
@@ -460,6 +682,18 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const int my_col = lane / LPC;
     uint32_t gg = 0;
     bool ok = true;
+    if constexpr (FUSED) {
+      if (early) grid_dependency_wait();
+      // segments with nothing visible (every CTA planned them): out = 0, lse = -inf, written
+      // by CTA seg % grid
+      for (int seg = blockIdx.x; seg < nseg; seg += gridDim.x) {
+        if (s_plan[seg].z != 0) continue;
+        const int b = seg / p.Hkv, h = seg - b * p.Hkv;
+        uint4* o = reinterpret_cast<uint4*>(p.out + (int64_t(b) * p.Hq + h * G) * D);
+        for (int k = t; k < G * D / 8; k += 128) o[k] = make_uint4(0, 0, 0, 0);
+        if (p.lse && t < G) p.lse[int64_t(b) * p.Hq + h * G + t] = -INFINITY;
+      }
+    }
     for (int k = 0; ok; ++k) {
       const int slot = k % kRing;
       const bool got_item = wait_or_abort(sh, smem_addr(&sh.iq_full[slot]), (k / kRing) & 1);
@@ -589,7 +823,44 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           ws.part_lse[int64_t(po.slot) * G + t] = sh.lse2[t];
         }
       }
-      named_bar_sync(1, 128);   // sh.redl / sh.lse2 are rewritten by the next portion
+      if constexpr (FUSED) {
+        if (split) {
+          // The CTA whose partial completes the segment merges them all (log-sum-exp).  A
+          // segment cut over more than kMergeFan CTAs is merged in two levels: groups of
+          // kMergeFan consecutive CTAs first, each by the group's last arrival, then the
+          // group results.  Every counter is returned to zero by the CTA that reads it last.
+          const long long T = sh.T, gs = sh.gs;
+          const int n = po.n_splits, j = int(blockIdx.x) - po.cta0;
+          const bool two = n > kMergeFan;
+          const int n_grp = (n + kMergeFan - 1) / kMergeFan;
+          const int q = j / kMergeFan, cq = po.cta0 + q * kMergeFan;
+          const int gslot = split_slot(cq, po.cta0, po.tile0, T, gs);
+          int32_t* cnt = two ? ws.counters + kDecMaxGrid + gslot : ws.counters + po.cta0;
+          const int need = two ? min(kMergeFan, n - q * kMergeFan) : n;
+          named_bar_sync(1, 128);
+          if (t == 0) sh.last = arrive_last(cnt, need);
+          named_bar_sync(1, 128);
+          if (sh.last) {
+            __nv_bfloat16* out_row = p.out + (int64_t(po.tok) * p.Hq + h * G) * D;
+            float* lse_row = p.lse ? p.lse + int64_t(po.tok) * p.Hq + h * G : nullptr;
+            if (!two) {
+              merge_splits<D>(n, po.cta0, 1, po.cta0, po.tile0, T, gs, ws.part_lse, ws.part_o, G, out_row, lse_row,
+                              nullptr, nullptr, t);
+            } else {
+              merge_splits<D>(need, cq, 1, po.cta0, po.tile0, T, gs, ws.part_lse, ws.part_o, G, nullptr, nullptr,
+                              ws.grp_lse + int64_t(gslot) * G, ws.grp_o + int64_t(gslot) * G * D, t);
+              named_bar_sync(1, 128);
+              if (t == 0) sh.last = arrive_last(ws.counters + po.cta0, n_grp);
+              named_bar_sync(1, 128);
+              if (sh.last) {
+                merge_splits<D>(n_grp, po.cta0, kMergeFan, po.cta0, po.tile0, T, gs, ws.grp_lse, ws.grp_o, G,
+                                out_row, lse_row, nullptr, nullptr, t);
+              }
+            }
+          }
+        }
+      }
+      named_bar_sync(1, 128);   // sh.redl / sh.lse2 / sh.last are rewritten by the next portion
     }
     if (!ok && lane == 0) set_abort(sh, p.status);
   }
@@ -679,21 +950,9 @@ __global__ __launch_bounds__(256) void combine_decode_tc_kernel(AttnParams p, De
   }
 }
 
-cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
 template <int D, int NG>
 cudaError_t launch_t(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream) {
+  const bool fused = p.B * p.Hkv <= kDecFusedSegs;
   using LY = DecLayout<D>;
   CUtensorMap mq, mk, mv;
   const cuuint64_t qdims[3] = {cuuint64_t(D), cuuint64_t(p.Hq), cuuint64_t(p.total_q)};
@@ -709,14 +968,20 @@ cudaError_t launch_t(const AttnParams& p, const DecWorkspace& ws, cudaStream_t s
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, NG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          LY::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_tc_kernel<D, NG, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               LY::kSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(ws.grid), dim3(kThreads), LY::kSmem, stream, attr);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG>, mq, mk, mv, p, ws);
+  if (fused) return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, true>, mq, mk, mv, p, ws);
+  cudaError_t e = launch_plan_decode(p, ws, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, false>, mq, mk, mv, p, ws);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t cfg2 = pdl_config(dim3(4 * ws.grid), dim3(256), 0, stream, attr2);

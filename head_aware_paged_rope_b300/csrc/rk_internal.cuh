@@ -108,6 +108,7 @@ struct AttnParams {
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
+  int32_t flags;       // RK_ATTN_* bits
 };
 
 // Workspace carve-up for the attention calls.
@@ -154,19 +155,162 @@ struct DecHeader {
 
 struct DecWorkspace {
   DecHeader* header;
+  int32_t* counters;     // [3 * kDecMaxGrid] split arrivals, zero between calls (single-launch path):
+                         // per segment (indexed by its first CTA), then per group of CTAs (by slot)
   DecSeg* segs;          // [B*Hkv]
   DecCta* ctas;          // [grid]
   int32_t* split_segs;   // [B*Hkv]
   float* part_lse;       // [max_slots][G], log2 domain
   float* part_o;         // [max_slots][G][d], normalised partial outputs
-  int32_t max_slots;     // >= the slots any plan needs: B*Hkv + grid
+  float* grp_lse;        // [2 * grid][G]: merged groups of partials (single-launch path)
+  float* grp_o;          // [2 * grid][G][d]
+  int32_t max_slots;     // >= the slots any plan needs: max(B*Hkv + grid, 2 * grid)
   int32_t grid;
 };
 
 constexpr int kDecTileKeys = 128;
 constexpr int kDecMaxSegs = 16384;   // B * Hkv of one decode call (the planner keeps 8 bytes per segment on chip)
+constexpr int kDecFusedSegs = 512;   // up to this many segments every decode CTA plans for itself
+constexpr int kDecMaxGrid = 1024;    // split counters kept at the start of the decode workspace
+constexpr size_t kDecCounterBytes = 256 + sizeof(int32_t) * 3 * kDecMaxGrid;   // header + counters
+
+// Lower bound (first entry >= x) of an ascending logical-page list from its two ends: the
+// answer when the ends decide it, else -1 and a guess g (0 <= g <= n-2) to verify with
+// lb_verify after loading row[g] and row[g+1].  `hint` is where the answer lies if the
+// list is contiguous near it.
+__device__ __forceinline__ int lb_ends(const int32_t* row, int n, int first, int last, int x, int hint, int& g) {
+  g = -1;
+  if (!row) return min(max(x, 0), n);
+  if (n <= 0 || x <= first) return 0;
+  if (x > last) return n;
+  if (last - first == n - 1) return x - first;
+  g = min(max(hint, 0), n - 2);   // first < x <= last implies n >= 2
+  return -1;
+}
+
+__device__ __forceinline__ int lb_verify(const int32_t* row, int n, int x, int g, int at, int at1) {
+  if (at == x) return g;                    // strictly ascending: every earlier entry is < x
+  if (at < x && at1 >= x) return g + 1;
+  int lo = at < x ? g + 2 : 0, hi = at < x ? n : g;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(row + mid) < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Visible entry ranges of one decode segment (its query sits at position seq_len - 1),
+// found in three rounds of loads -- the segment's scalars, the two ends of its logical-page
+// list, one check of every bound the ends leave open -- so that a thread can interleave
+// the rounds of several segments.  Result: e_sink, e_w, n_vis as in Unit.
+struct DecRange {
+  int b, L, n, cls, W, S, first, last;
+  const int32_t* lrow;
+  int x_hi, x_w, x_s, r_hi, r_w, r_s, g_hi, g_w, g_s;
+  int a_hi, b_hi, a_w, b_w, a_s, b_s;
+  int e_sink, e_w, n_vis;
+
+  __device__ __forceinline__ void load1(const AttnParams& p, int seg) {
+    b = seg / p.Hkv;
+    L = __ldg(p.seq_len + b);
+    n = __ldg(p.n_pages + seg);
+    cls = __ldg(p.head_class + seg);
+    const int Wr = __ldg(p.window + seg);
+    const int Sr = p.sink ? __ldg(p.sink + seg) : 0;
+    const bool local = cls == RK_CLASS_LOCAL;
+    W = local ? Wr : 0;
+    S = local ? Sr : 0;
+    if (n < 0 || n > p.max_pages) { report(p.status, RK_ERR_DEVICE_BOUNDS); n = 0; }
+    lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
+  }
+  __device__ __forceinline__ void load2() {
+    first = last = 0;
+    if (lrow && n > 0 && L > 0) {
+      first = __ldg(lrow);
+      last = __ldg(lrow + n - 1);
+    }
+  }
+  __device__ __forceinline__ void load3(const AttnParams& p) {
+    g_hi = g_w = g_s = -1;
+    r_hi = r_w = r_s = 0;
+    if (L <= 0 || n <= 0) return;
+    const bool local = cls == RK_CLASS_LOCAL;
+    const int pos = L - 1;
+    x_hi = pos / p.P + 1;                   // entries with logical page <= pos / P
+    x_w = max(0, pos - W + 1) / p.P;        // first window page
+    x_s = (S - 1) / p.P + 1;                // entries past the sink pages
+    r_hi = lb_ends(lrow, n, first, last, x_hi, n - 1 - (last - x_hi), g_hi);
+    if (local) r_w = lb_ends(lrow, n, first, last, x_w, n - 1 - (last - x_w), g_w);
+    if (local && S > 0) r_s = lb_ends(lrow, n, first, last, x_s, x_s - first, g_s);
+    if (g_hi >= 0) { a_hi = __ldg(lrow + g_hi); b_hi = __ldg(lrow + g_hi + 1); }
+    if (g_w >= 0) { a_w = __ldg(lrow + g_w); b_w = __ldg(lrow + g_w + 1); }
+    if (g_s >= 0) { a_s = __ldg(lrow + g_s); b_s = __ldg(lrow + g_s + 1); }
+  }
+  __device__ __forceinline__ void finish() {
+    e_sink = e_w = n_vis = 0;
+    if (L <= 0 || n <= 0) return;
+    if (g_hi >= 0) r_hi = lb_verify(lrow, n, x_hi, g_hi, a_hi, b_hi);
+    if (g_w >= 0) r_w = lb_verify(lrow, n, x_w, g_w, a_w, b_w);
+    if (g_s >= 0) r_s = lb_verify(lrow, n, x_s, g_s, a_s, b_s);
+    const int e_hi = r_hi;
+    if (cls == RK_CLASS_LOCAL) {
+      int ew = min(r_w, e_hi), es = S > 0 ? min(r_s, e_hi) : 0;
+      if (es >= ew) { es = 0; ew = 0; }
+      e_sink = es;
+      e_w = ew;
+      n_vis = es + (e_hi - ew);
+    } else {
+      n_vis = e_hi;
+    }
+  }
+};
+
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, at most
+// 1024); returns the prefix, writes the total.  s_warp holds 32 ints.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (blockDim.x >> 5) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;   // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  const int base = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return base + x - v;
+}
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Launch configuration with programmatic dependent launch: the kernel may be scheduled
+// before its predecessor in the stream has finished; it must execute
+// griddepcontrol.wait before touching anything the predecessor writes.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                     cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
 
 // Launchers implemented in the .cu files.
 cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int rows_per_unit,

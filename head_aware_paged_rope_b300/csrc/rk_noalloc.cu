@@ -32,6 +32,8 @@ extern "C" rk_status rk_segpaged_decode_noalloc(const rk_attn_args* args, rk_str
     if (!g_scratch_addr[dev]) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return RK_ERR_CUDA;
+      // the decode workspace's split counters start at zero (each call leaves them so)
+      if (cudaMemset(p, 0, rk::kDecCounterBytes) != cudaSuccess) return RK_ERR_CUDA;
       g_scratch_addr[dev] = p;
     }
     scratch = g_scratch_addr[dev];

@@ -46,33 +46,6 @@ __device__ __forceinline__ int upper_bound_lp(const int32_t* row, int n, int x) 
   return lower_bound_lp(row, n, x + 1);
 }
 
-// Block-wide exclusive scan of one int per thread; returns the prefix, writes the total.
-__device__ int block_exclusive_scan(int v, int* total, int* s_warp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < (blockDim.x >> 5) ? s_warp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    s_warp[lane] = w;   // inclusive prefix of warp sums
-  }
-  __syncthreads();
-  const int base = warp ? s_warp[warp - 1] : 0;
-  *total = s_warp[(blockDim.x >> 5) - 1];
-  __syncthreads();
-  return base + x - v;
-}
-
 __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWorkspace ws, int tok_per_unit,
                                                             int entries_per_tile, int target_items,
                                                             int min_chunk_tiles, int decode,
@@ -80,6 +53,8 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
   __shared__ int s_warp[32];
   __shared__ unsigned long long s_total_entries;
   __shared__ int s_chunk;
+  sm100::grid_dependency_wait();      // inputs written by earlier kernels in the stream
+  sm100::grid_launch_dependents();    // the attention kernel may start its prologue
   const int tid = threadIdx.x;
   if (tid == 0) s_total_entries = 0ull;
 
@@ -175,15 +150,17 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
   const int chunk = s_chunk;
 
   // 4. items, longest first: the full-size chunks of every unit, then each unit's shorter
-  //    last chunk (or its only, empty, item)
+  //    last chunk (or its only, empty, item).  A remainder of at most half a chunk joins
+  //    the unit's last full chunk instead of becoming an item of its own.
   int carry_full = 0, carry_rem = 0;
   for (int base = 0; base < n_units; base += kPlanThreads) {
     const int u = base + tid;
     int nf = 0, rm = 0;
     if (u < n_units) {
       const int nv = ws.units[u].n_vis;
+      const int r = nv % chunk;
       nf = nv / chunk;
-      rm = (nv % chunk != 0 || nv == 0) ? 1 : 0;
+      rm = (nv == 0 || (r != 0 && (nf == 0 || 2 * r > chunk))) ? 1 : 0;
     }
     int tot_f, tot_r;
     const int pre_f = block_exclusive_scan(nf, &tot_f, s_warp);
@@ -209,7 +186,7 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
       Item item;
       item.unit = u;
       item.v_begin = s * chunk;
-      item.v_end = min(nv, (s + 1) * chunk);
+      item.v_end = s == un.n_splits - 1 ? nv : (s + 1) * chunk;
       item.split = s;
       ws.items[it] = item;
     }
@@ -223,65 +200,77 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
 }
 
 // Merge the split partials of each unit: lse = log sum_s e^{lse_s}, o = sum_s e^{lse_s - lse} o_s.
-// One warp per query row.
+// Work is (unit, block of 8 rows): warp w of a block merges row 8*blk + w in one pass over
+// the unit's splits with a running maximum, four splits' loads in flight at a time; lane l
+// holds channels [l*C, l*C + C).
+template <int D>
 __global__ __launch_bounds__(256) void combine_kernel(AttnParams p, AttnWorkspace ws) {
+  sm100::grid_dependency_wait();   // the attention kernel is complete
+  constexpr int C = D / 32;        // 4 or 2 channels per lane
   const int n_units = ws.header->n_units;
-  const int warps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  const int rb = (ws.rows + 7) / 8;
+  const long long n_blk = (long long)n_units * rb;
+  for (long long blk = blockIdx.x; blk < n_blk; blk += gridDim.x) {
+    const int u = int(blk / rb);
+    const int ns = ws.units[u].n_splits;
+    if (ns <= 1) continue;
     const Unit un = ws.units[u];
-    if (un.n_splits <= 1) continue;
-    const int rows = un.ntok * G;
-    const int h = un.seg % p.Hkv;
-    for (int r = warp; r < rows; r += warps) {
-      float m = -INFINITY;
-      for (int s = 0; s < un.n_splits; ++s)
-        m = fmaxf(m, ws.part_lse[int64_t(unit_item(un, s)) * ws.rows + r]);
-      float wsum = 0.f;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int per_lane = p.d / 32;   // 2 or 4
-      for (int s = 0; s < un.n_splits; ++s) {
-        const int64_t it = unit_item(un, s);
-        const float l = ws.part_lse[it * ws.rows + r];
-        const float w = (m == -INFINITY) ? 0.f : expf(l - m);
-        wsum += w;
-        const float* po = ws.part_o + (it * ws.rows + r) * p.d + lane * per_lane;
-        for (int c = 0; c < per_lane; ++c) acc[c] += w * po[c];
+    const int r = int(blk - (long long)u * rb) * 8 + warp;
+    if (r >= un.ntok * G) continue;
+    float M = -INFINITY, den = 0.f, acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
+    for (int s0 = 0; s0 < ns; s0 += 4) {
+      float lv[4], ov[4][C];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        lv[k] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < C; ++c) ov[k][c] = 0.f;
+        if (s0 + k < ns) {
+          const int64_t it = unit_item(un, s0 + k);
+          lv[k] = ws.part_lse[it * ws.rows + r];
+          const float* po = ws.part_o + (it * ws.rows + r) * D + lane * C;
+          if constexpr (C == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(po);
+            ov[k][0] = v.x; ov[k][1] = v.y; ov[k][2] = v.z; ov[k][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(po);
+            ov[k][0] = v.x; ov[k][1] = v.y;
+          }
+        }
       }
-      const int t = un.tok0 + r / G;
-      const int hq = h * G + (r % G);
-      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-      __nv_bfloat16* o = p.out + (int64_t(t) * p.Hq + hq) * p.d + lane * per_lane;
-      for (int c = 0; c < per_lane; ++c) o[c] = __float2bfloat16_rn(acc[c] * inv);
-      if (p.lse && lane == 0) p.lse[int64_t(t) * p.Hq + hq] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+      const float mc = fmaxf(fmaxf(M, fmaxf(lv[0], lv[1])), fmaxf(lv[2], lv[3]));
+      if (mc == -INFINITY) continue;
+      const float f = M == -INFINITY ? 0.f : expf(M - mc);
+      den *= f;
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[c] *= f;
+      M = mc;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float w = lv[k] == -INFINITY ? 0.f : expf(lv[k] - M);
+        den += w;
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] = fmaf(w, ov[k][c], acc[c]);
+      }
     }
+    const int t = un.tok0 + r / G;
+    const int hq = (un.seg % p.Hkv) * G + (r % G);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __nv_bfloat16* o = p.out + (int64_t(t) * p.Hq + hq) * D + lane * C;
+    if constexpr (C == 4) {
+      uint2 w;
+      w.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+      w.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(o) = w;
+    } else {
+      *reinterpret_cast<uint32_t*>(o) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    }
+    if (p.lse && lane == 0) p.lse[int64_t(t) * p.Hq + hq] = den > 0.f ? M + logf(den) : -INFINITY;
   }
-}
-
-// Lower bound (first entry >= x) of an ascending logical-page list from its two ends: the
-// answer when the ends decide it, else -1 and a guess g (0 <= g <= n-2) to verify with
-// lb_verify after loading row[g] and row[g+1].  `hint` is where the answer lies if the
-// list is contiguous near it.
-__device__ __forceinline__ int lb_ends(const int32_t* row, int n, int first, int last, int x, int hint, int& g) {
-  g = -1;
-  if (!row) return min(max(x, 0), n);
-  if (n <= 0 || x <= first) return 0;
-  if (x > last) return n;
-  if (last - first == n - 1) return x - first;
-  g = min(max(hint, 0), n - 2);   // first < x <= last implies n >= 2
-  return -1;
-}
-
-__device__ __forceinline__ int lb_verify(const int32_t* row, int n, int x, int g, int at, int at1) {
-  if (at == x) return g;                    // strictly ascending: every earlier entry is < x
-  if (at < x && at1 >= x) return g + 1;
-  int lo = at < x ? g + 2 : 0, hi = at < x ? n : g;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(row + mid) < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
 }
 
 // Decode plan: one query per sequence at position seq_len - 1.
@@ -310,49 +299,13 @@ __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p,
 
   // 1. visible ranges
   for (int seg = tid; seg < nseg; seg += kPlanThreads) {
-    const int b = seg / p.Hkv;
-    const int L = __ldg(p.seq_len + b);
-    int n = __ldg(p.n_pages + seg);
-    const int cls = __ldg(p.head_class + seg);
-    const int Wr = __ldg(p.window + seg);
-    const int Sr = p.sink ? __ldg(p.sink + seg) : 0;
-    const bool local = cls == RK_CLASS_LOCAL;
-    const int W = local ? Wr : 0, S = local ? Sr : 0;
-    if (n < 0 || n > p.max_pages) { report(p.status, RK_ERR_DEVICE_BOUNDS); n = 0; }
-    const int pos = L - 1;
-    const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
-    int first = 0, last = 0;
-    if (lrow && n > 0 && L > 0) {
-      first = __ldg(lrow);
-      last = __ldg(lrow + n - 1);
-    }
-    int n_vis = 0, e_sink = 0, e_w = 0;
-    if (L > 0 && n > 0) {
-      const int x_hi = pos / p.P + 1;                   // entries with logical page <= pos / P
-      const int x_w = max(0, pos - W + 1) / p.P;        // first window page
-      const int x_s = (S - 1) / p.P + 1;                // entries past the sink pages
-      int g_hi, g_w = -1, g_s = -1;
-      int r_hi = lb_ends(lrow, n, first, last, x_hi, n - 1 - (last - x_hi), g_hi);
-      int r_w = local ? lb_ends(lrow, n, first, last, x_w, n - 1 - (last - x_w), g_w) : 0;
-      int r_s = (local && S > 0) ? lb_ends(lrow, n, first, last, x_s, x_s - first, g_s) : 0;
-      int a_hi = 0, b_hi = 0, a_w = 0, b_w = 0, a_s = 0, b_s = 0;   // all checks in one round
-      if (g_hi >= 0) { a_hi = __ldg(lrow + g_hi); b_hi = __ldg(lrow + g_hi + 1); }
-      if (g_w >= 0) { a_w = __ldg(lrow + g_w); b_w = __ldg(lrow + g_w + 1); }
-      if (g_s >= 0) { a_s = __ldg(lrow + g_s); b_s = __ldg(lrow + g_s + 1); }
-      if (g_hi >= 0) r_hi = lb_verify(lrow, n, x_hi, g_hi, a_hi, b_hi);
-      if (g_w >= 0) r_w = lb_verify(lrow, n, x_w, g_w, a_w, b_w);
-      if (g_s >= 0) r_s = lb_verify(lrow, n, x_s, g_s, a_s, b_s);
-      const int e_hi = r_hi;
-      if (local) {
-        int ew = min(r_w, e_hi), es = S > 0 ? min(r_s, e_hi) : 0;
-        if (es >= ew) { es = 0; ew = 0; }
-        e_sink = es;
-        e_w = ew;
-        n_vis = es + (e_hi - ew);
-      } else {
-        n_vis = e_hi;
-      }
-    }
+    DecRange r;
+    r.load1(p, seg);
+    r.load2();
+    r.load3(p);
+    r.finish();
+    const int b = r.b, L = r.L, cls = r.cls, W = r.W, S = r.S, pos = L - 1;
+    const int e_sink = r.e_sink, e_w = r.e_w, n_vis = r.n_vis;
     DecSeg& ds = ws.segs[seg];
     ds.e_sink = e_sink;
     ds.e_w = e_w;
@@ -471,16 +424,20 @@ cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int tok_pe
                         cudaStream_t stream) {
   // the tile prefix lives right after the partial outputs (sized by the host)
   int32_t* tile_prefix = reinterpret_cast<int32_t*>(ws.part_o + int64_t(ws.max_items) * ws.rows * p.d);
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, ws, tok_per_unit, entries_per_tile, target_items,
-                                              min_chunk_tiles, decode ? 1 : 0, tile_prefix);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(1), dim3(kPlanThreads), 0, stream, attr);
+  return cudaLaunchKernelEx(&cfg, plan_kernel, p, ws, tok_per_unit, entries_per_tile, target_items,
+                            min_chunk_tiles, decode ? 1 : 0, tile_prefix);
 }
 
 cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, bool decode, cudaStream_t stream) {
-  const int grid = std::max(1, std::min(ws.max_units, device_sm_count() * 4));
-  combine_kernel<<<grid, 256, 0, stream>>>(p, ws);
+  const long long blocks = (long long)ws.max_units * ((ws.rows + 7) / 8);
+  const int grid = int(std::max(1LL, std::min(blocks, (long long)device_sm_count() * 8)));
   (void)decode;
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, stream, attr);
+  return p.d == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p, ws)
+                    : cudaLaunchKernelEx(&cfg, combine_kernel<64>, p, ws);
 }
 
 }  // namespace rk

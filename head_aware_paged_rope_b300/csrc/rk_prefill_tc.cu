@@ -139,6 +139,8 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_slot;
+  grid_dependency_wait();      // the plan (and everything before it in the stream) is complete
+  grid_launch_dependents();    // the combine kernel may be scheduled as CTAs of this one finish
 
   const int G = p.G;
   const int n_items = ws.header->n_items;
@@ -582,8 +584,9 @@ cudaError_t launch_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cu
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  prefill_tc_kernel<D, P><<<grid, kTcThreads, LY::kSmem, stream>>>(mq, mk, mv, p, ws);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kTcThreads), LY::kSmem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, P>, mq, mk, mv, p, ws);
 }
 
 }  // namespace

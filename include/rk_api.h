@@ -23,8 +23,10 @@
  *    argument struct itself, which is read on the host during the call only.
  *  - The library never allocates device memory and never synchronises.  Work is
  *    enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).  Scratch
- *    memory is the caller's `workspace`, sized by the matching *_workspace_size call;
- *    its contents need no initialisation and are undefined afterwards.
+ *    memory is the caller's `workspace`, sized by the matching *_workspace_size call.
+ *    RoPE and prefill workspaces need no initialisation and are undefined afterwards;
+ *    a decode workspace must be zero-filled before its first decode call (see
+ *    rk_segpaged_decode).
  *  - Host-side validation happens before anything is enqueued; on an error nothing is
  *    enqueued.  Checks that need device data (page ids inside the pool, slots inside a
  *    table) run in the kernels: a failing access is skipped and RK_ERR_DEVICE_BOUNDS
@@ -164,7 +166,17 @@ typedef struct rk_attn_args {
   void* out;                   /* bf16 [total_q][Hq][d] */
   float* lse;                  /* fp32 [total_q][Hq] or NULL */
   int32_t* status;             /* optional device int32 error word, may be NULL */
+  int32_t flags;               /* RK_ATTN_* bits below, 0 for none */
 } rk_attn_args;
+
+/* The table and length arrays (cu_seqlens_q, seq_len, page_table, page_logical, n_pages,
+ * head_class, window, sink) were written by work that completed before the kernel
+ * preceding this call on `stream` began -- e.g. copied once at the start of a decode
+ * step, before the layers run.  The decode kernel then plans its work from them while
+ * that kernel is still finishing, and waits for it only before reading q and the pools
+ * and before writing.  Without the flag nothing is read before the preceding work has
+ * completed.  Ignored by prefill. */
+#define RK_ATTN_METADATA_STABLE 1
 
 /* Bytes of workspace rk_segpaged_prefill / rk_segpaged_decode need for these sizes
  * (work list plus split-KV partial results).  Returns 0 for invalid sizes. */
@@ -180,7 +192,14 @@ RK_API rk_status rk_segpaged_prefill(const rk_attn_args* args, void* workspace, 
 
 /* Decode: one query per sequence at position seq_len[b] - 1 (q is [B][Hq][d]); split-KV
  * over each head's visible pages, partial results merged by log-sum-exp.  Same errors, and
- * RK_ERR_UNSUPPORTED when B * Hkv exceeds 16384. */
+ * RK_ERR_UNSUPPORTED when B * Hkv exceeds 16384.
+ *
+ * Workspace: its first 12544 bytes hold per-call split counters.  They must be zero before
+ * the first decode call that uses the workspace (e.g. cudaMemsetAsync of the whole
+ * buffer once, after allocating it); every call returns them to zero before it completes,
+ * so the workspace can be reused by any later decode call, of any shape, on the same
+ * stream without clearing.  Do not use it for other calls in between.  After a call that
+ * reported RK_ERR_TIMEOUT, zero it again. */
 RK_API rk_status rk_segpaged_decode(const rk_attn_args* args, void* workspace, size_t workspace_bytes,
                              rk_stream_t stream);
 
@@ -198,9 +217,9 @@ RK_API rk_status rk_segpaged_decode(const rk_attn_args* args, void* workspace, s
  * with that device current), so make that first call before any stream capture.  No call
  * allocates memory.  Every call on a device shares the one array: calls that may overlap
  * on the GPU (different streams, or different host threads) race and must be serialised
- * by the caller; calls on one stream are ordered.  The array keeps the last call's
- * contents; nothing in it needs to start at zero, because each call's planning kernel
- * rewrites the work list and resets its item counter before the decode kernel reads them. */
+ * by the caller; calls on one stream are ordered.  The array's split counters are zeroed
+ * at that first call and every call leaves them at zero (after RK_ERR_TIMEOUT on the
+ * device, the array cannot be reused: the process should start over). */
 #define RK_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 RK_API rk_status rk_segpaged_decode_noalloc(const rk_attn_args* args, rk_stream_t stream);
 

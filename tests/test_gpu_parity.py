@@ -63,10 +63,10 @@ def _check_rope(w, got_pool_bits):
     return O.apply_rope_to_pool(w.attn.k_pool, (pages, slots, rows))
 
 
-def _gpu_attn(rk, batch, decode=False, k_pool=None, use_logical=True):
+def _gpu_attn(rk, batch, decode=False, k_pool=None, use_logical=True, flags=0):
     da = attn_to_device(batch, "cuda", k_pool=k_pool)
     st = _status()
-    args = da.args(rk, decode=decode, status=st, use_logical=use_logical)
+    args = da.args(rk, decode=decode, status=st, use_logical=use_logical, flags=flags)
     (rk.segpaged_decode if decode else rk.segpaged_prefill)(args)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
@@ -224,9 +224,11 @@ def test_prefill_device_bounds_check(rk):
 
 
 # ------------------------------------------------------------------------- decode
-def test_decode_microbench_full_size(rk):
+@pytest.mark.parametrize("flags", [0, 1])
+def test_decode_microbench_full_size(rk, flags):
+    # flags 1: RK_ATTN_METADATA_STABLE (work planned before the preceding kernel completes)
     w = synth.decode_microbench()
-    out, lse = _gpu_attn(rk, w.attn, decode=True)
+    out, lse = _gpu_attn(rk, w.attn, decode=True, flags=flags)
     _compare(w.attn, out, lse)
 
 
@@ -244,6 +246,69 @@ def test_decode_d64_gqa2(rk):
     _compare(a, out, lse)
 
 
+def test_decode_one_segment_over_every_cta(rk):
+    # one global head over 70000 keys: its 547 key tiles are cut over the whole grid, so a
+    # single segment has one partial per CTA and the merge runs over all of them
+    w = synth.decode_microbench(B=1, ctx=70000, Hq=8, Hkv=1, window=256, sink=0)
+    out, lse = _gpu_attn(rk, w.attn, decode=True, flags=rk.RK_ATTN_METADATA_STABLE)
+    _compare(w.attn, out, lse)
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_decode_empty_lists_and_empty_context(rk, flags):
+    # head segments with nothing visible: an empty page list, and a sequence of length 0
+    w = synth.decode_microbench(B=4, ctx=900, Hq=16, Hkv=4, window=100, sink=4, seed=21)
+    a = w.attn
+    n = a.n_pages.copy()
+    n[1] = 0                       # sequence 0, KV head 1
+    n[9] = 0                       # sequence 2, KV head 1
+    seq = a.seq_len.copy()
+    seq[3] = 0                     # sequence 3: no context at all
+    a = dataclasses.replace(a, n_pages=n, seq_len=seq)
+    da = attn_to_device(a, "cuda")
+    da.out.fill_(float("nan"))
+    st = _status()
+    rk.segpaged_decode(da.args(rk, decode=True, status=st, flags=flags))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    out, lse = da.out.float().cpu().numpy(), da.lse.cpu().numpy()
+    G = a.Hq // a.Hkv
+    for t, h in ((0, 1), (2, 1), (3, 0), (3, 3)):
+        assert np.all(out[t, h * G:(h + 1) * G] == 0) and np.all(np.isneginf(lse[t, h * G:(h + 1) * G]))
+    rows = [(t, h) for t in range(3) for h in range(a.Hkv)]
+    _compare(a, out, lse, rows=rows)
+
+
+def test_decode_many_segments_separate_planner(rk):
+    # 576 head segments: more than every CTA plans for itself, so the separate planning and
+    # merging kernels run
+    w = synth.decode_microbench(B=72, ctx=700, Hq=32, Hkv=8, window=100, sink=4)
+    out, lse = _gpu_attn(rk, w.attn, decode=True)
+    _compare(w.attn, out, lse)
+
+
+def test_decode_workspace_reused_across_shapes(rk):
+    # one workspace, zeroed once, serves decode calls of different shapes and both schedules;
+    # each call leaves its split counters at zero
+    shapes = [dict(B=3, ctx=5000, Hq=32, Hkv=8, window=256, sink=4, seed=11),
+              dict(B=72, ctx=700, Hq=32, Hkv=8, window=100, sink=4, seed=12),
+              dict(B=1, ctx=30000, Hq=16, Hkv=1, window=64, sink=0, seed=13),
+              dict(B=3, ctx=5000, Hq=32, Hkv=8, window=256, sink=4, seed=11)]
+    batches = [synth.decode_microbench(**kw).attn for kw in shapes]
+    devs = [attn_to_device(b, "cuda") for b in batches]
+    st = _status()
+    sizes = [rk.segpaged_decode_workspace_size(d.args(rk, decode=True, status=st)) for d in devs]
+    ws = torch.zeros(max(sizes), dtype=torch.uint8, device="cuda")
+    for flags in (0, rk.RK_ATTN_METADATA_STABLE):
+        for b, d in zip(batches, devs):
+            d.out.fill_(float("nan"))
+            rk.segpaged_decode(d.args(rk, decode=True, status=st, flags=flags), workspace=ws)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0
+            _compare(b, d.out.float().cpu().numpy(), d.lse.cpu().numpy())
+            assert int(ws[256:12544].count_nonzero().item()) == 0
+
+
 def test_stack_small_prefill_then_decode(rk):
     w = synth.stack_layer(0, n_segments=4, seg_tokens=1024, n_suffix=100, n_decode=4)
     kp = _gpu_rope(rk, w)
@@ -253,7 +318,7 @@ def test_stack_small_prefill_then_decode(rk):
     _compare(a, out, lse)
     for step in (0, 3):
         d = synth.decode_batch_from(dataclasses.replace(w, attn=a), step)
-        out, lse = _gpu_attn(rk, d, decode=True)
+        out, lse = _gpu_attn(rk, d, decode=True, flags=rk.RK_ATTN_METADATA_STABLE)
         _compare(d, out, lse)
 
 

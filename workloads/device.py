@@ -32,11 +32,12 @@ class DeviceAttn:
     total_q: int
     max_q: int
 
-    def args(self, rk, decode: bool = False, status=None, use_logical: bool = True):
+    def args(self, rk, decode: bool = False, status=None, use_logical: bool = True, flags: int = 0):
         return rk.attn_args(self.q, self.seq_len, self.k_pool, self.v_pool, self.page_table,
                             self.page_logical if use_logical else None, self.n_pages, self.head_class,
                             self.window, self.sink, self.out, cu_seqlens_q=None if decode else self.cu_seqlens_q,
-                            lse=self.lse, status=status, total_q=self.total_q, max_q=1 if decode else self.max_q)
+                            lse=self.lse, status=status, total_q=self.total_q, max_q=1 if decode else self.max_q,
+                            flags=flags)
 
 
 def attn_to_device(batch, device, k_pool: torch.Tensor = None, v_pool: torch.Tensor = None) -> DeviceAttn:
