@@ -175,8 +175,8 @@ constexpr int kDecMaxGrid = 1024;    // split counters kept at the start of the 
 constexpr size_t kDecCounterBytes = 256 + sizeof(int32_t) * 3 * kDecMaxGrid;   // header + counters
 
 // Lower bound (first entry >= x) of an ascending logical-page list from its two ends: the
-// answer when the ends decide it, else -1 and a guess g (0 <= g <= n-2) to verify with
-// lb_verify after loading row[g] and row[g+1].  `hint` is where the answer lies if the
+// answer when the ends decide it, else -1 and a guess g (1 <= g <= n-1) to verify with
+// lb_verify after loading row[g-1] and row[g].  `hint` is where the answer lies if the
 // list is contiguous near it.
 __device__ __forceinline__ int lb_ends(const int32_t* row, int n, int first, int last, int x, int hint, int& g) {
   g = -1;
@@ -184,14 +184,14 @@ __device__ __forceinline__ int lb_ends(const int32_t* row, int n, int first, int
   if (n <= 0 || x <= first) return 0;
   if (x > last) return n;
   if (last - first == n - 1) return x - first;
-  g = min(max(hint, 0), n - 2);   // first < x <= last implies n >= 2
+  g = min(max(hint, 1), n - 1);   // first < x <= last: the answer is in [1, n-1]
   return -1;
 }
 
-__device__ __forceinline__ int lb_verify(const int32_t* row, int n, int x, int g, int at, int at1) {
-  if (at == x) return g;                    // strictly ascending: every earlier entry is < x
-  if (at < x && at1 >= x) return g + 1;
-  int lo = at < x ? g + 2 : 0, hi = at < x ? n : g;
+// below = row[g-1], at = row[g]
+__device__ __forceinline__ int lb_verify(const int32_t* row, int n, int x, int g, int below, int at) {
+  if (below < x && at >= x) return g;
+  int lo = at < x ? g + 1 : 1, hi = at < x ? n : g - 1;   // row[0] < x; row[g-1] >= x in the second case
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
     if (__ldg(row + mid) < x) lo = mid + 1; else hi = mid;
@@ -242,9 +242,9 @@ struct DecRange {
     r_hi = lb_ends(lrow, n, first, last, x_hi, n - 1 - (last - x_hi), g_hi);
     if (local) r_w = lb_ends(lrow, n, first, last, x_w, n - 1 - (last - x_w), g_w);
     if (local && S > 0) r_s = lb_ends(lrow, n, first, last, x_s, x_s - first, g_s);
-    if (g_hi >= 0) { a_hi = __ldg(lrow + g_hi); b_hi = __ldg(lrow + g_hi + 1); }
-    if (g_w >= 0) { a_w = __ldg(lrow + g_w); b_w = __ldg(lrow + g_w + 1); }
-    if (g_s >= 0) { a_s = __ldg(lrow + g_s); b_s = __ldg(lrow + g_s + 1); }
+    if (g_hi >= 0) { a_hi = __ldg(lrow + g_hi - 1); b_hi = __ldg(lrow + g_hi); }
+    if (g_w >= 0) { a_w = __ldg(lrow + g_w - 1); b_w = __ldg(lrow + g_w); }
+    if (g_s >= 0) { a_s = __ldg(lrow + g_s - 1); b_s = __ldg(lrow + g_s); }
   }
   __device__ __forceinline__ void finish() {
     e_sink = e_w = n_vis = 0;
