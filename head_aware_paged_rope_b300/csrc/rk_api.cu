@@ -302,6 +302,8 @@ rk_status rk_rope_reposition(const rk_rope_args* a, void* workspace, size_t work
   const size_t need = rk_rope_workspace_size(a->n_runs, a->d);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return RK_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->k_src) & 15u) != 0 || (reinterpret_cast<uintptr_t>(a->k_dst) & 15u) != 0)
+    return RK_ERR_INVALID_ARG;   // rows move by 16-byte bulk copies and vector stores
   const cudaError_t e = rk::launch_rope(*a, workspace, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }

@@ -122,10 +122,12 @@ RK_API size_t rk_rope_workspace_size(int32_t n_runs, int32_t d);
 /* Enqueue the repositioning of every run.  Rows of different runs must not overlap in
  * k_dst, and k_dst may alias k_src only when every token reads and writes the very same
  * row (in-place update).  Errors: RK_ERR_INVALID_ARG (NULL pointers with n_runs > 0,
- * negative sizes, theta <= 1 or not finite), RK_ERR_UNSUPPORTED (P, d, style, or max_tok
- * above 8388480), RK_ERR_WORKSPACE, RK_ERR_CUDA.  On the device, a run with n_tok > max_tok
- * or a negative position, a table slot beyond its run's table or the table array, or a
- * page id outside its pool sets RK_ERR_DEVICE_BOUNDS and the affected rows are skipped. */
+ * negative sizes, theta <= 1 or not finite, k_src or k_dst not 16-byte aligned),
+ * RK_ERR_UNSUPPORTED (P, d, style, or max_tok above 8388480), RK_ERR_WORKSPACE,
+ * RK_ERR_CUDA.  On the device, a run with n_tok > max_tok or a negative position or table
+ * offset is skipped whole; a table slot beyond its run's table or the table array, or a
+ * page id outside its pool, skips the rows of that page; both set RK_ERR_DEVICE_BOUNDS.
+ * A wait that exceeds its limit sets RK_ERR_TIMEOUT. */
 RK_API rk_status rk_rope_reposition(const rk_rope_args* args, void* workspace, size_t workspace_bytes,
                              rk_stream_t stream);
 

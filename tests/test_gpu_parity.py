@@ -142,6 +142,43 @@ def test_rope_mixed_d64_interleaved(rk):
     _check_rope(w, bf16_bits(_gpu_rope(rk, w)))
 
 
+def test_rope_device_bounds_skip_only_bad_rows(rk):
+    # run 0 gets a source page id outside the pool for its 4th table entry, run 1 an n_tok
+    # above max_tok: both are reported; run 0's other rows and every other run are written
+    w = synth.tiny_prefill()
+    r = w.rope
+    src_tables = r.src_tables.copy()
+    runs = r.runs.copy()
+    bad_entry = int(runs[0, 0]) + 3
+    src_tables[bad_entry] = r.k_src.shape[0] + 5
+    runs[1, 6] = r.max_tok + 1
+    job = dataclasses.replace(r, src_tables=src_tables, runs=runs)
+    dr = rope_to_device(job, "cuda")
+    dr.max_tok = r.max_tok                           # the launch's bound stays 256
+    kp = to_device(w.attn.k_pool, "cuda")
+    st = _status()
+    dr.run(rk, kp, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 4                       # RK_ERR_DEVICE_BOUNDS
+    got = bf16_bits(kp)
+    good = np.ones(len(runs), dtype=bool)
+    good[1] = False
+    pages, slots, rows, inputs = O.paged_rope_reposition(r.k_src, r.src_tables, r.dst_tables, r.runs[good], w.theta,
+                                                         r.P, r.style, return_inputs=True)
+    # rows of run 0 that read the bad source entry keep their old content
+    n0 = int(r.runs[0, 6])
+    t = np.arange(n0)
+    bad = np.zeros(len(pages), dtype=bool)
+    bad[:n0] = (int(r.runs[0, 4]) + t) // r.P == 3
+    assert bad.sum() == r.P
+    ok = O.rope_within_one_ulp(got[pages[~bad], slots[~bad]], rows[~bad], inputs[~bad], r.style)
+    assert ok.all()
+    assert np.array_equal(got[pages[bad], slots[bad]], w.attn.k_pool[pages[bad], slots[bad]])
+    # run 1 (skipped whole) leaves its destination rows unchanged
+    p1, s1, _ = O.paged_rope_reposition(r.k_src, r.src_tables, r.dst_tables, r.runs[1:2], w.theta, r.P, r.style)
+    assert np.array_equal(got[p1, s1], w.attn.k_pool[p1, s1])
+
+
 # ------------------------------------------------------------------------- prefill
 def test_whole_path_tiny(rk):
     """GPU RoPE then GPU attention vs oracle RoPE (stored as bf16) then oracle attention."""
