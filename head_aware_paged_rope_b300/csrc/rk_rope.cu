@@ -59,24 +59,26 @@ __device__ __forceinline__ void rotate_pair(float xa, float xb, const float4& cf
 }
 
 // Kernel 2 is persistent (two CTAs per SM).  The runs' tokens are cut into blocks of kRows
-// rows (8 KB of K); CTA c takes a contiguous range of blocks.  Its producer warp fetches
+// rows (32 KB of K); CTA c takes a contiguous range of blocks.  Its producer warp fetches
 // the page ids of a group of blocks at once (one table entry per lane), then copies each
-// block's source rows, one bulk copy per source page, into a ring of kStages shared-memory
-// stages, so that up to 12 blocks (96 KB) per CTA are in flight.  Eight consumer warps
-// rotate the rows (thread = row x 16 channels) and store them to their destination pages
-// with 16-byte streaming stores.  Every wait is bounded.
+// block's source rows, one bulk copy per source page (one lane each), into a ring of
+// kStages shared-memory stages.  Eight consumer warps rotate the rows (thread = row x 16
+// channels, kRowsPerThread rows each) and store them to their destination pages with
+// 16-byte streaming stores.  Every wait is bounded.
 constexpr int kRopeConsumers = 256;
 constexpr int kRopeThreads = kRopeConsumers + 32;
-constexpr int kRopeStages = 12;
+constexpr int kRopeStages = 3;
+constexpr int kRowsPerThread = 4;
 constexpr uint64_t kRopeWaitNs = 1000000000ull;
 
 template <int D>
 struct RopeCfg {
   static constexpr int kLanes = D / 16;                 // lanes per row (8 channel pairs each)
-  static constexpr int kRows = kRopeConsumers / kLanes; // rows per block: 32 (d 128), 64 (d 64)
+  static constexpr int kRowsPerPass = kRopeConsumers / kLanes;
+  static constexpr int kRows = kRowsPerPass * kRowsPerThread;   // rows per block: 128 (d 128), 256 (d 64)
   static constexpr int kRowBytes = D * 2;
-  static constexpr int kStageBytes = kRows * kRowBytes; // 8 KB
-  static constexpr int kMaxPages = kRows / 16 + 1;      // pages one block touches (P >= 16)
+  static constexpr int kStageBytes = kRows * kRowBytes; // 32 KB
+  static constexpr int kMaxPages = kRows / 16 + 1;      // pages one block touches (P >= 16): 9 or 17
   static constexpr int kSmem = kRopeStages * kStageBytes + 128;
 };
 
@@ -85,8 +87,8 @@ struct RopeMeta {
   int32_t pos_off0, pos_on0;
   int32_t src_p0, dst_p0;       // first table entry (logical page) the block touches
   uint32_t src_ok;              // bit i: the rows of source page src_p0 + i were copied
-  int32_t dst_id[5];            // physical page of destination entry dst_p0 + i, -1 if invalid
-  int32_t pad[3];
+  int32_t dst_id[17];           // physical page of destination entry dst_p0 + i, -1 if invalid
+  int32_t pad[7];
 };
 
 struct RopeShared {
@@ -250,7 +252,7 @@ __global__ __launch_bounds__(kRopeThreads) void rope_apply_kernel(
   } else {
     // ---------------------------------------------------------------- consumers
     const int ln = tid % C::kLanes;    // pairs 8*ln .. 8*ln+7
-    const int row = tid / C::kLanes;
+    const int row0 = tid / C::kLanes;
     const int ca = STYLE == RK_ROPE_HALF_SPLIT ? 8 * ln : 16 * ln;
     const int cb = STYLE == RK_ROPE_HALF_SPLIT ? D / 2 + 8 * ln : 16 * ln + 8;
     int cur_run = -1;
@@ -271,7 +273,10 @@ __global__ __launch_bounds__(kRopeThreads) void rope_apply_kernel(
 #pragma unroll
         for (int i = 0; i < 8; ++i) cf[i] = __ldg(cr + i);
       }
-      if (row < n) {
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerThread; ++rr) {
+        const int row = rr * C::kRowsPerPass + row0;
+        if (row >= n) continue;
         const int t = m.t0 + row;
         const int spos = m.pos_off0 + t, opos = m.pos_on0 + t;
         const bool src_ok = (m.src_ok >> (spos / P - m.src_p0)) & 1u;
