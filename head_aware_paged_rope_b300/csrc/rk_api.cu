@@ -183,7 +183,7 @@ DecLayoutHost dec_layout(const rk_attn_args* a) {
   static_assert(sizeof(DecHeader) == 256, "the split counters start at byte 256");
   size_t off = align256(sizeof(DecHeader));
   l.off_counters = off;
-  off += align256(sizeof(int32_t) * size_t(3 * kDecMaxGrid));   // ends at kDecCounterBytes
+  off += align256(sizeof(int32_t) * size_t(7 * kDecMaxGrid));   // ends at kDecCounterBytes
   l.off_segs = off;
   off += align256(sizeof(DecSeg) * size_t(l.nseg));
   l.off_ctas = off;

@@ -166,16 +166,31 @@ __device__ __forceinline__ int split_slot(int c, int cta0, int tile0, long long 
   return (c == cta0 && (long long)c * T / gs < tile0) ? 2 * c + 1 : 2 * c;
 }
 
-// One arrival at a counter that `need` arrivals complete: true for the last one, which also
-// returns the counter to zero.  Called by one thread after a barrier of the threads that
-// wrote the partial: the release publishes their stores (cumulativity through the barrier),
-// the acquire makes the other CTAs' partials visible to the last arrival.
-__device__ __forceinline__ int arrive_last(int32_t* cnt, int need) {
-  int old;
-  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
-  if (old != need - 1) return 0;
-  asm volatile("st.relaxed.gpu.s32 [%0], 0;" :: "l"(cnt) : "memory");
-  return 1;
+// Merge protocol of a split segment (single-launch path).  Each CTA holding a piece takes a
+// ticket from the segment's (or group's) counter as its epilogue starts; the CTA with the
+// last ticket merges.  Every other piece stores its partial and then raises its slot's flag
+// with a release store (one thread, after a barrier of the storing threads); the merger
+// waits for those flags with acquire loads, lowers them and returns the counter to zero, so
+// all of it is zero again when the kernel ends.  The merger waits only for CTAs that took a
+// ticket before it, which are running.
+__device__ __forceinline__ int take_ticket(int32_t* cnt) { return atomicAdd(cnt, 1); }
+__device__ __forceinline__ void raise_flag(int32_t* f) {
+  asm volatile("st.release.gpu.s32 [%0], 1;" :: "l"(f) : "memory");
+}
+__device__ __forceinline__ void zero_word(int32_t* f) {
+  asm volatile("st.relaxed.gpu.s32 [%0], 0;" :: "l"(f) : "memory");
+}
+__device__ __forceinline__ bool wait_flag(int32_t* f) {
+  int v;
+  asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  if (v) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(32);
+    asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v) return true;
+    if (globaltimer() - t0 > kWaitNs) return false;
+  }
 }
 
 // Log-sum-exp merge of n normalised partials (lse in log2 units) of one segment, whose slots
@@ -781,6 +796,26 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
+      const bool split = po.slot >= 0;
+      // split segment: take the merge ticket now; its round trip overlaps the epilogue
+      int ticket = 0;
+      int32_t* cnt = nullptr;
+      int need = 1, n_grp = 1, cq = 0, gslot = 0;
+      bool two = false;
+      if constexpr (FUSED) {
+        if (split) {
+          const long long T = sh.T, gs = sh.gs;
+          const int n = po.n_splits, j = int(blockIdx.x) - po.cta0;
+          two = n > kMergeFan;
+          n_grp = (n + kMergeFan - 1) / kMergeFan;
+          const int q = j / kMergeFan;
+          cq = po.cta0 + q * kMergeFan;
+          gslot = split_slot(cq, po.cta0, po.tile0, T, gs);
+          cnt = two ? ws.counters + kDecMaxGrid + gslot : ws.counters + po.cta0;
+          need = two ? min(kMergeFan, n - q * kMergeFan) : n;
+          if (t == 0) ticket = take_ticket(cnt);
+        }
+      }
       const bool got_o = wait_or_abort(sh, smem_addr(&sh.p_empty[(gg - 1) & 1]), ((gg - 1) >> 1) & 1);
       tc_fence_after();
       uint32_t ov[16];
@@ -805,7 +840,6 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         sh.lse2[t] = ll > 0.f ? mm + fast_log2(ll) : -INFINITY;
       }
       named_bar_sync(1, 128);
-      const bool split = po.slot >= 0;
       if (t < D) {
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
@@ -825,34 +859,54 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       }
       if constexpr (FUSED) {
         if (split) {
-          // The CTA whose partial completes the segment merges them all (log-sum-exp).  A
-          // segment cut over more than kMergeFan CTAs is merged in two levels: groups of
-          // kMergeFan consecutive CTAs first, each by the group's last arrival, then the
-          // group results.  Every counter is returned to zero by the CTA that reads it last.
+          // Log-sum-exp merge of the segment's pieces by the CTA with the last ticket; beyond
+          // kMergeFan pieces in two levels (groups of kMergeFan consecutive CTAs, then the
+          // group results).
           const long long T = sh.T, gs = sh.gs;
-          const int n = po.n_splits, j = int(blockIdx.x) - po.cta0;
-          const bool two = n > kMergeFan;
-          const int n_grp = (n + kMergeFan - 1) / kMergeFan;
-          const int q = j / kMergeFan, cq = po.cta0 + q * kMergeFan;
-          const int gslot = split_slot(cq, po.cta0, po.tile0, T, gs);
-          int32_t* cnt = two ? ws.counters + kDecMaxGrid + gslot : ws.counters + po.cta0;
-          const int need = two ? min(kMergeFan, n - q * kMergeFan) : n;
+          int32_t* flags = ws.counters + 3 * kDecMaxGrid;    // per partial slot
+          int32_t* gflags = ws.counters + 5 * kDecMaxGrid;   // per group slot
+          named_bar_sync(1, 128);                            // every partial store of the CTA is done
+          if (t == 0) sh.last = ticket == need - 1;
           named_bar_sync(1, 128);
-          if (t == 0) sh.last = arrive_last(cnt, need);
-          named_bar_sync(1, 128);
-          if (sh.last) {
+          if (!sh.last) {
+            if (t == 0) raise_flag(flags + po.slot);
+          } else {
+            int ticket2 = 0;
+            if (t == 0) {
+              zero_word(cnt);
+              if (two) ticket2 = take_ticket(ws.counters + po.cta0);
+            }
+            if (t < need) {   // the group's (or segment's) other pieces
+              const int s = split_slot(cq + t, po.cta0, po.tile0, T, gs);
+              if (s != po.slot) {
+                if (!wait_flag(flags + s)) report(p.status, RK_ERR_TIMEOUT);
+                zero_word(flags + s);
+              }
+            }
+            named_bar_sync(1, 128);
             __nv_bfloat16* out_row = p.out + (int64_t(po.tok) * p.Hq + h * G) * D;
             float* lse_row = p.lse ? p.lse + int64_t(po.tok) * p.Hq + h * G : nullptr;
             if (!two) {
-              merge_splits<D>(n, po.cta0, 1, po.cta0, po.tile0, T, gs, ws.part_lse, ws.part_o, G, out_row, lse_row,
+              merge_splits<D>(need, cq, 1, po.cta0, po.tile0, T, gs, ws.part_lse, ws.part_o, G, out_row, lse_row,
                               nullptr, nullptr, t);
             } else {
               merge_splits<D>(need, cq, 1, po.cta0, po.tile0, T, gs, ws.part_lse, ws.part_o, G, nullptr, nullptr,
                               ws.grp_lse + int64_t(gslot) * G, ws.grp_o + int64_t(gslot) * G * D, t);
+              named_bar_sync(1, 128);                        // the group result is stored
+              if (t == 0) sh.last = ticket2 == n_grp - 1;
               named_bar_sync(1, 128);
-              if (t == 0) sh.last = arrive_last(ws.counters + po.cta0, n_grp);
-              named_bar_sync(1, 128);
-              if (sh.last) {
+              if (!sh.last) {
+                if (t == 0) raise_flag(gflags + gslot);
+              } else {
+                if (t == 0) zero_word(ws.counters + po.cta0);
+                if (t < n_grp) {
+                  const int s = split_slot(po.cta0 + t * kMergeFan, po.cta0, po.tile0, T, gs);
+                  if (s != gslot) {
+                    if (!wait_flag(gflags + s)) report(p.status, RK_ERR_TIMEOUT);
+                    zero_word(gflags + s);
+                  }
+                }
+                named_bar_sync(1, 128);
                 merge_splits<D>(n_grp, po.cta0, kMergeFan, po.cta0, po.tile0, T, gs, ws.grp_lse, ws.grp_o, G,
                                 out_row, lse_row, nullptr, nullptr, t);
               }

@@ -155,8 +155,9 @@ struct DecHeader {
 
 struct DecWorkspace {
   DecHeader* header;
-  int32_t* counters;     // [3 * kDecMaxGrid] split arrivals, zero between calls (single-launch path):
-                         // per segment (indexed by its first CTA), then per group of CTAs (by slot)
+  int32_t* counters;     // [7 * kDecMaxGrid], zero between calls (single-launch path): merge tickets
+                         // per segment (by its first CTA) and per group of CTAs (by group slot),
+                         // then ready flags per partial slot and per group slot
   DecSeg* segs;          // [B*Hkv]
   DecCta* ctas;          // [grid]
   int32_t* split_segs;   // [B*Hkv]
@@ -172,7 +173,7 @@ constexpr int kDecTileKeys = 128;
 constexpr int kDecMaxSegs = 16384;   // B * Hkv of one decode call (the planner keeps 8 bytes per segment on chip)
 constexpr int kDecFusedSegs = 512;   // up to this many segments every decode CTA plans for itself
 constexpr int kDecMaxGrid = 1024;    // split counters kept at the start of the decode workspace
-constexpr size_t kDecCounterBytes = 256 + sizeof(int32_t) * 3 * kDecMaxGrid;   // header + counters
+constexpr size_t kDecCounterBytes = 256 + sizeof(int32_t) * 7 * kDecMaxGrid;   // header + counters + flags
 
 // Lower bound (first entry >= x) of an ascending logical-page list from its two ends: the
 // answer when the ends decide it, else -1 and a guess g (1 <= g <= n-1) to verify with

@@ -196,7 +196,7 @@ RK_API rk_status rk_segpaged_prefill(const rk_attn_args* args, void* workspace, 
  * over each head's visible pages, partial results merged by log-sum-exp.  Same errors, and
  * RK_ERR_UNSUPPORTED when B * Hkv exceeds 16384.
  *
- * Workspace: its first 12544 bytes hold per-call split counters.  They must be zero before
+ * Workspace: its first 28928 bytes hold per-call split counters and flags.  They must be zero before
  * the first decode call that uses the workspace (e.g. cudaMemsetAsync of the whole
  * buffer once, after allocating it); every call returns them to zero before it completes,
  * so the workspace can be reused by any later decode call, of any shape, on the same
