@@ -154,6 +154,20 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(torch, value, device, world):
+    """The largest of a per-rank time over all ranks (the job's time is its slowest rank)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(work_per_rank, world, ms):
+    """Whole-job rate: every rank processes `work_per_rank` units (weak scaling) in `ms`."""
+    return work_per_rank * world / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- reference arm
 def _oracle_sample(layer_wl, n_queries, seed):
     """Rows (query token, KV head) sampled from a layer: n_queries spread tokens x all KV heads."""
@@ -394,10 +408,7 @@ def ours_main(args, world, rank, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(torch, ms_step, dev, world)
 
     # per-phase timing (each phase captured alone and replayed)
     parts = {}
@@ -439,7 +450,7 @@ def ours_main(args, world, rank, local):
     roof["peak_source"] = peaks_src + (" (burst)" if roof["bound"] == "tensor" else " (copy)")
 
     step_flops = flops_prefill + flops_decode
-    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(step_flops, world, ms_step) / 1e12
 
     # end-to-end through the C ABI from pinned host buffers
     e2e = None
@@ -468,12 +479,8 @@ def ours_main(args, world, rank, local):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = e0.elapsed_time(e1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": step_flops * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ms_e2e = max_over_ranks(torch, e0.elapsed_time(e1) / args.e2e_steps, dev, world)
+        e2e = {"value": job_throughput(step_flops, world, ms_e2e) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": args.e2e_steps}
         del ins, outs
 
