@@ -58,7 +58,6 @@ def parse_args():
 def profiled_traffic(kernel):
     """DRAM bytes per launch of `kernel` from the ncu capture summarised in profiles/, or None
     when the kernel's sources have changed since (their SHA-256 is recorded with the figure)."""
-    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -66,11 +65,22 @@ def profiled_traffic(kernel):
         entry = json.load(f).get(kernel)
     if not entry:
         return None
+    return entry["dram_bytes_per_launch"] if sources_digest(entry["sources"]) == entry["sources_sha256"] else None
+
+
+def sources_digest(paths):
+    """SHA-256 of the code of `paths` with comments and blank space removed (comment edits
+    leave a measurement valid, code edits do not)."""
+    import hashlib
+    import re
     h = hashlib.sha256()
-    for rel in entry["sources"]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    return entry["dram_bytes_per_launch"] if h.hexdigest() == entry["sources_sha256"] else None
+    for rel in paths:
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(re.sub(r"\s+", " ", text).strip().encode())
+    return h.hexdigest()
 
 
 def load_peaks():

@@ -11,9 +11,15 @@
 //   S^T[key][g]  = K[key][:] . q[g][:]           M = 128 keys, N = 16 (G heads, padded), K = d
 //   O^T[c][g]   += V^T[c][key] . P^T[key][g]     M = 128 channels, N = 16, K = 128 keys
 //
-// Schedule (rk_plan.cu, plan_decode_kernel): the 128-key tiles of all head segments form
-// one sequence and CTA c takes the equal share [c*T/gs, (c+1)*T/gs) of it (gs = the
-// smaller of the grid, one CTA per SM, and T).  A share is walked as "portions" (the part of one segment inside the share).
+// Schedule: the 128-key tiles of all head segments form one sequence of T tiles and CTA c
+// takes the equal share [c*T/gs, (c+1)*T/gs) of it (gs = the smaller of the grid, one CTA
+// per SM, and T); when no segment has more than kAlignTiles tiles and there are no more
+// segments than CTAs, CTA c takes segment c whole instead.  Up to kDecFusedSegs head
+// segments every CTA plans this itself (visible ranges in three interleaved rounds of
+// loads, a block scan of the tile counts) and a segment shared by several CTAs is merged
+// inside the kernel; beyond that, plan_decode_kernel (rk_plan.cu) plans and
+// combine_decode_tc_kernel merges.  A share is walked as "portions" (the part of one
+// segment inside the share).
 //   warp 4   producer: walks the share, pushes each portion into a 2-entry ring, loads its
 //            G query rows (TMA) into one of two Q buffers, and gathers each tile page by
 //            page (one TMA box per page and 64 channels) from the shared K and V pools
@@ -26,8 +32,8 @@
 //            keeps a per-head running maximum that moves only when it grows by more than
 //            2^8 (then O^T is rescaled in TMEM), writes P^T = 2^(S - m) as bf16 into shared
 //            memory, and at the end of a portion normalises O^T and stores it -- the output
-//            itself, or, for a segment shared with other CTAs, a partial result that
-//            combine_decode_tc_kernel merges by log-sum-exp.
+//            itself, or, for a segment shared with other CTAs, a partial result for the
+//            log-sum-exp merge.
 // Every wait is bounded; a timeout sets RK_ERR_TIMEOUT and all roles leave.
 #include "rk_internal.cuh"
 #include "rk_sm100.cuh"
