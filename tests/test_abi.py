@@ -104,3 +104,32 @@ def test_workspace_size_grows_with_queries(rk):
     small = rk.segpaged_prefill_workspace_size(_attn_args(rk, total_q=10))
     big = rk.segpaged_prefill_workspace_size(_attn_args(rk, total_q=10000, max_q=5000))
     assert 0 < small < big
+
+
+def test_unknown_flag_bits_are_rejected(rk):
+    a = _attn_args(rk, flags=2)
+    assert rk.LIB.rk_segpaged_prefill(ctypes.byref(a), None, 0, None) == 1
+    d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_METADATA_STABLE | 4)
+    assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 1
+    d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_METADATA_STABLE)
+    assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 6           # valid flag: workspace next
+
+
+def test_decode_workspace_holds_the_zeroed_counter_prefix(rk):
+    # the split tickets and ready flags (7 x 1024 int32 after a 256-byte header) come first
+    for B, Hkv in ((1, 1), (32, 8), (1000, 8)):
+        a = _attn_args(rk, cu_seqlens_q=None, B=B, Hq=8 * Hkv, Hkv=Hkv, total_q=B, max_q=1)
+        assert rk.segpaged_decode_workspace_size(a) >= 256 + 4 * 7 * 1024
+
+
+def test_decode_rejects_more_segments_than_supported(rk):
+    a = _attn_args(rk, cu_seqlens_q=None, B=4096, Hq=64, Hkv=8, total_q=4096, max_q=1)   # 32768 segments
+    assert rk.LIB.rk_segpaged_decode(ctypes.byref(a), ctypes.c_void_p(1 << 20), 1 << 30, None) == 2
+
+
+def test_misaligned_pools_are_rejected_before_any_launch(rk):
+    ws = ctypes.c_void_p(1 << 20)                                          # never dereferenced on the host
+    a = _rope_args(rk, k_src=8)                                            # 8-byte aligned only
+    assert rk.LIB.rk_rope_reposition(ctypes.byref(a), ws, 1 << 30, None) == 1
+    p = _attn_args(rk, q=16, k_pool=24)
+    assert rk.LIB.rk_segpaged_prefill(ctypes.byref(p), ws, 1 << 40, None) == 1
