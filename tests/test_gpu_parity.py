@@ -316,6 +316,36 @@ def test_decode_empty_lists_and_empty_context(rk, flags):
     _compare(a, out, lse, rows=rows)
 
 
+def _last_query_decode(attn):
+    """Decode batch from a prefill batch: each sequence's last suffix query, at seq_len - 1."""
+    last = np.asarray(attn.cu_seqlens_q[1:]) - 1
+    return dataclasses.replace(attn, q=np.ascontiguousarray(attn.q[last]),
+                               cu_seqlens_q=np.arange(attn.B + 1, dtype=np.int32), name=attn.name + "_decode")
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_decode_mixed_classes_retrieval_and_dense(rk, flags):
+    # every head class, retrieval heads listing a random subset of pages (the planner's
+    # search falls back from its guesses), page 32
+    w = synth.mixed_classes(B=4, lengths=(1024, 2048, 3000), suffix_range=(40, 90), seg_tokens=512)
+    a = _last_query_decode(w.attn)
+    out, lse = _gpu_attn(rk, a, decode=True, flags=flags)
+    _compare(a, out, lse)
+
+
+def test_decode_page32_d64(rk):
+    w = synth.decode_microbench(B=5, ctx=2500, Hq=16, Hkv=4, d=64, P=32, window=200, sink=4, seed=31)
+    out, lse = _gpu_attn(rk, w.attn, decode=True, flags=rk.RK_ATTN_METADATA_STABLE)
+    _compare(w.attn, out, lse)
+
+
+def test_prefill_page32_d64_mixed(rk):
+    w = synth.mixed_classes(B=3, lengths=(1024, 2048), suffix_range=(50, 140), seg_tokens=512, Hq=16, Hkv=8, d=64,
+                            P=32)
+    out, lse = _gpu_attn(rk, w.attn)
+    _compare(w.attn, out, lse)
+
+
 def test_decode_many_segments_separate_planner(rk):
     # 576 head segments: more than every CTA plans for itself, so the separate planning and
     # merging kernels run
