@@ -133,3 +133,20 @@ def test_misaligned_pools_are_rejected_before_any_launch(rk):
     assert rk.LIB.rk_rope_reposition(ctypes.byref(a), ws, 1 << 30, None) == 1
     p = _attn_args(rk, q=16, k_pool=24)
     assert rk.LIB.rk_segpaged_prefill(ctypes.byref(p), ws, 1 << 40, None) == 1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    # the binding has no CPU path: without librk.so it raises instead of computing anything
+    import head_aware_paged_rope_b300._binding as B
+    with pytest.raises(ImportError):
+        B.load_library(str(tmp_path / "librk.so"))
+
+
+def test_oracle_is_not_imported_by_the_product_path():
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r); import head_aware_paged_rope_b300 as rk; rk.LIB; "
+            "import head_aware_paged_rope_b300.roofline; "
+            "assert not any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules), 'oracle imported'" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
