@@ -267,3 +267,64 @@ def test_rope_tolerance_floor_only_covers_fp64_roundoff():
     # and so is a small absolute error well above the fp64 round-off
     got3 = np.array([[0x3F80, 0, 0x2F00, 0]], np.uint16)      # 1.2e-10 where 1.4e-17 is exact
     assert not O.rope_within_one_ulp(got3, exact, x, O.ROPE_HALF_SPLIT)[0, 2]
+
+
+# ------------------------------------------------------------------ sparse page lists
+def test_gather_rows_on_a_sparse_list_follows_the_block_table():
+    """The worked block table of "PagedAttention & RadixAttention" (block size 4; logical
+    blocks 0, 1, 2 in physical blocks 7, 1, 3) with logical block 1 dropped from the list,
+    as a retrieval head or a window-only local head lists its pages: entry e of the list
+    holds logical page [0, 2][e] in physical page [7, 3][e].  gather_rows must return, for
+    every position of a listed page, the row token_to_physical gives on the full table --
+    not the row of entry position // P (which would be logical block 1's page or past the
+    list)."""
+    g = _load("vllm_block_table.json")
+    P, full = g["block_size"], g["block_table"]
+    rng = np.random.default_rng(12)
+    pool = rng.integers(0, 2 ** 15, size=(g["n_physical_blocks"], P, 3)).astype(np.uint16)
+    listed_logical = np.array([0, 2], np.int32)
+    table_row = np.array([full[0], full[2]], np.int32)          # [7, 3]
+    positions = np.array([0, 1, 2, 3, 8], np.int64)               # the tokens of logical blocks 0 and 2
+    got = O.gather_rows(pool, table_row, listed_logical, 2, P, positions)
+    for i, t in enumerate(positions):
+        phys, slot = O.token_to_physical(full, P, int(t))
+        assert np.array_equal(got[i], O.bf16_to_f64(pool[phys, slot]))
+    assert O.listed_positions(listed_logical, 2, P).tolist() == [0, 1, 2, 3, 8, 9, 10, 11]
+    with pytest.raises(KeyError):                                # position 5 is on an unlisted page
+        O.gather_rows(pool, table_row, listed_logical, 2, P, np.array([5]))
+
+
+def test_retrieval_head_on_a_sparse_list_equals_hand_indexed_attention():
+    """A retrieval head listing logical pages 0, 2 and 5 (of 6) in hand-picked physical
+    pages: its output equals softmax attention over the keys read straight from the pool
+    at (physical page of the listed logical page, slot), enumerated here by hand from the
+    page size and the causal bound -- no table lookup shared with the oracle."""
+    P, d, Hq, Hkv = 4, 8, 2, 1
+    rng = np.random.default_rng(13)
+    n_pool = 9
+    k_pool = synth.f32_to_bf16_bits(rng.standard_normal((n_pool, P, d)).astype(np.float32))
+    v_pool = synth.f32_to_bf16_bits(rng.standard_normal((n_pool, P, d)).astype(np.float32))
+    q = synth.f32_to_bf16_bits(rng.standard_normal((2, Hq, d)).astype(np.float32))
+    # logical page 0 -> physical 6, logical 2 -> physical 1, logical 5 -> physical 4
+    table = np.array([[6, 1, 4, -1]], np.int32)
+    logical = np.array([[0, 2, 5, -1]], np.int32)
+    batch = synth.AttnBatch(B=1, Hq=Hq, Hkv=Hkv, d=d, P=P, q=q, cu_seqlens_q=np.array([0, 2], np.int32),
+                            seq_len=np.array([23], np.int32), k_pool=k_pool, v_pool=v_pool, page_table=table,
+                            page_logical=logical, n_pages=np.array([3], np.int32),
+                            head_class=np.array([O.RETRIEVAL], np.int32), window=np.array([0], np.int32),
+                            sink=np.array([0], np.int32))
+    res = O.segpaged_attention(batch)
+    # query 0 at position 21, query 1 at 22: listed positions 0-3, 8-11 and 20-23, causal
+    by_hand = {21: [(6, 0), (6, 1), (6, 2), (6, 3), (1, 0), (1, 1), (1, 2), (1, 3), (4, 0), (4, 1)],
+               22: [(6, 0), (6, 1), (6, 2), (6, 3), (1, 0), (1, 1), (1, 2), (1, 3), (4, 0), (4, 1), (4, 2)]}
+    for t, p in ((0, 21), (1, 22)):
+        rows = by_hand[p]
+        kk = np.stack([O.bf16_to_f64(k_pool[pg, s]) for pg, s in rows])
+        vv = np.stack([O.bf16_to_f64(v_pool[pg, s]) for pg, s in rows])
+        qq = O.bf16_to_f64(q[t])
+        s = qq @ kk.T / math.sqrt(d)
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        o = (w @ vv) / w.sum(axis=1, keepdims=True)
+        got_o, got_l = res[(t, 0)]
+        assert np.allclose(got_o, o, atol=1e-13)
+        assert np.allclose(got_l, np.log(np.exp(s).sum(axis=1)), atol=1e-12)
