@@ -15,10 +15,12 @@ import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librk.so")
 
-RK_OK, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED, RK_ERR_CUDA, RK_ERR_DEVICE_BOUNDS, RK_ERR_TIMEOUT, RK_ERR_WORKSPACE = range(7)
+(RK_OK, RK_ERR_INVALID_ARG, RK_ERR_UNSUPPORTED, RK_ERR_CUDA, RK_ERR_DEVICE_BOUNDS, RK_ERR_TIMEOUT, RK_ERR_WORKSPACE,
+ RK_ERR_DEVICE_ORDER) = range(8)
 RK_CLASS_GLOBAL, RK_CLASS_LOCAL, RK_CLASS_RETRIEVAL, RK_CLASS_DENSE = range(4)
 RK_ROPE_HALF_SPLIT, RK_ROPE_INTERLEAVED = 0, 1
 RK_ATTN_METADATA_STABLE = 1
+RK_ATTN_DIAG_EXPIRE_WAIT = 1 << 30
 
 
 class RkError(RuntimeError):

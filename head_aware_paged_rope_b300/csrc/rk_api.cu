@@ -9,33 +9,9 @@
 
 namespace rk {
 
-int prefill_mma_rows();
-int prefill_mma_keys();
 int prefill_tc_rows();
 int prefill_tc_keys();
 cudaError_t launch_prefill_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cudaStream_t stream);
-
-// The prefill kernel: tcgen05 (default) or the mma.sync baseline, the latter kept only for
-// A/B measurement (RK_PREFILL_KERNEL=mma).
-static bool use_mma_prefill() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("RK_PREFILL_KERNEL");
-    v = (e && std::string(e) == "mma") ? 1 : 0;
-  }
-  return v == 1;
-}
-
-// The decode kernel: tcgen05 (default) or the CUDA-core split-KV kernel, the latter kept for
-// A/B measurement (RK_DECODE_KERNEL=simt).
-static bool use_simt_decode() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("RK_DECODE_KERNEL");
-    v = (e && std::string(e) == "simt") ? 1 : 0;
-  }
-  return v == 1;
-}
 
 int device_sm_count() {
   static int cache[64] = {0};
@@ -52,9 +28,9 @@ namespace {
 
 bool supported_dp(int d, int P) { return (d == 64 || d == 128) && (P == 16 || P == 32); }
 
-// Sizes shared by the workspace-size functions and the entry points.
+// Prefill workspace sizes, shared by the workspace-size function and the entry point.
 struct AttnLayout {
-  int rows;         // rows per unit (query tile rows, or G for decode)
+  int rows;         // rows per unit (query tile rows)
   int tok_per_unit;
   int max_units;
   int max_items;
@@ -84,7 +60,7 @@ rk_status check_attn(const rk_attn_args* a, bool decode) {
   if (a->n_pool_pages * int64_t(a->P) >= (int64_t(1) << 31) || int64_t(a->total_q) * a->Hq >= (int64_t(1) << 31))
     return RK_ERR_UNSUPPORTED;   // row coordinates of the tensor maps are int32
   if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
-  if (a->flags & ~RK_ATTN_METADATA_STABLE) return RK_ERR_INVALID_ARG;
+  if (a->flags & ~(RK_ATTN_METADATA_STABLE | RK_ATTN_DIAG_EXPIRE_WAIT)) return RK_ERR_INVALID_ARG;
   return RK_OK;
 }
 
@@ -94,19 +70,13 @@ bool aligned16(const rk_attn_args* a) {
   return ok(a->q) && ok(a->k_pool) && ok(a->v_pool) && ok(a->out);
 }
 
-AttnLayout attn_layout(const rk_attn_args* a, bool decode) {
+AttnLayout attn_layout(const rk_attn_args* a) {
   AttnLayout l{};
   const int G = a->Hq / a->Hkv;
-  if (decode) {
-    l.rows = G;
-    l.tok_per_unit = 1;
-    l.max_units = a->B * a->Hkv;
-  } else {
-    l.rows = use_mma_prefill() ? prefill_mma_rows() : prefill_tc_rows();
-    l.tok_per_unit = l.rows / G;
-    const int64_t tiles = (int64_t(a->total_q) + l.tok_per_unit - 1) / l.tok_per_unit + a->B;
-    l.max_units = int(std::min<int64_t>(tiles * a->Hkv, int64_t(1) << 30));
-  }
+  l.rows = prefill_tc_rows();
+  l.tok_per_unit = l.rows / G;
+  const int64_t tiles = (int64_t(a->total_q) + l.tok_per_unit - 1) / l.tok_per_unit + a->B;
+  l.max_units = int(std::min<int64_t>(tiles * a->Hkv, int64_t(1) << 30));
   l.max_items = l.max_units + kTargetItems;
   size_t off = align256(sizeof(PlanHeader));
   l.off_units = off;
@@ -219,9 +189,7 @@ DecWorkspace make_dec_ws(void* base, const DecLayoutHost& l) {
   return ws;
 }
 
-size_t decode_ws_bytes(const rk_attn_args* a) {
-  return use_simt_decode() ? attn_layout(a, true).total : dec_layout(a).total;
-}
+size_t decode_ws_bytes(const rk_attn_args* a) { return dec_layout(a).total; }
 
 rk_status check_ws(void* ws, size_t bytes, size_t need) {
   if (need == 0) return RK_OK;
@@ -234,7 +202,7 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
   if (st != RK_OK) return st;
   if (a->B == 0 || a->total_q == 0) return RK_OK;
   const int sms = device_sm_count();
-  if (decode && !use_simt_decode()) {
+  if (decode) {
     if (int64_t(a->B) * a->Hkv > kDecMaxSegs) return RK_ERR_UNSUPPORTED;
     const DecLayoutHost dl = dec_layout(a);
     st = check_ws(workspace, bytes, dl.total);
@@ -248,33 +216,17 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
     const cudaError_t e = launch_decode_tc(p, ws, stream);
     return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
   }
-  const AttnLayout l = attn_layout(a, decode);
+  const AttnLayout l = attn_layout(a);
   st = check_ws(workspace, bytes, l.total);
   if (st != RK_OK) return st;
   if (!aligned16(a)) return RK_ERR_INVALID_ARG;
   const AttnParams p = make_params(a, l);
   const AttnWorkspace ws = make_ws(workspace, l);
-  cudaError_t e;
-  if (decode) {
-    const int grid = std::max(1, std::min(l.max_items, sms * decode_ctas_per_sm(a->P)));
-    e = launch_plan(p, ws, 1, 1, std::min(kTargetItems, grid), 4, true, stream);
-    if (e == cudaSuccess) e = launch_decode(p, ws, grid, stream);
-    if (e == cudaSuccess) e = launch_combine_decode(p, ws, stream);
-    return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
-  } else {
-    if (use_mma_prefill()) {
-      const int grid = std::max(1, std::min(l.max_items, sms * 2));
-      const int ept = prefill_mma_keys() / a->P;
-      e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 4, false, stream);
-      if (e == cudaSuccess) e = launch_prefill_mma(p, ws, grid, stream);
-    } else {
-      const int grid = std::max(1, std::min(l.max_items, sms));
-      const int ept = prefill_tc_keys() / a->P;
-      e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 2, false, stream);
-      if (e == cudaSuccess) e = launch_prefill_tc(p, ws, grid, stream);
-    }
-  }
-  if (e == cudaSuccess) e = launch_combine(p, ws, decode, stream);
+  const int grid = std::max(1, std::min(l.max_items, sms));
+  const int ept = prefill_tc_keys() / a->P;
+  cudaError_t e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 2, stream);
+  if (e == cudaSuccess) e = launch_prefill_tc(p, ws, grid, stream);
+  if (e == cudaSuccess) e = launch_combine(p, ws, stream);
   return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }
 
@@ -311,7 +263,7 @@ rk_status rk_rope_reposition(const rk_rope_args* a, void* workspace, size_t work
 size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* a) {
   if (rk::check_attn(a, false) != RK_OK) return 0;
   if (a->B == 0 || a->total_q == 0) return 0;
-  return rk::attn_layout(a, false).total;
+  return rk::attn_layout(a).total;
 }
 
 size_t rk_segpaged_decode_workspace_size(const rk_attn_args* a) {
@@ -337,6 +289,7 @@ const char* rk_status_string(rk_status s) {
     case RK_ERR_DEVICE_BOUNDS: return "device-side bounds check failed";
     case RK_ERR_TIMEOUT: return "device-side wait timed out";
     case RK_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case RK_ERR_DEVICE_ORDER: return "device-side check failed: page_logical list not ascending";
   }
   return "unknown status";
 }

@@ -703,8 +703,13 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const int my_col = lane / LPC;
     uint32_t gg = 0;
     bool ok = true;
+    if (early) grid_dependency_wait();
+    if ((p.flags & RK_ATTN_DIAG_EXPIRE_WAIT) && blockIdx.x == 0) {
+      // diagnostic: a wait on a header word that nothing sets runs out; all roles then leave
+      const bool got = t == 0 ? wait_flag(&ws.header->pad[0]) : true;
+      ok = named_bar_and(1, 128, got);
+    }
     if constexpr (FUSED) {
-      if (early) grid_dependency_wait();
       // segments with nothing visible (every CTA planned them): out = 0, lse = -inf, written
       // by CTA seg % grid
       for (int seg = blockIdx.x; seg < nseg; seg += gridDim.x) {

@@ -120,7 +120,7 @@ struct AttnWorkspace {
   float* part_o;       // [max_items][rows][d]
   int32_t max_units;
   int32_t max_items;
-  int32_t rows;        // rows per unit (query tile rows or G for decode)
+  int32_t rows;        // rows per unit (query tile rows)
 };
 
 constexpr int kTargetItems = 2048;   // upper bound on items beyond one per unit
@@ -232,6 +232,8 @@ struct DecRange {
     }
   }
   __device__ __forceinline__ void load3(const AttnParams& p) {
+    // n strictly ascending entries span at least n - 1 logical pages
+    if (lrow && n > 1 && L > 0 && (long long)last - first < n - 1) report(p.status, RK_ERR_DEVICE_ORDER);
     g_hi = g_w = g_s = -1;
     r_hi = r_w = r_s = 0;
     if (L <= 0 || n <= 0) return;
@@ -315,21 +317,13 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
 
 // Launchers implemented in the .cu files.
 cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int rows_per_unit,
-                        int entries_per_tile, int target_items, int min_chunk_tiles,
-                        bool decode, cudaStream_t stream);
-cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, bool decode,
-                           cudaStream_t stream);
-cudaError_t launch_prefill_mma(const AttnParams& p, const AttnWorkspace& ws, int grid,
-                               cudaStream_t stream);
-cudaError_t launch_decode(const AttnParams& p, const AttnWorkspace& ws, int grid,
-                          cudaStream_t stream);
-cudaError_t launch_combine_decode(const AttnParams& p, const AttnWorkspace& ws, cudaStream_t stream);
+                        int entries_per_tile, int target_items, int min_chunk_tiles, cudaStream_t stream);
+cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, cudaStream_t stream);
 cudaError_t launch_plan_decode(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream);
 cudaError_t launch_decode_tc(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream);
 // bf16 2-D / 3-D tensor map with 128-byte swizzle (rk_prefill_tc.cu)
 bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                       const cuuint32_t* box);
-int decode_ctas_per_sm(int P);
 cudaError_t launch_rope(const rk_rope_args& a, void* workspace, cudaStream_t stream);
 
 int device_sm_count();

@@ -32,8 +32,10 @@ extern "C" rk_status rk_segpaged_decode_noalloc(const rk_attn_args* args, rk_str
     if (!g_scratch_addr[dev]) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return RK_ERR_CUDA;
-      // the decode workspace's split counters start at zero (each call leaves them so)
-      if (cudaMemset(p, 0, rk::kDecCounterBytes) != cudaSuccess) return RK_ERR_CUDA;
+      // the decode workspace's split counters start at zero (each call leaves them so); the
+      // zeroing is ordered before this call's decode on the caller's stream
+      if (cudaMemsetAsync(p, 0, rk::kDecCounterBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return RK_ERR_CUDA;
       g_scratch_addr[dev] = p;
     }
     scratch = g_scratch_addr[dev];

@@ -48,8 +48,7 @@ __device__ __forceinline__ int upper_bound_lp(const int32_t* row, int n, int x) 
 
 __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWorkspace ws, int tok_per_unit,
                                                             int entries_per_tile, int target_items,
-                                                            int min_chunk_tiles, int decode,
-                                                            int32_t* tile_prefix) {
+                                                            int min_chunk_tiles, int32_t* tile_prefix) {
   __shared__ int s_warp[32];
   __shared__ unsigned long long s_total_entries;
   __shared__ int s_chunk;
@@ -64,7 +63,7 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
     const int b = base + tid;
     int tiles = 0;
     if (b < p.B) {
-      const int nq = decode ? 1 : (__ldg(p.cu_seqlens_q + b + 1) - __ldg(p.cu_seqlens_q + b));
+      const int nq = __ldg(p.cu_seqlens_q + b + 1) - __ldg(p.cu_seqlens_q + b);
       tiles = nq > 0 ? (nq + tok_per_unit - 1) / tok_per_unit : 0;
     }
     int total;
@@ -93,8 +92,8 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
     const int b = lo;
     const int tile = tile_g - tile_prefix[b];
     const int seg = b * p.Hkv + h;
-    const int q0 = decode ? b : __ldg(p.cu_seqlens_q + b);
-    const int nq = decode ? 1 : (__ldg(p.cu_seqlens_q + b + 1) - q0);
+    const int q0 = __ldg(p.cu_seqlens_q + b);
+    const int nq = __ldg(p.cu_seqlens_q + b + 1) - q0;
     const int L = __ldg(p.seq_len + b);
     Unit un;
     un.seg = seg;
@@ -115,6 +114,8 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
     const int p_first = un.pos0, p_last = un.pos0 + un.ntok - 1;
     if (L > 0 && p_last >= 0 && n > 0) {
       const int32_t* lrow = p.page_logical ? p.page_logical + int64_t(seg) * p.max_pages : nullptr;
+      // n strictly ascending entries span at least n - 1 logical pages
+      if (lrow && n > 1 && (long long)__ldg(lrow + n - 1) - __ldg(lrow) < n - 1) report(p.status, RK_ERR_DEVICE_ORDER);
       const int cap = min(p_last, L - 1);
       const int e_hi = upper_bound_lp(lrow, n, cap / p.P);
       const int cls = __ldg(p.head_class + seg);
@@ -420,20 +421,18 @@ cudaError_t launch_plan_decode(const AttnParams& p, const DecWorkspace& ws, cuda
 }
 
 cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int tok_per_unit,
-                        int entries_per_tile, int target_items, int min_chunk_tiles, bool decode,
-                        cudaStream_t stream) {
+                        int entries_per_tile, int target_items, int min_chunk_tiles, cudaStream_t stream) {
   // the tile prefix lives right after the partial outputs (sized by the host)
   int32_t* tile_prefix = reinterpret_cast<int32_t*>(ws.part_o + int64_t(ws.max_items) * ws.rows * p.d);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(1), dim3(kPlanThreads), 0, stream, attr);
   return cudaLaunchKernelEx(&cfg, plan_kernel, p, ws, tok_per_unit, entries_per_tile, target_items,
-                            min_chunk_tiles, decode ? 1 : 0, tile_prefix);
+                            min_chunk_tiles, tile_prefix);
 }
 
-cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, bool decode, cudaStream_t stream) {
+cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, cudaStream_t stream) {
   const long long blocks = (long long)ws.max_units * ((ws.rows + 7) / 8);
   const int grid = int(std::max(1LL, std::min(blocks, (long long)device_sm_count() * 8)));
-  (void)decode;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, stream, attr);
   return p.d == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p, ws)

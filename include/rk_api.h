@@ -61,7 +61,8 @@ typedef enum rk_status {
   RK_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
   RK_ERR_DEVICE_BOUNDS = 4,  /* device-side check: page id / slot / table index out of range */
   RK_ERR_TIMEOUT = 5,        /* device-side bounded wait gave up */
-  RK_ERR_WORKSPACE = 6       /* workspace NULL, misaligned (256 B) or smaller than required */
+  RK_ERR_WORKSPACE = 6,      /* workspace NULL, misaligned (256 B) or smaller than required */
+  RK_ERR_DEVICE_ORDER = 7    /* device-side check: a page_logical list is not ascending */
 } rk_status;
 
 /* Head classes ("小红书 RedKnot", section 3, first component). */
@@ -156,7 +157,11 @@ typedef struct rk_attn_args {
   int64_t n_pool_pages;
   const int32_t* page_table;   /* int32 [B*Hkv][max_pages] physical page of each listed entry */
   const int32_t* page_logical; /* int32 [B*Hkv][max_pages] strictly ascending logical page of each
-                                  entry, or NULL: entry e is logical page e */
+                                  entry, or NULL: entry e is logical page e.  The kernels find the
+                                  visible entries by searching these lists, so a list that is not
+                                  ascending gives an undefined visible set (reads stay inside the
+                                  pools); a list whose last entry is below its first is reported
+                                  as RK_ERR_DEVICE_ORDER, other violations go undetected */
   const int32_t* n_pages;      /* int32 [B*Hkv] listed entries, 0 <= n <= max_pages */
   const int32_t* head_class;   /* int32 [B*Hkv] RK_CLASS_* */
   const int32_t* window;       /* int32 [B*Hkv] local window W >= 1 (read for local heads) */
@@ -179,6 +184,13 @@ typedef struct rk_attn_args {
  * and before writing.  Without the flag nothing is read before the preceding work has
  * completed.  Ignored by prefill. */
 #define RK_ATTN_METADATA_STABLE 1
+
+/* Diagnostic, decode only: the first CTA of the decode kernel also waits for a word of the
+ * workspace header that nothing sets, so that its bounded wait (1 s) runs out.  The call
+ * then ends with RK_ERR_TIMEOUT in the status word, the way a wait that never completes
+ * would end it, without any fault; every role of the kernel leaves.  For testing that error
+ * path only.  Zero the workspace again before its next use. */
+#define RK_ATTN_DIAG_EXPIRE_WAIT (1 << 30)
 
 /* Bytes of workspace rk_segpaged_prefill / rk_segpaged_decode need for these sizes
  * (work list plus split-KV partial results).  Returns 0 for invalid sizes. */
@@ -216,12 +228,13 @@ RK_API rk_status rk_segpaged_decode(const rk_attn_args* args, void* workspace, s
  * rk_segpaged_decode_workspace_size exceeds it return RK_ERR_UNSUPPORTED and enqueue
  * nothing; use rk_segpaged_decode with a workspace for those.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress, once per device,
- * with that device current), so make that first call before any stream capture.  No call
+ * with that device current) and enqueues the zeroing of the array's split counters on
+ * `stream`, ahead of its decode; so make that first call before any stream capture.  No call
  * allocates memory.  Every call on a device shares the one array: calls that may overlap
  * on the GPU (different streams, or different host threads) race and must be serialised
- * by the caller; calls on one stream are ordered.  The array's split counters are zeroed
- * at that first call and every call leaves them at zero (after RK_ERR_TIMEOUT on the
- * device, the array cannot be reused: the process should start over). */
+ * by the caller; calls on one stream are ordered.  Every call leaves the split counters at
+ * zero (after RK_ERR_TIMEOUT on the device, the array cannot be reused: the process should
+ * start over). */
 #define RK_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 RK_API rk_status rk_segpaged_decode_noalloc(const rk_attn_args* args, rk_stream_t stream);
 

@@ -41,6 +41,7 @@ def test_status_strings(rk):
     assert rk.status_string(0) == "ok"
     assert "bounds" in rk.status_string(4)
     assert rk.status_string(99) == "unknown status"
+    assert "ascending" in rk.status_string(7)
 
 
 def _rope_args(rk, **kw):
@@ -113,6 +114,8 @@ def test_unknown_flag_bits_are_rejected(rk):
     assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 1
     d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_METADATA_STABLE)
     assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 6           # valid flag: workspace next
+    d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_DIAG_EXPIRE_WAIT)
+    assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 6           # the diagnostic bit is known
 
 
 def test_decode_workspace_holds_the_zeroed_counter_prefix(rk):

@@ -426,3 +426,81 @@ def test_stack_layer_full_size_sampled(rk):
         d = synth.decode_batch_from(dataclasses.replace(w, attn=a), step)
         out, lse = _gpu_attn(rk, d, decode=True)
         _compare(d, out, lse)
+
+
+# ------------------------------------------------------------------------- group sizes and pairings
+@pytest.mark.parametrize("Hq,Hkv", [(64, 4), (8, 8)], ids=["G16", "G1"])
+def test_prefill_group_sizes(rk, Hq, Hkv):
+    # G = 16 fills the decode MMA's N with no padding and gives 16-token prefill units;
+    # G = 1 (one query head per KV head) gives 256-token units
+    rng = np.random.default_rng(60 + Hkv)
+    cls = [[0, 1, 2, 1, 3, 1, 1, 0][h] for h in range(Hkv)]
+    w = synth._build("g", rng, B=2, Hq=Hq, Hkv=Hkv, d=128, P=16, theta=1e6, ctx_len=[700, 1900], n_suffix=[45, 300],
+                     classes=[cls] * 2, windows=[[100 if c == 1 else 0 for c in cls]] * 2, sinks=[[0] * Hkv] * 2,
+                     seg_tokens=[256, 512])
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
+    _compare(dataclasses.replace(w.attn, k_pool=oracle_pool), out, lse)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 4), (8, 8)], ids=["G16", "G1"])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_decode_group_sizes(rk, Hq, Hkv, flags):
+    w = synth.decode_microbench(B=6, ctx=3333, Hq=Hq, Hkv=Hkv, window=256, sink=4, seed=70 + Hkv)
+    out, lse = _gpu_attn(rk, w.attn, decode=True, flags=flags)
+    _compare(w.attn, out, lse)
+
+
+def test_rope_d128_interleaved(rk):
+    rng = np.random.default_rng(17)
+    w = synth._build("i", rng, B=2, Hq=8, Hkv=4, d=128, P=16, theta=1e6, ctx_len=[5000, 2100], n_suffix=[3, 7],
+                     classes=[[0, 1, 2, 3]] * 2, windows=[[0, 64, 0, 0]] * 2, sinks=[[0] * 4] * 2,
+                     seg_tokens=[1250, 700], style=1)
+    _check_rope(w, bf16_bits(_gpu_rope(rk, w)))
+
+
+# ------------------------------------------------------------------------- error paths on the device
+def test_decode_bounded_wait_runs_out_and_the_workspace_recovers(rk):
+    """RK_ATTN_DIAG_EXPIRE_WAIT makes the decode kernel's first CTA wait on a word nothing
+    sets: the bounded wait (1 s) runs out, the call reports RK_ERR_TIMEOUT and every role
+    of the kernel leaves -- no fault, no hang.  After the workspace is zeroed again, the
+    next call on the same workspace is correct and leaves its counters at zero."""
+    import time
+    w = synth.decode_microbench(B=4, ctx=20000, Hq=32, Hkv=8, window=256, sink=4, seed=81)
+    da = attn_to_device(w.attn, "cuda")
+    st = _status()
+    base = da.args(rk, decode=True, status=st)
+    ws = torch.zeros(rk.segpaged_decode_workspace_size(base), dtype=torch.uint8, device="cuda")
+    t0 = time.time()
+    rk.segpaged_decode(da.args(rk, decode=True, status=st, flags=rk.RK_ATTN_DIAG_EXPIRE_WAIT), workspace=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5                       # RK_ERR_TIMEOUT
+    assert time.time() - t0 < 20
+    ws.zero_()
+    st.zero_()
+    for flags in (0, rk.RK_ATTN_METADATA_STABLE):
+        da.out.fill_(float("nan"))
+        rk.segpaged_decode(da.args(rk, decode=True, status=st, flags=flags), workspace=ws)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        _compare(w.attn, da.out.float().cpu().numpy(), da.lse.cpu().numpy())
+        assert int(ws[256:28928].count_nonzero().item()) == 0
+
+
+def test_non_ascending_logical_list_is_reported(rk):
+    """A page list whose logical pages do not ascend (here: last entry below the span its
+    length needs) is reported as RK_ERR_DEVICE_ORDER by prefill and decode."""
+    w = synth.mixed_classes(B=2, lengths=(1024,), suffix_range=(60, 100), seg_tokens=512)
+    a = w.attn
+    lg = a.page_logical.copy()
+    n = int(a.n_pages[3])
+    lg[3, n - 1] = lg[3, 0]                          # duplicate of the first logical page
+    bad = dataclasses.replace(a, page_logical=lg)
+    for decode in (False, True):
+        b = _last_query_decode(bad) if decode else bad
+        da = attn_to_device(b, "cuda")
+        st = _status()
+        (rk.segpaged_decode if decode else rk.segpaged_prefill)(da.args(rk, decode=decode, status=st))
+        torch.cuda.synchronize()
+        assert int(st.item()) == 7                   # RK_ERR_DEVICE_ORDER
