@@ -4,12 +4,14 @@
 Workload (default): the 128K long-context layer stack -- 8 layers of 64 query / 8 KV
 heads, head dim 128, page 16; context of 131072 tokens made of 32 reusable segments of
 4096 tokens whose cached K is repositioned (RoPE) to its online offsets; a 1024-token
-suffix prefill per layer; then 64 decode steps over all 8 layers.  (layer, KV head)
-classes: exactly 3 of 64 global, the rest local with window 512.  All inputs are seeded
+suffix prefill per layer; then 64 decode steps over all 8 layers, each appending its
+token.  (layer, KV head) classes: exactly 3 of 64 global, the rest local with window 512,
+which store only their window and reuse a ring of pages during the decode.  All inputs are seeded
 synthetic bf16 N(0, 1) data (workloads/synth.py).
 
-One step = for every layer: rk_rope_reposition, rk_segpaged_prefill; then 64 x 8
-rk_segpaged_decode.  The step is captured once in a CUDA graph and replayed.
+One step = for every layer: rk_rope_reposition, rk_segpaged_prefill; then 64 decode steps,
+each: rk_ring_advance (all layers' page rings), then per layer rk_segpaged_decode, which
+also stores the layer's new token.  The step is captured once in a CUDA graph and replayed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -49,9 +51,11 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-queries", type=int, default=48)
+    ap.add_argument("--no-cases", action="store_true", help="skip the decode-microbenchmark and layer-prefill parts")
     ap.add_argument("--case", choices=["rag_prefill", "stack_prefill", "decode_microbench", "stack_decode", "rag_rope"],
                     help="run one call of one workload --steps times (for profiling) instead of the step")
+    ap.add_argument("--layer", type=int, default=None,
+                    help="with --case stack_*: the layer (default: the first layer holding a global head)")
     return ap.parse_args()
 
 
@@ -95,11 +99,13 @@ def load_peaks():
 def workload_config(args):
     return {
         "workload": "stack128k: %d layers x (64 q / 8 KV heads, d 128, page 16), context 131072 = 32 segments x 4096 "
-                    "repositioned, 1024-token suffix prefill, %d decode steps; 3 of 64 (layer, KV head) global, "
-                    "rest local window 512" % (args.layers, args.decode_steps),
+                    "repositioned, 1024-token suffix prefill, %d decode steps each appending its token; 3 of 64 "
+                    "(layer, KV head) global, rest local window 512 storing only their window (page ring of 33 "
+                    "pages in decode)" % (args.layers, args.decode_steps),
         "layers": args.layers, "context": 131072, "segments": 32, "segment_tokens": 4096, "suffix": 1024,
         "decode_steps": args.decode_steps, "Hq": 64, "Hkv": 8, "head_dim": 128, "page": 16, "theta": 1e6,
-        "l2": "inputs larger than L2 (about 0.8 GB of pools per layer, re-read every step)",
+        "l2": "inputs larger than L2: each replayed step reads about 0.47 GB of distinct K/V and offline K "
+              "(the decode windows, re-read every decode step, stay in L2 as in serving)",
         "parallelism": "replicas",
     }
 
@@ -207,6 +213,10 @@ def _blas_threads():
         return os.cpu_count()
 
 
+CPU_SAMPLE_QUERIES = 8      # query tokens of the oracle sample (x 8 KV heads)
+CPU_SAMPLE_ROPE = 1024      # RoPE tokens of the oracle sample
+
+
 def oracle_step(layer_wl, rows, n_rope_tok):
     """One bounded oracle pass: RoPE of one run prefix plus attention of the sampled rows."""
     from oracle import rk_oracle as O
@@ -219,28 +229,45 @@ def oracle_step(layer_wl, rows, n_rope_tok):
     return time.perf_counter() - t0
 
 
-def reference_main(args, world, rank):
-    if rank != 0:
-        return 0
+def cpu_sample(args):
+    """The oracle's bounded sample of the workload, the same for the CPU baseline and the
+    reference arm: a layer holding a global head, attention of CPU_SAMPLE_QUERIES spread
+    query tokens x every KV head (each with its 8 query heads) over their visible keys, plus
+    RoPE of CPU_SAMPLE_ROPE tokens of one run."""
     from workloads import synth
     classes = synth.stack_classes(n_layers=args.layers)
     layer = next((l for l, c in enumerate(classes) if 0 in c), 0)
     wl = synth.stack_layer(layer, n_layers=args.layers, n_decode=0)
-    rows = _oracle_sample(wl, max(4, args.cpu_sample_queries // 6), 17)
+    rows = _oracle_sample(wl, CPU_SAMPLE_QUERIES, 17)
     flops = _sample_flops(wl.attn, rows)
+    text = (f"layer {layer} (holds a global head): attention of {CPU_SAMPLE_QUERIES} query tokens x 8 KV heads "
+            f"(x 8 query heads each) over their visible keys, plus RoPE of {CPU_SAMPLE_ROPE} tokens of one run, "
+            f"per step; value = sample attention FLOPs / oracle time")
+    return wl, rows, flops, text
+
+
+def cpu_baseline(args, steps):
+    wl, rows, flops, text = cpu_sample(args)
+    secs = [oracle_step(wl, rows, CPU_SAMPLE_ROPE) for _ in range(steps)]
+    return {"value": flops * steps / sum(secs) / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": text + f"; {steps} steps, {sum(secs):.1f} s"}
+
+
+def reference_main(args, world, rank):
+    if rank != 0:
+        return 0
+    wl, rows, flops, text = cpu_sample(args)
     for _ in range(args.warmup):
-        oracle_step(wl, rows, 256)
-    times = [oracle_step(wl, rows, 256) for _ in range(args.steps)]
+        oracle_step(wl, rows, CPU_SAMPLE_ROPE)
+    times = [oracle_step(wl, rows, CPU_SAMPLE_ROPE) for _ in range(args.steps)]
     total = sum(times)
     value = flops * args.steps / total / 1e12
-    cores = _blas_threads()
-    sample = (f"layer {layer} (holds a global head): attention of {len(rows) // wl.attn.Hkv} query tokens x 8 KV heads "
-              f"(x 8 query heads each) over their visible keys, plus RoPE of 256 tokens of one run, per step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(args),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                             "sample": text},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -248,9 +275,11 @@ def reference_main(args, world, rank):
 
 # ----------------------------------------------------------------------------- our arm
 class LayerState:
-    """Device inputs, outputs and prebuilt C-ABI argument structs of one layer."""
+    """Device inputs, outputs and prebuilt C-ABI argument structs of one layer.  The decode
+    tables of all layers live in one stack (`dec`) so one rk_ring_advance call per decode
+    step advances every layer's page rings."""
 
-    def __init__(self, rk, wl, dev, n_dec, torch):
+    def __init__(self, rk, wl, dev, n_dec, torch, dec, layer):
         from workloads.device import attn_to_device, rope_to_device, to_device
         self.wl = wl
         a = wl.attn
@@ -268,45 +297,70 @@ class LayerState:
         self.prefill_args = self.attn.args(rk, status=self.status)
         self.prefill_ws = torch.empty(max(1, rk.segpaged_prefill_workspace_size(self.prefill_args)), dtype=torch.uint8,
                                       device=dev)
-        # decode: one query per step at position seq_len + s
+        # decode step s: append the token at position seq_len + s, then one query there
         self.n_dec = n_dec
-        self.dec_q = to_device(wl.decode_q[:n_dec].reshape(n_dec, a.Hq, a.d), dev) if n_dec else None
-        self.dec_seq = torch.tensor([[int(a.seq_len[0]) + s + 1] for s in range(n_dec)], dtype=torch.int32, device=dev)
+        self.dec_q = to_device(wl.decode_q[:n_dec].reshape(n_dec, a.Hq, a.d), dev)
+        self.dec_k = to_device(wl.decode_k[:n_dec], dev)           # [n_dec][1][Hkv][d]
+        self.dec_v = to_device(wl.decode_v[:n_dec], dev)
         self.dec_out = torch.empty((n_dec, a.Hq, a.d), dtype=torch.bfloat16, device=dev)
         self.dec_lse = torch.empty((n_dec, a.Hq), dtype=torch.float32, device=dev)
+        tab, lg, nn = dec.tab[layer], dec.lg[layer], dec.n[layer]
         self.dec_args = []
         for s in range(n_dec):
             da = self.attn
             self.dec_args.append(rk.AttnArgs(
-                q=self.dec_q[s].data_ptr(), cu_seqlens_q=None, seq_len=self.dec_seq[s].data_ptr(),
+                q=self.dec_q[s].data_ptr(), cu_seqlens_q=None, seq_len=dec.seq[s].data_ptr(),
                 k_pool=da.k_pool.data_ptr(), v_pool=da.v_pool.data_ptr(), n_pool_pages=da.k_pool.shape[0],
-                page_table=da.page_table.data_ptr(), page_logical=da.page_logical.data_ptr(),
-                n_pages=da.n_pages.data_ptr(), head_class=da.head_class.data_ptr(), window=da.window.data_ptr(),
-                sink=da.sink.data_ptr(), B=1, Hq=a.Hq, Hkv=a.Hkv, d=a.d, P=a.P, max_pages=da.page_table.shape[1],
-                total_q=1, max_q=1, scale=0.0, out=self.dec_out[s].data_ptr(), lse=self.dec_lse[s].data_ptr(),
-                status=self.status.data_ptr(), flags=rk.RK_ATTN_METADATA_STABLE))
-        self.dec_ws = torch.zeros(max(1, rk.segpaged_decode_workspace_size(self.dec_args[0])) if n_dec else 1,
-                                  dtype=torch.uint8, device=dev)
+                page_table=tab.data_ptr(), page_logical=lg.data_ptr(), n_pages=nn.data_ptr(),
+                head_class=da.head_class.data_ptr(), window=da.window.data_ptr(), sink=da.sink.data_ptr(), B=1,
+                Hq=a.Hq, Hkv=a.Hkv, d=a.d, P=a.P, max_pages=tab.shape[1], total_q=1, max_q=1, scale=0.0,
+                out=self.dec_out[s].data_ptr(), lse=self.dec_lse[s].data_ptr(), status=self.status.data_ptr(),
+                flags=rk.RK_ATTN_METADATA_STABLE, k_new=self.dec_k[s].data_ptr(), v_new=self.dec_v[s].data_ptr()))
+        self.dec_ws = torch.zeros(max(1, rk.segpaged_decode_workspace_size(self.dec_args[0])), dtype=torch.uint8,
+                                  device=dev)
 
-    # host copies for the end-to-end leg: (device tensor, pinned host tensor) pairs
-    def host_inputs(self, torch):
-        pairs = []
+    def host_inputs(self):
         d = self.attn
-        for t in (self.rope.k_src, self.rope.src_tables, self.rope.dst_tables, self.rope.runs, d.q, d.cu_seqlens_q,
-                  d.seq_len, d.k_pool, d.v_pool, d.page_table, d.page_logical, d.n_pages, d.head_class, d.window,
-                  d.sink, self.dec_q, self.dec_seq):
-            if t is None:
-                continue
-            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            h.copy_(t)
-            pairs.append((t, h))
-        return pairs
+        return [self.rope.k_src, self.rope.src_tables, self.rope.dst_tables, self.rope.runs, d.q, d.cu_seqlens_q,
+                d.seq_len, d.k_pool, d.v_pool, d.page_table, d.page_logical, d.n_pages, d.head_class, d.window,
+                d.sink, self.dec_q, self.dec_k, self.dec_v]
 
-    def host_outputs(self, torch):
-        pairs = []
-        for t in (self.attn.out, self.attn.lse, self.dec_out, self.dec_lse):
-            pairs.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
-        return pairs
+    def host_outputs(self):
+        return [self.attn.out, self.attn.lse, self.dec_out, self.dec_lse]
+
+
+class DecodeTables:
+    """The decode page tables of all layers, stacked as [layers][B*Hkv][max_pages] (layers
+    as extra sequences of one rk_ring_advance call), their starting state (restored at the
+    start of every replayed decode phase), the ring sizes, and per-step positions."""
+
+    def __init__(self, rk, wls, dev, n_dec, torch):
+        from workloads.device import to_device
+        L = len(wls)
+        a0 = wls[0].attn
+        nseg = a0.B * a0.Hkv
+        mp = max(int(w.dec_page_table.shape[1]) for w in wls)
+        tab = np.full((L, nseg, mp), -1, np.int32)
+        lg = np.full((L, nseg, mp), -1, np.int32)
+        for l, w in enumerate(wls):
+            tab[l, :, :w.dec_page_table.shape[1]] = w.dec_page_table
+            lg[l, :, :w.dec_page_logical.shape[1]] = w.dec_page_logical
+        self.tab0, self.lg0 = to_device(tab, dev), to_device(lg, dev)
+        self.tab, self.lg = self.tab0.clone(), self.lg0.clone()
+        self.n = to_device(np.stack([w.dec_n_pages for w in wls]), dev)
+        self.ring = to_device(np.concatenate([w.ring for w in wls]), dev)
+        self.window = to_device(np.concatenate([w.attn.window for w in wls]), dev)
+        self.sink = to_device(np.concatenate([w.attn.sink for w in wls]), dev)
+        base = int(a0.seq_len[0])
+        self.pos = torch.tensor([[base + s] * L for s in range(n_dec)], dtype=torch.int32, device=dev)
+        self.seq = torch.tensor([[base + s + 1] for s in range(n_dec)], dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ring_args = [rk.ring_args(self.pos[s], self.tab.view(L * nseg, mp), self.lg.view(L * nseg, mp),
+                                       self.n.view(-1), self.ring, self.window, self.sink, Hkv=a0.Hkv, P=a0.P,
+                                       status=self.status) for s in range(n_dec)]
+
+    def host_inputs(self):
+        return [self.tab0, self.lg0, self.n, self.ring, self.window, self.sink, self.pos, self.seq]
 
 
 def _call(fn, args_struct, ws, stream_handle):
@@ -315,7 +369,15 @@ def _call(fn, args_struct, ws, stream_handle):
         raise RuntimeError(f"librk call failed with status {code}")
 
 
-def enqueue(rk, layers, stream_handle, phase):
+def _call2(fn, args_struct, stream_handle):
+    code = fn(ctypes.byref(args_struct), ctypes.c_void_p(stream_handle))
+    if code != 0:
+        raise RuntimeError(f"librk call failed with status {code}")
+
+
+def enqueue(rk, layers, dec, stream_handle, phase):
+    """Enqueue one phase (or the whole step) through the C ABI; returns the number of our
+    kernels it launches."""
     n = 0
     if phase in ("step", "rope", "prefill"):
         for L in layers:
@@ -326,22 +388,25 @@ def enqueue(rk, layers, stream_handle, phase):
                 _call(rk.LIB.rk_segpaged_prefill, L.prefill_args, L.prefill_ws, stream_handle)
                 n += 3
     if phase in ("step", "decode"):
-        n_dec = layers[0].n_dec
-        for s in range(n_dec):
-            for L in layers:
+        dec.tab.copy_(dec.tab0)            # the rings start from the state after the prefill
+        dec.lg.copy_(dec.lg0)
+        for s in range(layers[0].n_dec):
+            _call2(rk.LIB.rk_ring_advance, dec.ring_args[s], stream_handle)
+            n += 1
+            for L in layers:   # each decode call first stores its layer's new token (k_new / v_new)
                 _call(rk.LIB.rk_segpaged_decode, L.dec_args[s], L.dec_ws, stream_handle)
                 # one kernel for up to 512 head segments (B * Hkv), else planner + attention + merge
                 n += 1 if L.dec_args[s].B * L.dec_args[s].Hkv <= 512 else 3
     return n
 
 
-def capture(torch, rk, layers, phase, stream):
+def capture(torch, rk, layers, dec, phase, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        enqueue(rk, layers, stream.cuda_stream, phase)           # eager warm-up (sets kernel attributes)
+        enqueue(rk, layers, dec, stream.cuda_stream, phase)      # eager warm-up (sets kernel attributes)
     torch.cuda.synchronize()
     with torch.cuda.graph(g, stream=stream):
-        n = enqueue(rk, layers, torch.cuda.current_stream().cuda_stream, phase)
+        n = enqueue(rk, layers, dec, torch.cuda.current_stream().cuda_stream, phase)
     torch.cuda.synchronize()
     return g, n
 
@@ -360,6 +425,108 @@ def time_graph(torch, g, stream, steps, warmup):
     return e0.elapsed_time(e1) / steps
 
 
+def masked_dense_inputs(torch, batch, dev):
+    """Dense K/V and explicit masks of a prefill launch, for the masked comparison path:
+    per KV head h, K[h] / V[h] hold keys 0..L-1 gathered from the head's pages (every head
+    must list every page below L), and mask[h][i][j] is True when key j is visible to
+    query i (causal, and for a local head inside its window or its sink).  This is the
+    form a dense attention kernel takes: the visible set as an attn_mask tensor.  Plumbing
+    only -- built once, outside any timed region."""
+    from workloads.device import to_device
+    assert batch.B == 1, "one sequence"
+    L, P, nq = int(batch.seq_len[0]), batch.P, batch.total_q
+    j = torch.arange(L, device=dev)
+    pos = (L - nq + torch.arange(nq, device=dev))[:, None]
+    kp, vp = to_device(batch.k_pool, dev), to_device(batch.v_pool, dev)
+    ks, vs, masks = [], [], []
+    for h in range(batch.Hkv):
+        lg = batch.page_logical[h, :int(batch.n_pages[h])]
+        assert np.array_equal(lg, np.arange(len(lg))) and len(lg) * P >= L, "full page lists"
+        pages = to_device(batch.page_table[h, :len(lg)].astype(np.int64), dev)
+        rows = pages[j // P] * P + j % P
+        ks.append(kp.view(-1, batch.d)[rows])
+        vs.append(vp.view(-1, batch.d)[rows])
+        m = j[None, :] <= pos
+        if int(batch.head_class[h]) == 1:
+            W, S = int(batch.window[h]), int(batch.sink[h])
+            m &= (j[None, :] > pos - W) | (j[None, :] < S)
+        masks.append(m)
+    q = to_device(batch.q, dev)                                     # [nq][Hq][d]
+    return q, ks, vs, masks
+
+
+def masked_dense_sdpa(torch, q, ks, vs, masks, G, causal_only=False):
+    """One prefill over dense K/V through torch's scaled_dot_product_attention, one call per
+    KV head (its G query heads): with the explicit boolean mask (the masked path), or with
+    is_causal and no mask (the unmasked fast path, every head treated as global)."""
+    F = torch.nn.functional
+    outs = []
+    for h in range(len(ks)):
+        qh = q[:, h * G:(h + 1) * G].transpose(0, 1)[None]           # [1][G][nq][d]
+        kh, vh = ks[h][None, None].expand(1, G, -1, -1), vs[h][None, None].expand(1, G, -1, -1)
+        if causal_only:   # queries at the end of the keys: the causal mask aligned to the lower right
+            from torch.nn.attention.bias import causal_lower_right
+            o = F.scaled_dot_product_attention(qh, kh, vh, attn_mask=causal_lower_right(qh.shape[2], kh.shape[2]))
+        else:
+            o = F.scaled_dot_product_attention(qh, kh, vh, attn_mask=masks[h][None, None])
+        outs.append(o[0].transpose(0, 1))
+    return torch.cat(outs, dim=1)                                     # [nq][Hq][d]
+
+
+def time_masked_comparison(torch, rk, dev, steps, warmup):
+    """The RAG prefill layer three ways: SegPagedAttention (our prefill over the page lists),
+    the masked path (dense K/V + an attn_mask tensor per head through torch's
+    scaled_dot_product_attention), and the unmasked fast path on the same dense K/V
+    (is_causal, no mask, every head dense) -- the comparison the pages make between their
+    mask-free kernel and a prefix cache that must pass a mask."""
+    from head_aware_paged_rope_b300 import roofline
+    from workloads import synth
+    from workloads.device import attn_to_device
+    wl = synth.rag_prefill()
+    a = wl.attn
+    G = a.Hq // a.Hkv
+    q, ks, vs, masks = masked_dense_inputs(torch, a, dev)
+    da = attn_to_device(a, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    args = da.args(rk, status=st)
+    ws = torch.empty(rk.segpaged_prefill_workspace_size(args), dtype=torch.uint8, device=dev)
+
+    def t(fn, n):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    ms_seg = t(lambda: rk.segpaged_prefill(args, workspace=ws), max(steps, 10))
+    ms_mask = t(lambda: masked_dense_sdpa(torch, q, ks, vs, masks, G), max(3, steps // 3))
+    ms_flash = t(lambda: masked_dense_sdpa(torch, q, ks, vs, masks, G, causal_only=True), max(3, steps // 3))
+    assert int(st.item()) == 0
+    flops = roofline.attention_flops(a)
+    return {"workload": "RAG layer (6 x 5000 context, 512-query suffix, 64 q / 8 KV heads, 1 global + 7 local W 256)",
+            "segpaged_ms": ms_seg, "masked_dense_ms": ms_mask, "unmasked_dense_causal_ms": ms_flash,
+            "masked_over_segpaged": ms_mask / ms_seg, "masked_over_unmasked": ms_mask / ms_flash,
+            "segpaged_TFLOP/s": flops / (ms_seg * 1e-3) / 1e12,
+            "masked_path": "torch scaled_dot_product_attention with a boolean attn_mask per KV head",
+            "unmasked_path": "torch scaled_dot_product_attention is_causal=True on the same dense K/V"}
+
+
+def time_cases(torch, rk, dev, steps, warmup):
+    """The decode microbenchmark (one call) and the isolated 128K layer prefill, each timed
+    like `--case` (calls captured in a graph, pools rotated past L2)."""
+    out = {}
+    for case in ("decode_microbench", "stack_prefill"):
+        calls, work, unit, label = build_case(torch, rk, dev, case, None)
+        ms = time_calls(torch, dev, calls, max(steps, 10), max(warmup, 3))
+        out[case] = {"ms": ms, unit: work / (ms * 1e-3), "workload": label, "pool_copies": len(calls)}
+    return out
+
+
 def ours_main(args, world, rank, local):
     import torch
     import head_aware_paged_rope_b300 as rk
@@ -374,33 +541,35 @@ def ours_main(args, world, rank, local):
     peaks, peaks_src = load_peaks()
 
     t_gen = time.time()
-    layers = []
+    wls = [synth.stack_layer(l, n_layers=args.layers, n_decode=args.decode_steps) for l in range(args.layers)]
     flops_prefill = flops_decode = 0
     bytes_rope = bytes_decode = 0
-    per_layer_prefill_flops = []
-    for l in range(args.layers):
-        wl = synth.stack_layer(l, n_layers=args.layers, n_decode=args.decode_steps)
-        fp = roofline.attention_flops(wl.attn)
-        per_layer_prefill_flops.append(fp)
-        flops_prefill += fp
+    for wl in wls:
+        flops_prefill += roofline.attention_flops(wl.attn)
         bytes_rope += roofline.rope_bytes(wl.rope)
+        a = wl.attn
         for s in range(args.decode_steps):
-            d = synth.decode_batch_from(wl, s)
+            n_tok = a.seq_len + s + 1
+            d = synth.dense_listing(dataclasses.replace(a, seq_len=n_tok.astype(np.int32),
+                                                        cu_seqlens_q=np.arange(a.B + 1, dtype=np.int32)), n_tok)
             flops_decode += roofline.attention_flops(d)
             bytes_decode += roofline.decode_kv_bytes(d)
-        layers.append(LayerState(rk, wl, dev, args.decode_steps, torch))
-        del wl
+    dec = DecodeTables(rk, wls, dev, args.decode_steps, torch)
+    layers = [LayerState(rk, wl, dev, args.decode_steps, torch, dec, l) for l, wl in enumerate(wls)]
+    del wls
     torch.cuda.synchronize()
     t_gen = time.time() - t_gen
 
     stream = torch.cuda.Stream(device=dev)
-    g_step, launches_per_step = capture(torch, rk, layers, "step", stream)
+    g_step, launches_per_step = capture(torch, rk, layers, dec, "step", stream)
     for L in layers:
         L.status.zero_()
+    dec.status.zero_()
     # correctness guard: the device status word of every call must stay clear
     g_step.replay()
     torch.cuda.synchronize()
-    bad = [int(L.status.item()) for L in layers if int(L.status.item()) != 0]
+    bad = [int(L.status.item()) for L in layers if int(L.status.item()) != 0] + \
+        ([int(dec.status.item())] if int(dec.status.item()) else [])
     if bad:
         raise RuntimeError(f"device status {bad}")
 
@@ -423,7 +592,7 @@ def ours_main(args, world, rank, local):
     # per-phase timing (each phase captured alone and replayed)
     parts = {}
     for phase in ("rope", "prefill", "decode"):
-        g, n = capture(torch, rk, layers, phase, stream)
+        g, n = capture(torch, rk, layers, dec, phase, stream)
         ms = time_graph(torch, g, stream, max(3, args.steps // 2), args.warmup)
         parts[phase] = {"ms": ms, "launches": n}
         del g
@@ -433,15 +602,25 @@ def ours_main(args, world, rank, local):
                              "calls": args.layers})
     parts["decode"].update({"GB/s": bytes_decode / (parts["decode"]["ms"] * 1e-3) / 1e9, "bytes": bytes_decode,
                             "TFLOP/s": flops_decode / (parts["decode"]["ms"] * 1e-3) / 1e12,
-                            "calls": args.layers * args.decode_steps})
+                            "calls": args.layers * args.decode_steps,
+                            "note": "per step: one rk_ring_advance for all layers, then per layer one "
+                                    "rk_segpaged_decode that also stores the layer's new token (k_new / v_new)"})
     parts["rope"]["frac_hbm"] = parts["rope"]["GB/s"] / peaks["hbm_gbs"]
     parts["decode"]["frac_hbm"] = parts["decode"]["GB/s"] / peaks["hbm_gbs"]
     parts["prefill"]["frac_bf16_burst"] = parts["prefill"]["TFLOP/s"] / peaks["bf16_tflops"]
     parts["prefill"]["frac_bf16_sustained"] = parts["prefill"]["TFLOP/s"] / peaks["bf16_tflops_sustained"]
+    if not args.no_cases:
+        parts["masked_comparison"] = time_masked_comparison(torch, rk, dev, args.steps, args.warmup)
+        for name, v in time_cases(torch, rk, dev, args.steps, args.warmup).items():
+            if "GB/s" in v:
+                v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+            else:
+                v["frac_bf16_burst"] = v["TFLOP/s"] / peaks["bf16_tflops"]
+            parts[name] = v
 
     dom = max(("rope", "prefill", "decode"), key=lambda k: parts[k]["ms"])
     if dom == "prefill":
-        roof = {"kernel": "rk_segpaged_prefill (plan + attention + combine)", "bound": "tensor",
+        roof = {"kernel": "prefill_tc_kernel (with its planner and combine)", "bound": "tensor",
                 "achieved": parts["prefill"]["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
         roof["traffic"] = None
     elif dom == "decode":
@@ -462,56 +641,61 @@ def ours_main(args, world, rank, local):
     step_flops = flops_prefill + flops_decode
     value = job_throughput(step_flops, world, ms_step) / 1e12
 
-    # end-to-end through the C ABI from pinned host buffers
-    e2e = None
+    # end to end from pinned host buffers: every input copied in and every output copied out
+    # each step; "e2e" enqueues the step through the C ABI call by call, "e2e_graph" replays
+    # the captured step between the copies
+    e2e = e2e_graph = None
     if not args.no_e2e:
         ins, outs = [], []
-        for L in layers:
-            ins += L.host_inputs(torch)
-            outs += L.host_outputs(torch)
+        for t in [x for L in layers for x in L.host_inputs()] + dec.host_inputs():
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            ins.append((t, h))
+        for t in [x for L in layers for x in L.host_outputs()]:
+            outs.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
         h2d = sum(h.numel() * h.element_size() for _, h in ins)
         d2h = sum(h.numel() * h.element_size() for _, h in outs)
 
-        def e2e_step():
+        def run_e2e(replay):
             with torch.cuda.stream(stream):
                 for dt, ht in ins:
                     dt.copy_(ht, non_blocking=True)
-            g_step.replay()
-            with torch.cuda.stream(stream):
+                if replay:
+                    g_step.replay()
+                else:
+                    enqueue(rk, layers, dec, stream.cuda_stream, "step")
                 for dt, ht in outs:
                     ht.copy_(dt, non_blocking=True)
 
-        e2e_step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms_e2e = max_over_ranks(torch, e0.elapsed_time(e1) / args.e2e_steps, dev, world)
-        e2e = {"value": job_throughput(step_flops, world, ms_e2e) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": args.e2e_steps}
+        res = {}
+        for replay in (False, True):
+            run_e2e(replay)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.e2e_steps):
+                run_e2e(replay)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = max_over_ranks(torch, e0.elapsed_time(e1) / args.e2e_steps, dev, world)
+            res[replay] = {"value": job_throughput(step_flops, world, ms) / 1e12, "unit": UNIT,
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+                           "steps": args.e2e_steps}
+        e2e, e2e_graph = res[False], res[True]
+        e2e["how"] = "every rk_* call of the step enqueued through the C ABI (ctypes) between the copies"
+        e2e_graph["how"] = "the captured step replayed between the copies"
         del ins, outs
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        classes = synth.stack_classes(n_layers=args.layers)
-        layer = next((l for l, c in enumerate(classes) if 0 in c), 0)
-        wl = synth.stack_layer(layer, n_layers=args.layers, n_decode=0)
-        rows = _oracle_sample(wl, args.cpu_sample_queries, 17)
-        fl = _sample_flops(wl.attn, rows)
-        secs = oracle_step(wl, rows, 4096)
-        cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-               "sample": f"layer {layer} (holds a global head): attention of {len(rows) // wl.attn.Hkv} query tokens "
-                         f"x 8 KV heads (x 8 query heads each) + RoPE of one 4096-token run; {secs:.1f} s"}
+        cpu = cpu_baseline(args, steps=2)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1) K/V/q, seeded page "
                 "permutations and head classes; no dataset)", "config": workload_config(args),
-                "parts": parts, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "parts": parts, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "e2e_graph": e2e_graph,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "setup_s": round(t_gen, 1)}
         print(json.dumps(line), flush=True)
@@ -520,86 +704,104 @@ def ours_main(args, world, rank, local):
     return 0
 
 
-def case_main(args):
-    """One library call of one workload, repeated: a small, self-contained target for ncu.
-
-    The calls are captured once in a CUDA graph (args.steps calls, replayed args.steps
-    times after args.warmup replays) so host launch overhead is not measured.  Attention
-    calls cycle through enough copies of the K/V pools that the visible bytes of
-    consecutive calls exceed three times the L2, so they are not served from L2.  Prints
-    the average time per call measured with CUDA events on the replay stream."""
-    import torch
-    import head_aware_paged_rope_b300 as rk
+def build_case(torch, rk, dev, case, layer):
+    """Calls (closures, each one library call) of one workload, cycling through enough
+    copies of the K/V pools that the visible bytes of consecutive calls exceed three times
+    the L2, so they are not served from L2; and the work of one call."""
     from head_aware_paged_rope_b300 import roofline
     from workloads import synth
     from workloads.device import attn_to_device, rope_to_device, to_device
-    dev = torch.device("cuda", 0)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    if args.case == "rag_prefill":
-        wl = synth.rag_prefill()
-    elif args.case == "stack_prefill":
-        classes = synth.stack_classes()
-        wl = synth.stack_layer(next(l for l, c in enumerate(classes) if 0 in c), n_decode=0)
-    elif args.case == "decode_microbench":
-        wl = synth.decode_microbench()
-    elif args.case == "stack_decode":
-        classes = synth.stack_classes()
-        layer_wl = synth.stack_layer(next(l for l, c in enumerate(classes) if 0 in c), n_decode=1)
-        wl = dataclasses.replace(layer_wl, attn=synth.decode_batch_from(layer_wl, 0))
+    classes = synth.stack_classes()
+    glob_layer = next(l for l, c in enumerate(classes) if 0 in c)
+    if case == "rag_prefill" or case == "rag_rope":
+        wl, label = synth.rag_prefill(), "RAG layer (6 x 5000 context, 512-query suffix, 64 q / 8 KV heads)"
+    elif case == "stack_prefill":
+        layer = glob_layer if layer is None else layer
+        wl = synth.stack_layer(layer, n_decode=0)
+        label = f"128K stack layer {layer} prefill (1024 queries over 131072 + 1024 keys)"
+    elif case == "decode_microbench":
+        wl, label = synth.decode_microbench(), "decode microbenchmark (32 x 8192, 32 q / 8 KV heads, page 16)"
+    elif case == "stack_decode":
+        layer = glob_layer if layer is None else layer
+        w = synth.stack_layer(layer, n_decode=1)
+        a = w.attn
+        wl = dataclasses.replace(w, attn=dataclasses.replace(
+            a, q=np.ascontiguousarray(w.decode_q[0]), cu_seqlens_q=np.arange(a.B + 1, dtype=np.int32),
+            seq_len=(a.seq_len + 1).astype(np.int32), page_table=w.dec_page_table, page_logical=w.dec_page_logical,
+            n_pages=w.dec_n_pages))
+        label = f"128K stack layer {layer}, first decode step"
     else:
-        wl = synth.rag_prefill()
+        raise ValueError(case)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     calls = []
-    if args.case == "rag_rope":
+    if case == "rag_rope":
         dr = rope_to_device(wl.rope, dev)
         kp = to_device(wl.attn.k_pool, dev)
         ws = torch.empty(rk.rope_workspace_size(wl.rope.n_runs, wl.attn.d), dtype=torch.uint8, device=dev)
         calls.append(lambda: dr.run(rk, kp, status=st, workspace=ws))
-        work, unit = roofline.rope_bytes(wl.rope) / 1e9, "GB/s"
-        touched = 2 * wl.rope.k_src.nbytes
+        return calls, roofline.rope_bytes(wl.rope) / 1e9, "GB/s", label + ", RoPE"
+    decode = case in ("decode_microbench", "stack_decode")
+    da = attn_to_device(wl.attn, dev)
+    base = da.args(rk, decode=decode, status=st, flags=rk.RK_ATTN_METADATA_STABLE if decode else 0)
+    n = (rk.segpaged_decode_workspace_size if decode else rk.segpaged_prefill_workspace_size)(base)
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    fn = rk.segpaged_decode if decode else rk.segpaged_prefill
+    if decode:
+        work, unit = roofline.decode_kv_bytes(wl.attn) / 1e9, "GB/s"
     else:
-        decode = args.case in ("decode_microbench", "stack_decode")
-        da = attn_to_device(wl.attn, dev)
-        base = da.args(rk, decode=decode, status=st, flags=rk.RK_ATTN_METADATA_STABLE if decode else 0)
-        n = (rk.segpaged_decode_workspace_size if decode else rk.segpaged_prefill_workspace_size)(base)
-        ws = torch.zeros(n, dtype=torch.uint8, device=dev)
-        fn = rk.segpaged_decode if decode else rk.segpaged_prefill
-        if decode:
-            work, unit = roofline.decode_kv_bytes(wl.attn) / 1e9, "GB/s"
-        else:
-            work, unit = roofline.attention_flops(wl.attn) / 1e12, "TFLOP/s"
-        touched = max(1, roofline.decode_kv_bytes(wl.attn))
-        copies = max(1, min(8, -(-3 * l2 // touched)))
-        keep = []
-        for c in range(copies):
-            a = rk.AttnArgs.from_buffer_copy(base)
-            if c:
-                kc, vc = da.k_pool.clone(), da.v_pool.clone()
-                keep += [kc, vc]
-                a.k_pool, a.v_pool = kc.data_ptr(), vc.data_ptr()
-            calls.append(lambda a=a: fn(a, workspace=ws))
-    for i in range(args.warmup):
+        work, unit = roofline.attention_flops(wl.attn) / 1e12, "TFLOP/s"
+    touched = max(1, roofline.decode_kv_bytes(wl.attn))
+    copies = max(1, min(8, -(-3 * l2 // touched)))
+    keep = [da]
+    for c in range(copies):
+        a = rk.AttnArgs.from_buffer_copy(base)
+        if c:
+            kc, vc = da.k_pool.clone(), da.v_pool.clone()
+            keep += [kc, vc]
+            a.k_pool, a.v_pool = kc.data_ptr(), vc.data_ptr()
+        calls.append(lambda a=a, keep=keep: fn(a, workspace=ws))
+    calls.append(st)      # the status word, checked after timing
+    return calls, work, unit, label
+
+
+def time_calls(torch, dev, calls, steps, warmup):
+    """Average time of one call: `steps` calls captured in a CUDA graph, replayed `steps`
+    times after `warmup` replays, CUDA events on the replay stream."""
+    st = calls[-1]
+    calls = calls[:-1] if isinstance(st, torch.Tensor) else calls
+    for i in range(warmup):
         calls[i % len(calls)]()
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=dev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for i in range(args.steps):
+        for i in range(steps):
             calls[i % len(calls)]()
-    for _ in range(max(1, args.warmup)):
+    for _ in range(max(1, warmup)):
         g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             g.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (args.steps * args.steps)
-    assert int(st.item()) == 0, f"device status {int(st.item())}"
-    print(json.dumps({"case": args.case, "ms_per_call": ms, unit: work / (ms * 1e-3), "pool_copies": len(calls)}),
-          flush=True)
+    if isinstance(st, torch.Tensor):
+        assert int(st.item()) == 0, f"device status {int(st.item())}"
+    return e0.elapsed_time(e1) / (steps * steps)
+
+
+def case_main(args):
+    """One library call of one workload, repeated: a small, self-contained target for ncu."""
+    import torch
+    import head_aware_paged_rope_b300 as rk
+    dev = torch.device("cuda", 0)
+    calls, work, unit, label = build_case(torch, rk, dev, args.case, args.layer)
+    ms = time_calls(torch, dev, calls, args.steps, args.warmup)
+    print(json.dumps({"case": args.case, "workload": label, "ms_per_call": ms, unit: work / (ms * 1e-3),
+                      "pool_copies": len(calls) - 1}), flush=True)
     return 0
 
 

@@ -55,7 +55,26 @@ class AttnArgs(ctypes.Structure):
         ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32),
         ("P", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q", ctypes.c_int32),
         ("scale", ctypes.c_float), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("status", ctypes.c_void_p),
-        ("flags", ctypes.c_int32),
+        ("flags", ctypes.c_int32), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+    ]
+
+
+class AppendArgs(ctypes.Structure):
+    _fields_ = [
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+        ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("n_pool_pages", ctypes.c_int64),
+        ("page_table", ctypes.c_void_p), ("page_logical", ctypes.c_void_p), ("n_pages", ctypes.c_void_p),
+        ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("P", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32), ("status", ctypes.c_void_p),
+    ]
+
+
+class RingArgs(ctypes.Structure):
+    _fields_ = [
+        ("pos", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("page_logical", ctypes.c_void_p),
+        ("n_pages", ctypes.c_void_p), ("ring", ctypes.c_void_p), ("window", ctypes.c_void_p),
+        ("sink", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("P", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32), ("status", ctypes.c_void_p),
     ]
 
 
@@ -75,6 +94,10 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.rk_append_kv.restype = ctypes.c_int
+    lib.rk_append_kv.argtypes = [ctypes.POINTER(AppendArgs), ctypes.c_void_p]
+    lib.rk_ring_advance.restype = ctypes.c_int
+    lib.rk_ring_advance.argtypes = [ctypes.POINTER(RingArgs), ctypes.c_void_p]
     lib.rk_status_string.restype = ctypes.c_char_p
     lib.rk_status_string.argtypes = [ctypes.c_int]
     lib.rk_version.restype = ctypes.c_int32
@@ -139,7 +162,7 @@ def rope_reposition(k_src: torch.Tensor, k_dst: torch.Tensor, src_tables: torch.
 
 def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, head_class, window, sink, out,
               *, cu_seqlens_q=None, lse=None, status=None, total_q: int, max_q: int, scale: float = 0.0,
-              flags: int = 0) -> AttnArgs:
+              flags: int = 0, k_new=None, v_new=None) -> AttnArgs:
     B = seq_len.shape[0]
     Hq, d = q.shape[1], q.shape[2]
     Hkv = n_pages.shape[0] // max(B, 1)
@@ -148,7 +171,8 @@ def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, hea
                     page_logical=_ptr(page_logical), n_pages=_ptr(n_pages), head_class=_ptr(head_class),
                     window=_ptr(window), sink=_ptr(sink), B=B, Hq=Hq, Hkv=Hkv, d=d, P=k_pool.shape[1],
                     max_pages=page_table.shape[1], total_q=int(total_q), max_q=int(max_q), scale=float(scale),
-                    out=_ptr(out), lse=_ptr(lse), status=_ptr(status), flags=int(flags))
+                    out=_ptr(out), lse=_ptr(lse), status=_ptr(status), flags=int(flags), k_new=_ptr(k_new),
+                    v_new=_ptr(v_new))
 
 
 def segpaged_prefill_workspace_size(args: AttnArgs) -> int:
@@ -173,6 +197,32 @@ def segpaged_decode(args: AttnArgs, *, device=None, workspace: Optional[torch.Te
     ws = _workspace(n, device or torch.device("cuda"), workspace, zeroed=True)
     _check(LIB.rk_segpaged_decode(ctypes.byref(args), _ptr(ws), ws.numel() if ws is not None else 0,
                                   _stream(stream)), "rk_segpaged_decode")
+
+
+def append_args(k_new, v_new, pos, k_pool, v_pool, page_table, page_logical, n_pages, *, status=None) -> AppendArgs:
+    """k_new/v_new: bf16 [B][Hkv][d]; pos: int32 [B]; tables as for attention."""
+    B, Hkv, d = k_new.shape
+    return AppendArgs(k_new=_ptr(k_new), v_new=_ptr(v_new), pos=_ptr(pos), k_pool=_ptr(k_pool), v_pool=_ptr(v_pool),
+                      n_pool_pages=k_pool.shape[0], page_table=_ptr(page_table), page_logical=_ptr(page_logical),
+                      n_pages=_ptr(n_pages), B=B, Hkv=Hkv, d=d, P=k_pool.shape[1], max_pages=page_table.shape[1],
+                      status=_ptr(status))
+
+
+def append_kv(args: AppendArgs, stream=None) -> None:
+    _check(LIB.rk_append_kv(ctypes.byref(args), _stream(stream)), "rk_append_kv")
+
+
+def ring_args(pos, page_table, page_logical, n_pages, ring, window, sink, *, Hkv: int, P: int,
+              status=None) -> RingArgs:
+    """Tables [B*Hkv][max_pages] (several layers may be stacked as extra sequences); pos: int32 [B]."""
+    B = pos.shape[0]
+    return RingArgs(pos=_ptr(pos), page_table=_ptr(page_table), page_logical=_ptr(page_logical),
+                    n_pages=_ptr(n_pages), ring=_ptr(ring), window=_ptr(window), sink=_ptr(sink), B=B, Hkv=Hkv,
+                    P=P, max_pages=page_table.shape[1], status=_ptr(status))
+
+
+def ring_advance(args: RingArgs, stream=None) -> None:
+    _check(LIB.rk_ring_advance(ctypes.byref(args), _stream(stream)), "rk_ring_advance")
 
 
 def version() -> int:

@@ -61,13 +61,14 @@ rk_status check_attn(const rk_attn_args* a, bool decode) {
     return RK_ERR_UNSUPPORTED;   // row coordinates of the tensor maps are int32
   if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
   if (a->flags & ~(RK_ATTN_METADATA_STABLE | RK_ATTN_DIAG_EXPIRE_WAIT)) return RK_ERR_INVALID_ARG;
+  if ((a->k_new != nullptr) != (a->v_new != nullptr) || (!decode && a->k_new)) return RK_ERR_INVALID_ARG;
   return RK_OK;
 }
 
 // q, the pools and out are read and written with 16-byte vectors and TMA.
 bool aligned16(const rk_attn_args* a) {
   const auto ok = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
-  return ok(a->q) && ok(a->k_pool) && ok(a->v_pool) && ok(a->out);
+  return ok(a->q) && ok(a->k_pool) && ok(a->v_pool) && ok(a->out) && ok(a->k_new) && ok(a->v_new);
 }
 
 AttnLayout attn_layout(const rk_attn_args* a) {
@@ -117,6 +118,8 @@ AttnParams make_params(const rk_attn_args* a, const AttnLayout& l) {
   p.lse = a->lse;
   p.status = a->status;
   p.flags = a->flags;
+  p.k_new = static_cast<const __nv_bfloat16*>(a->k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(a->v_new);
   return p;
 }
 
@@ -278,6 +281,30 @@ rk_status rk_segpaged_prefill(const rk_attn_args* a, void* ws, size_t bytes, rk_
 
 rk_status rk_segpaged_decode(const rk_attn_args* a, void* ws, size_t bytes, rk_stream_t stream) {
   return rk::run_attention(a, ws, bytes, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+rk_status rk_append_kv(const rk_append_args* a, rk_stream_t stream) {
+  if (!a) return RK_ERR_INVALID_ARG;
+  if (a->B < 0 || a->Hkv < 0 || a->max_pages < 0 || a->n_pool_pages < 0) return RK_ERR_INVALID_ARG;
+  if (!rk::supported_dp(a->d, a->P)) return RK_ERR_UNSUPPORTED;
+  if (a->B == 0 || a->Hkv == 0) return RK_OK;
+  if (!a->k_new || !a->v_new || !a->pos || !a->k_pool || !a->v_pool || !a->page_table || !a->n_pages)
+    return RK_ERR_INVALID_ARG;
+  const auto al16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  if (!al16(a->k_new) || !al16(a->v_new) || !al16(a->k_pool) || !al16(a->v_pool)) return RK_ERR_INVALID_ARG;
+  if (int64_t(a->B) * a->Hkv >= (int64_t(1) << 31) / 32) return RK_ERR_UNSUPPORTED;
+  return rk::launch_append_kv(*a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+}
+
+rk_status rk_ring_advance(const rk_ring_args* a, rk_stream_t stream) {
+  if (!a) return RK_ERR_INVALID_ARG;
+  if (a->B < 0 || a->Hkv < 0 || a->max_pages < 0) return RK_ERR_INVALID_ARG;
+  if (a->P != 16 && a->P != 32) return RK_ERR_UNSUPPORTED;
+  if (a->B == 0 || a->Hkv == 0) return RK_OK;
+  if (!a->pos || !a->page_table || !a->page_logical || !a->n_pages || !a->ring || !a->window)
+    return RK_ERR_INVALID_ARG;
+  if (int64_t(a->B) * a->Hkv >= (int64_t(1) << 31) / 32) return RK_ERR_UNSUPPORTED;
+  return rk::launch_ring_advance(*a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }
 
 const char* rk_status_string(rk_status s) {

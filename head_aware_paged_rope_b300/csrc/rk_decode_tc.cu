@@ -12,9 +12,12 @@
 //   O^T[c][g]   += V^T[c][key] . P^T[key][g]     M = 128 channels, N = 16, K = 128 keys
 //
 // Schedule: the 128-key tiles of all head segments form one sequence of T tiles and CTA c
-// takes the equal share [c*T/gs, (c+1)*T/gs) of it (gs = the smaller of the grid, one CTA
-// per SM, and T); when no segment has more than kAlignTiles tiles and there are no more
-// segments than CTAs, CTA c takes segment c whole instead.  Up to kDecFusedSegs head
+// takes the share [cut(c), cut(c+1)) of it, cut(c) = c*T/gs (gs = the smaller of the grid,
+// one CTA per SM, and T); when no segment has more than kAlignTiles tiles and there are no
+// more segments than CTAs, CTA c takes segment c whole instead.  On the single-launch path
+// a cut that falls inside a segment of at most kShortTiles tiles moves to the nearer end
+// of that segment, so short segments (the windows of local heads) are never split and need
+// no merge; only long segments are shared by several CTAs.  Up to kDecFusedSegs head
 // segments every CTA plans this itself (visible ranges in three interleaved rounds of
 // loads, a block scan of the tile counts) and a segment shared by several CTAs is merged
 // inside the kernel; beyond that, plan_decode_kernel (rk_plan.cu) plans and
@@ -46,7 +49,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;           // warps 0-3 softmax, 4 controller, 5 MMA, 6-9 copy
+constexpr int kCopyWarp0 = 6;
 constexpr int kKeys = kDecTileKeys;     // keys per tile (MMA M of S^T)
 constexpr int kN = 16;                  // MMA N: query heads of the group, padded
 constexpr int kRing = 2;                // portion ring depth
@@ -76,7 +80,8 @@ struct Portion {
   int32_t seg, v_begin, v_end, slot;    // slot < 0: write the output directly
   int32_t n_kt, b, tok, pos;
   int32_t cls, W, S, L;
-  int32_t n_splits, cta0, tile0, pad;   // CTAs sharing the segment, the first of them, its first tile
+  int32_t n_splits, cta0, tile0;        // CTAs sharing the segment, the first of them, its first tile
+  int32_t c0_later;                     // the segment is not the first portion of cta0's share
 };
 
 struct DecShared {
@@ -86,7 +91,10 @@ struct DecShared {
   uint64_t q_full[2], q_empty[2];
   uint64_t iq_full[kRing], iq_empty[kRing];
   Portion ring[kRing];
+  uint64_t desc_full[6];    // controller -> copy warps: a stage's page ids are published
   int lp[6][8];             // logical page of each page slot of a stage (-1: none)
+  int pid[6][8];            // physical page of each page slot of a stage (-1: none, zeros are copied)
+  int cmd[6];               // per stage: 0 stop, 1 copy
   float red[2][4][kN];      // per-warp tile maxima (double-buffered by tile parity)
   float redl[4][kN];        // per-warp denominators
   float lse2[kN];
@@ -123,6 +131,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ int seg_entry(const DecSeg& s, int v) { return v < s.e_sink ? v : s.e_w + (v - s.e_sink); }
+
+// 16-byte global -> shared copy (L2 only); src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on the mbarrier once this thread's earlier cp.async copies have landed (counts as
+// one of its expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" :: "r"(addr), "h"(v) : "memory");
@@ -162,14 +181,34 @@ __device__ __forceinline__ float warp_reduce_cols(float (&v)[NG]) {
 }
 
 constexpr int kMergeFan = 12;   // partials one CTA merges at a time (single-launch path)
-constexpr int kStreamTiles = 32;  // segments of at least 4096 keys are streamed past L2 (evict-first)
 constexpr int kAlignTiles = 2;  // segments this short are never split when there are enough CTAs
+constexpr int kShortTiles = 8;  // single-launch path: segments this short are never split
 
 // Partial slot of CTA c for a split segment (two per CTA: its first and its last portion):
 // c's portion of the segment is its first one unless c = cta0 and c's share began in an
-// earlier segment.
-__device__ __forceinline__ int split_slot(int c, int cta0, int tile0, long long T, long long gs) {
-  return (c == cta0 && (long long)c * T / gs < tile0) ? 2 * c + 1 : 2 * c;
+// earlier segment (c0_later).
+__device__ __forceinline__ int split_slot(int c, int cta0, int c0_later) {
+  return (c == cta0 && c0_later) ? 2 * c + 1 : 2 * c;
+}
+
+// First tile of CTA c's share on the single-launch path: c*T/gs, moved to the nearer end
+// of the segment it falls in when that segment has at most kShortTiles tiles (ties go to
+// its start).  Monotone in c, so the shares stay disjoint and cover [0, T).  A tile of a
+// longer segment belongs to the same CTA as without the move: cuts inside it are not
+// moved, and cuts moved within other segments stay on their side of it.  plan[s].w is
+// the first tile of segment s, plan[s].z its visible entries.
+__device__ __forceinline__ int share_cut(int c, long long T, long long gs, const int4* plan, int nseg, int ept) {
+  if (c <= 0) return 0;
+  if (c >= gs) return int(T);
+  const int raw = int((long long)c * T / gs);
+  int lo = 0, hi = nseg - 1;   // last segment whose first tile is <= raw
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (plan[mid].w <= raw) lo = mid; else hi = mid - 1;
+  }
+  const int t0 = plan[lo].w, nt = (plan[lo].z + ept - 1) / ept;
+  if (raw <= t0 || raw >= t0 + nt || nt > kShortTiles) return raw;
+  return raw - t0 <= t0 + nt - raw ? t0 : t0 + nt;
 }
 
 // Merge protocol of a split segment (single-launch path).  Each CTA holding a piece takes a
@@ -204,8 +243,8 @@ __device__ __forceinline__ bool wait_flag(int32_t* f) {
 // log) or into one partial slot.  The 128 softmax threads each take (head, 4 channels)
 // columns, two at a time, eight partials' loads in flight.
 template <int D>
-__device__ __forceinline__ void merge_splits(int n, int c_first, int stride, int cta0, int tile0, long long T,
-                                             long long gs, const float* src_lse, const float* src_o, int G,
+__device__ __forceinline__ void merge_splits(int n, int c_first, int stride, int cta0, int c0_later,
+                                             const float* src_lse, const float* src_o, int G,
                                              __nv_bfloat16* out_row, float* lse_row, float* dst_lse, float* dst_o,
                                              int t) {
   constexpr int C4 = D / 4;
@@ -219,7 +258,7 @@ __device__ __forceinline__ void merge_splits(int n, int c_first, int stride, int
       float4 ov[2][8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int slot = k0 + k < n ? split_slot(c_first + (k0 + k) * stride, cta0, tile0, T, gs) : -1;
+        const int slot = k0 + k < n ? split_slot(c_first + (k0 + k) * stride, cta0, c0_later) : -1;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           lv[x][k] = -INFINITY;
@@ -273,15 +312,12 @@ __device__ __forceinline__ void merge_splits(int n, int c_first, int stride, int
 
 template <int D, int NG, bool FUSED>
 __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                                 const __grid_constant__ CUtensorMap tmK,
-                                                                 const __grid_constant__ CUtensorMap tmV,
                                                                  AttnParams p, DecWorkspace ws) {
   using LY = DecLayout<D>;
   constexpr int NS = LY::kStages;
   constexpr int HALVES = D / 64;
   constexpr uint32_t kIdescQK = idesc_bf16(kKeys, kN, 0, 0);
   constexpr uint32_t kIdescPV = idesc_bf16(128, kN, 0, 1);
-  constexpr uint32_t kTileTx = 2 * HALVES * kKeys * 128;   // K + V bytes of one tile
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -294,8 +330,9 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_addr(&sh.kv_full[s]), 1);
+      mbar_init(smem_addr(&sh.kv_full[s]), 128);   // one arrival per copy thread, when its copies land
       mbar_init(smem_addr(&sh.kv_empty[s]), 1);
+      mbar_init(smem_addr(&sh.desc_full[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&sh.s_full[s]), 1);
@@ -316,8 +353,6 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
   }
   if (warp == 4 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(&tmQ) : "memory");
-    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmK) : "memory");
-    asm volatile("prefetch.tensormap [%0];" :: "l"(&tmV) : "memory");
   }
   if (warp == 5) {
     tmem_alloc(smem_addr(&sh.tmem_slot), kTmemCols);
@@ -375,33 +410,40 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const bool aligned = sh.max_nt <= kAlignTiles && nseg <= int(gridDim.x);
     const int gs = min(int(gridDim.x), T);
     const int c = blockIdx.x;
-    const int tb = c < gs ? int((long long)c * T / gs) : T;
+    {
+      int t1 = t0;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int seg = s0 + i;
-      if (i < per && seg < nseg) {
-        plan[seg] = make_int4(rr[i].e_sink, rr[i].e_w, rr[i].n_vis, t0);
-        if (aligned) {
-          if (seg == c) {
-            sh.tb = nt[i] > 0 ? t0 : T;
-            sh.te = nt[i] > 0 ? t0 + nt[i] : T;
+      for (int i = 0; i < kPer; ++i) {
+        const int seg = s0 + i;
+        if (i < per && seg < nseg) {
+          plan[seg] = make_int4(rr[i].e_sink, rr[i].e_w, rr[i].n_vis, t1);
+          if (aligned && seg == c) {
+            sh.tb = nt[i] > 0 ? t1 : T;
+            sh.te = nt[i] > 0 ? t1 + nt[i] : T;
             sh.seg_first = seg;
           }
-        } else if (nt[i] > 0 && t0 <= tb && tb < t0 + nt[i]) {
-          sh.seg_first = seg;
+          t1 += nt[i];
         }
-        t0 += nt[i];
       }
     }
     if (tid == 0) {
       sh.T = T;
       sh.gs = gs;
       sh.aligned = aligned;
-      if (!aligned) {
-        sh.tb = tb;
-        sh.te = c < gs ? int((long long)(c + 1) * T / gs) : T;
-      } else if (c >= nseg) {
-        sh.tb = sh.te = T;
+      if (aligned && c >= nseg) sh.tb = sh.te = T;
+    }
+    __syncthreads();
+    if (!aligned) {
+      if (tid == 0) {
+        sh.tb = share_cut(c, T, gs, plan, nseg, EPT);
+        sh.te = share_cut(c + 1, T, gs, plan, nseg, EPT);
+      }
+      __syncthreads();
+      const int tb = sh.tb;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        if (i < per && s0 + i < nseg && nt[i] > 0 && t0 <= tb && tb < t0 + nt[i]) sh.seg_first = s0 + i;
+        t0 += nt[i];
       }
     }
     __syncthreads();
@@ -409,8 +451,6 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
 
   if (warp == 4) {
     // ------------------------------------------------------------------ producer
-    const int64_t oob_row = p.n_pool_pages * P;      // a row past the pool: TMA fills zeros
-    const uint64_t evict_first = l2_policy_evict_first();
     DecCta my;
     if constexpr (FUSED) {
       my.seg0 = sh.seg_first;
@@ -452,13 +492,15 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           const bool local = d.cls == RK_CLASS_LOCAL;
           d.W = local ? __ldg(p.window + s) : 0;
           d.S = local && p.sink ? __ldg(p.sink + s) : 0;
+          // only segments longer than kShortTiles are shared; the CTAs holding their tiles are
+          // the ones c*T/gs gives (cuts inside them are not moved)
           const long long T = sh.T, gs = sh.gs;
-          const bool cut = d.n_tiles > 0 && !sh.aligned;
+          const bool cut = d.n_tiles > kShortTiles && !sh.aligned;
           const int c0 = cut ? int((((long long)d.tile0 + 1) * gs + T - 1) / T) - 1 : s;
           const int c1 = cut ? int((((long long)d.tile0 + d.n_tiles) * gs + T - 1) / T) - 1 : s;
           d.cta0 = c0;
           d.n_splits = c1 - c0 + 1;
-          d.slot0 = -1;
+          d.slot0 = (cut && c1 > c0) ? int(share_cut(c0, T, gs, s_plan, nseg, EPT) < d.tile0) : 0;   // c0_later
         } else {
           d = ws.segs[s];
         }
@@ -472,8 +514,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       return d;
     };
     uint32_t gg = 0, qn = 0;
-    int last_stage = -1, last_q = -1;
-    uint32_t last_parity = 0, last_q_parity = 0;
+    int last_q = -1;
+    uint32_t last_q_parity = 0;
     bool ok = true;
     DecSeg cur = load_seg(t < t_end ? seg : nseg);
     while (t < t_end && cur.n_tiles == 0 && seg < nseg) cur = load_seg(++seg);
@@ -505,6 +547,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         po.n_splits = cur.n_splits;
         po.cta0 = cur.cta0;
         po.tile0 = cur.tile0;
+        po.c0_later = FUSED ? cur.slot0 : 0;
         po.b = cur.b;
         po.tok = cur.tok;
         po.pos = cur.pos;
@@ -543,9 +586,30 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
         ++qn;
       }
+      if (p.k_new && po.v_end == cur.n_vis) {
+        // this portion ends with the segment's last visible entry: store the new token (at
+        // the query position) into its slot before any copy of the portion's tiles is
+        // published -- the copy warps read it after the stage's release below
+        const int e = seg_entry(cur, cur.n_vis - 1);
+        const int pg = __ldg(p.page_table + int64_t(po.seg) * p.max_pages + e);
+        const int lp = p.page_logical ? __ldg(p.page_logical + int64_t(po.seg) * p.max_pages + e) : e;
+        if (lp == po.pos / P && pg >= 0 && pg < p.n_pool_pages) {
+          constexpr int CH = D / 8;                        // 16-byte chunks of a row
+          if (lane < 2 * CH) {
+            const int c = lane % CH;
+            const uint4* src = reinterpret_cast<const uint4*>(lane < CH ? p.k_new : p.v_new) + int64_t(po.seg) * CH + c;
+            uint4* dst = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(lane < CH ? p.k_pool : p.v_pool)) +
+                         (int64_t(pg) * P + po.pos % P) * CH + c;
+            *dst = __ldg(src);
+          }
+          __threadfence_block();
+        } else if (lane == 0) {
+          report(p.status, RK_ERR_DEVICE_BOUNDS);
+        }
+        __syncwarp();
+      }
       const int tpg = kGrp / EPT;                       // tiles per group
       const int n_grp = (po.n_kt + tpg - 1) / tpg;
-      const bool streaming = cur.n_tiles >= kStreamTiles;
       for (int grp = 0; ok && grp < n_grp; ++grp) {
         int raw_page_n, raw_lp_n;
         bool present_n;
@@ -558,49 +622,34 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           raw_page_n = raw_lp_n = -1;
           present_n = false;
         }
-        // this group's rows
+        // this group's page ids go to the copy warps, one stage (tile) at a time
         const bool page_ok = present && raw_page >= 0 && raw_page < p.n_pool_pages;
         if (present && !page_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
-        const int64_t row = page_ok ? int64_t(raw_page) * P : oob_row;
+        const int pidv = page_ok ? raw_page : -1;
         const int lpv = page_ok ? raw_lp : -1;
         const int tiles = min(tpg, po.n_kt - grp * tpg);
         for (int jt = 0; jt < tiles; ++jt, ++gg) {
           const int st = gg % NS;
-          int lps[8];
+          int lps[8], pids[8];
 #pragma unroll
-          for (int pg = 0; pg < 8; ++pg) lps[pg] = __shfl_sync(0xffffffffu, lpv, (jt * EPT + pg) & 31);
+          for (int pg = 0; pg < 8; ++pg) {
+            lps[pg] = __shfl_sync(0xffffffffu, lpv, (jt * EPT + pg) & 31);
+            pids[pg] = __shfl_sync(0xffffffffu, pidv, (jt * EPT + pg) & 31);
+          }
           bool got = true;
           if (lane == 0) {
             if (gg >= NS) got = wait_or_abort(sh, smem_addr(&sh.kv_empty[st]), ((gg / NS) - 1) & 1);
             if (got) {
 #pragma unroll
-              for (int pg = 0; pg < 8; ++pg)
-                if (pg < EPT) sh.lp[st][pg] = lps[pg];
-              mbar_arrive_expect_tx(smem_addr(&sh.kv_full[st]), kTileTx);
-              last_stage = st;
-              last_parity = (gg / NS) & 1;
+              for (int pg = 0; pg < 8; ++pg) {
+                sh.lp[st][pg] = pg < EPT ? lps[pg] : -1;
+                sh.pid[st][pg] = pg < EPT ? pids[pg] : -1;
+              }
+              sh.cmd[st] = 1;
+              mbar_arrive(smem_addr(&sh.desc_full[st]));
             }
           }
           if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-          const int pg = lane - jt * EPT;
-          if (pg >= 0 && pg < EPT) {
-            const uint32_t full = smem_addr(&sh.kv_full[st]);
-            if (streaming) {   // long segments: read once per call, keep them from evicting hot data
-#pragma unroll
-              for (int hf = 0; hf < HALVES; ++hf) {
-                const uint32_t off = st * LY::kStageBytes + hf * kHalfBytes + pg * P * 128;
-                tma_load_2d_hint(sK + off, &tmK, hf * 64, int(row), full, evict_first);
-                tma_load_2d_hint(sV + off, &tmV, hf * 64, int(row), full, evict_first);
-              }
-            } else {
-#pragma unroll
-              for (int hf = 0; hf < HALVES; ++hf) {
-                const uint32_t off = st * LY::kStageBytes + hf * kHalfBytes + pg * P * 128;
-                tma_load_2d(sK + off, &tmK, hf * 64, int(row), full);
-                tma_load_2d(sV + off, &tmV, hf * 64, int(row), full);
-              }
-            }
-          }
         }
         raw_page = raw_page_n;
         raw_lp = raw_lp_n;
@@ -610,12 +659,51 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       seg = nseg_idx;
       cur = nxt;
     }
-    if (!ok && lane == 0) set_abort(sh, p.status);
-    // copies still in flight after an abort: let them land before the CTA exits (bounded)
-    if (lane == 0 && aborted(sh)) {
-      if (last_stage >= 0) mbar_wait(smem_addr(&sh.kv_full[last_stage]), last_parity);
-      if (last_q >= 0) mbar_wait(smem_addr(&sh.q_full[last_q]), last_q_parity);
+    if (ok && lane == 0) {   // no more tiles: the copy warps stop
+      const int st = gg % NS;
+      if (gg < NS || wait_or_abort(sh, smem_addr(&sh.kv_empty[st]), ((gg / NS) - 1) & 1)) {
+        sh.cmd[st] = 0;
+        mbar_arrive(smem_addr(&sh.desc_full[st]));
+      } else {
+        ok = false;
+      }
     }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) set_abort(sh, p.status);
+    // a Q copy still in flight after an abort lands before the CTA exits (bounded)
+    if (lane == 0 && aborted(sh) && last_q >= 0) mbar_wait(smem_addr(&sh.q_full[last_q]), last_q_parity);
+  } else if (warp >= kCopyWarp0) {
+    // ------------------------------------------------------------------ copy warps
+    // Tile rows go straight from the pools into the 128-byte-swizzled layout the MMA reads
+    // (row r of a 64-channel block at r * 128 bytes, its 16-byte chunk c at chunk c ^ (r % 8)),
+    // with 16-byte cp.async copies: a warp instruction moves whole rows of one page (512
+    // contiguous bytes), and a copy thread's arrival on kv_full fires once its copies have landed.
+    constexpr int CH = D / 8;                         // 16-byte chunks per row
+    constexpr int RPI = 32 / CH;                      // rows per warp instruction
+    const int cw = warp - kCopyWarp0;
+    const int c16 = lane % CH, half = c16 >> 3, c = c16 & 7;
+    const int rsub = lane / CH;
+    const char* kb = reinterpret_cast<const char*>(p.k_pool);
+    const char* vb = reinterpret_cast<const char*>(p.v_pool);
+    const int pshift = P == 16 ? 4 : 5;
+    for (uint32_t gg = 0;; ++gg) {
+      const int st = gg % NS;
+      if (!wait_or_abort(sh, smem_addr(&sh.desc_full[st]), (gg / NS) & 1)) break;
+      const int cmd = sh.cmd[st];
+      if (cmd == 0) break;
+#pragma unroll
+      for (int i = 0; i < 32 / RPI; ++i) {
+        const int r = cw * 32 + i * RPI + rsub;       // key of the tile
+        const int pid = sh.pid[st][r >> pshift];
+        const uint32_t doff = st * LY::kStageBytes + half * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4);
+        const int64_t soff = pid >= 0 ? ((int64_t(pid) << pshift) + (r & (P - 1))) * (D * 2) + c16 * 16 : 0;
+        const uint32_t nb = pid >= 0 ? 16u : 0u;
+        cp_async16(sK + doff, kb + soff, nb);
+        cp_async16(sV + doff, vb + soff, nb);
+      }
+      cp_async_arrive(smem_addr(&sh.kv_full[st]));
+    }
+    cp_async_wait_all();   // nothing may land in shared memory after the CTA leaves
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -636,6 +724,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         // issue S^T(j) and the value product of earlier tiles in whatever order they become ready
         int qk = 0, pv = 0;
         uint64_t t_idle = 0;
+        uint32_t spins = 0;
         while (pv < n_kt) {
           bool did = false;
           if (qk < n_kt) {
@@ -644,6 +733,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             if (mbar_test(smem_addr(&sh.kv_full[st]), (g1 / NS) & 1) &&
                 (g1 < 2 || mbar_test(smem_addr(&sh.s_empty[sb]), ((g1 >> 1) - 1) & 1))) {
               tc_fence_after();
+              fence_proxy_async_smem();   // the copy warps' writes (generic proxy) before the MMA reads them
               const uint32_t kb = sK + st * LY::kStageBytes;
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
@@ -680,12 +770,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           }
           if (did) {
             t_idle = 0;
-          } else {
+            spins = 0;
+          } else if ((++spins & 255) == 0) {   // the timer and the abort flag are checked now and then
             if (aborted(sh)) { ok = false; break; }
             const uint64_t now = globaltimer();
             if (t_idle == 0) t_idle = now;
             else if (now - t_idle > kWaitNs) { ok = false; break; }
-            __nanosleep(32);
           }
         }
         gg += n_kt;
@@ -815,13 +905,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       bool two = false;
       if constexpr (FUSED) {
         if (split) {
-          const long long T = sh.T, gs = sh.gs;
           const int n = po.n_splits, j = int(blockIdx.x) - po.cta0;
           two = n > kMergeFan;
           n_grp = (n + kMergeFan - 1) / kMergeFan;
           const int q = j / kMergeFan;
           cq = po.cta0 + q * kMergeFan;
-          gslot = split_slot(cq, po.cta0, po.tile0, T, gs);
+          gslot = split_slot(cq, po.cta0, po.c0_later);
           cnt = two ? ws.counters + kDecMaxGrid + gslot : ws.counters + po.cta0;
           need = two ? min(kMergeFan, n - q * kMergeFan) : n;
           if (t == 0) ticket = take_ticket(cnt);
@@ -873,7 +962,6 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           // Log-sum-exp merge of the segment's pieces by the CTA with the last ticket; beyond
           // kMergeFan pieces in two levels (groups of kMergeFan consecutive CTAs, then the
           // group results).
-          const long long T = sh.T, gs = sh.gs;
           int32_t* flags = ws.counters + 3 * kDecMaxGrid;    // per partial slot
           int32_t* gflags = ws.counters + 5 * kDecMaxGrid;   // per group slot
           named_bar_sync(1, 128);                            // every partial store of the CTA is done
@@ -888,7 +976,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
               if (two) ticket2 = take_ticket(ws.counters + po.cta0);
             }
             if (t < need) {   // the group's (or segment's) other pieces
-              const int s = split_slot(cq + t, po.cta0, po.tile0, T, gs);
+              const int s = split_slot(cq + t, po.cta0, po.c0_later);
               if (s != po.slot) {
                 if (!wait_flag(flags + s)) report(p.status, RK_ERR_TIMEOUT);
                 zero_word(flags + s);
@@ -898,10 +986,10 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             __nv_bfloat16* out_row = p.out + (int64_t(po.tok) * p.Hq + h * G) * D;
             float* lse_row = p.lse ? p.lse + int64_t(po.tok) * p.Hq + h * G : nullptr;
             if (!two) {
-              merge_splits<D>(need, cq, 1, po.cta0, po.tile0, T, gs, ws.part_lse, ws.part_o, G, out_row, lse_row,
+              merge_splits<D>(need, cq, 1, po.cta0, po.c0_later, ws.part_lse, ws.part_o, G, out_row, lse_row,
                               nullptr, nullptr, t);
             } else {
-              merge_splits<D>(need, cq, 1, po.cta0, po.tile0, T, gs, ws.part_lse, ws.part_o, G, nullptr, nullptr,
+              merge_splits<D>(need, cq, 1, po.cta0, po.c0_later, ws.part_lse, ws.part_o, G, nullptr, nullptr,
                               ws.grp_lse + int64_t(gslot) * G, ws.grp_o + int64_t(gslot) * G * D, t);
               named_bar_sync(1, 128);                        // the group result is stored
               if (t == 0) sh.last = ticket2 == n_grp - 1;
@@ -911,14 +999,14 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
               } else {
                 if (t == 0) zero_word(ws.counters + po.cta0);
                 if (t < n_grp) {
-                  const int s = split_slot(po.cta0 + t * kMergeFan, po.cta0, po.tile0, T, gs);
+                  const int s = split_slot(po.cta0 + t * kMergeFan, po.cta0, po.c0_later);
                   if (s != gslot) {
                     if (!wait_flag(gflags + s)) report(p.status, RK_ERR_TIMEOUT);
                     zero_word(gflags + s);
                   }
                 }
                 named_bar_sync(1, 128);
-                merge_splits<D>(n_grp, po.cta0, kMergeFan, po.cta0, po.tile0, T, gs, ws.grp_lse, ws.grp_o, G,
+                merge_splits<D>(n_grp, po.cta0, kMergeFan, po.cta0, po.c0_later, ws.grp_lse, ws.grp_o, G,
                                 out_row, lse_row, nullptr, nullptr, t);
               }
             }
@@ -1019,15 +1107,11 @@ template <int D, int NG>
 cudaError_t launch_t(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream) {
   const bool fused = p.B * p.Hkv <= kDecFusedSegs;
   using LY = DecLayout<D>;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq;
   const cuuint64_t qdims[3] = {cuuint64_t(D), cuuint64_t(p.Hq), cuuint64_t(p.total_q)};
   const cuuint64_t qstr[2] = {cuuint64_t(D) * 2, cuuint64_t(p.Hq) * D * 2};
   const cuuint32_t qbox[3] = {64, cuuint32_t(p.G), 1};
-  const cuuint64_t kdims[2] = {cuuint64_t(D), cuuint64_t(p.n_pool_pages) * p.P};
-  const cuuint64_t kstr[1] = {cuuint64_t(D) * 2};
-  const cuuint32_t kbox[2] = {64, cuuint32_t(p.P)};
-  if (!encode_tmap_bf16(&mq, p.q, 3, qdims, qstr, qbox) || !encode_tmap_bf16(&mk, p.k_pool, 2, kdims, kstr, kbox) ||
-      !encode_tmap_bf16(&mv, p.v_pool, 2, kdims, kstr, kbox))
+  if (!encode_tmap_bf16(&mq, p.q, 3, qdims, qstr, qbox))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -1043,10 +1127,10 @@ cudaError_t launch_t(const AttnParams& p, const DecWorkspace& ws, cudaStream_t s
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(ws.grid), dim3(kThreads), LY::kSmem, stream, attr);
-  if (fused) return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, true>, mq, mk, mv, p, ws);
+  if (fused) return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, true>, mq, p, ws);
   cudaError_t e = launch_plan_decode(p, ws, stream);
   if (e != cudaSuccess) return e;
-  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, false>, mq, mk, mv, p, ws);
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, false>, mq, p, ws);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t cfg2 = pdl_config(dim3(4 * ws.grid), dim3(256), 0, stream, attr2);

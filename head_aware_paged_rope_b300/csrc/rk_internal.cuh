@@ -109,6 +109,8 @@ struct AttnParams {
   float* lse;
   int32_t* status;
   int32_t flags;       // RK_ATTN_* bits
+  const __nv_bfloat16* k_new;   // decode: the new token's K / V per head segment, or null
+  const __nv_bfloat16* v_new;
 };
 
 // Workspace carve-up for the attention calls.
@@ -325,6 +327,8 @@ cudaError_t launch_decode_tc(const AttnParams& p, const DecWorkspace& ws, cudaSt
 bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                       const cuuint32_t* box);
 cudaError_t launch_rope(const rk_rope_args& a, void* workspace, cudaStream_t stream);
+cudaError_t launch_append_kv(const rk_append_args& a, cudaStream_t stream);
+cudaError_t launch_ring_advance(const rk_ring_args& a, cudaStream_t stream);
 
 int device_sm_count();
 

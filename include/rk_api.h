@@ -174,6 +174,10 @@ typedef struct rk_attn_args {
   float* lse;                  /* fp32 [total_q][Hq] or NULL */
   int32_t* status;             /* optional device int32 error word, may be NULL */
   int32_t flags;               /* RK_ATTN_* bits below, 0 for none */
+  const void* k_new;           /* decode only, or NULL: bf16 [B][Hkv][d], the K of the token at
+                                  position seq_len[b] - 1, stored into its page slot before the
+                                  keys are read (as rk_append_kv would, within the same kernel) */
+  const void* v_new;           /* decode only, or NULL: bf16 [B][Hkv][d], its V; both or neither */
 } rk_attn_args;
 
 /* The table and length arrays (cu_seqlens_q, seq_len, page_table, page_logical, n_pages,
@@ -198,15 +202,19 @@ RK_API size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* args);
 RK_API size_t rk_segpaged_decode_workspace_size(const rk_attn_args* args);
 
 /* Prefill: any number of queries per sequence (a suffix at the end of the context).
- * Errors: RK_ERR_INVALID_ARG (NULL pointers, q / k_pool / v_pool / out not 16-byte aligned,
+ * Errors: RK_ERR_INVALID_ARG (NULL pointers, k_new or v_new set, q / k_pool / v_pool / out not 16-byte aligned,
  * B/Hq/Hkv/max_pages/total_q < 0, Hq % Hkv,
  * max_q > total_q), RK_ERR_UNSUPPORTED (d, P, Hq/Hkv > 16), RK_ERR_WORKSPACE, RK_ERR_CUDA. */
 RK_API rk_status rk_segpaged_prefill(const rk_attn_args* args, void* workspace, size_t workspace_bytes,
                               rk_stream_t stream);
 
 /* Decode: one query per sequence at position seq_len[b] - 1 (q is [B][Hq][d]); split-KV
- * over each head's visible pages, partial results merged by log-sum-exp.  Same errors, and
- * RK_ERR_UNSUPPORTED when B * Hkv exceeds 16384.
+ * over each head's visible pages, partial results merged by log-sum-exp.  With k_new and
+ * v_new the call first stores the new token's K and V at position seq_len[b] - 1 of every
+ * head segment -- the slot of the page its list gives for that logical page, which must
+ * be listed (else RK_ERR_DEVICE_BOUNDS and no store) -- so that a decode step needs no
+ * separate append.  Same errors as prefill (k_new / v_new: both or neither, 16-byte
+ * aligned), and RK_ERR_UNSUPPORTED when B * Hkv exceeds 16384.
  *
  * Workspace: its first 28928 bytes hold per-call split counters and flags.  They must be zero before
  * the first decode call that uses the workspace (e.g. cudaMemsetAsync of the whole
@@ -237,6 +245,68 @@ RK_API rk_status rk_segpaged_decode(const rk_attn_args* args, void* workspace, s
  * start over). */
 #define RK_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 RK_API rk_status rk_segpaged_decode_noalloc(const rk_attn_args* args, rk_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Decode-time storage: appending a step's K/V, and the page ring of local heads
+ *
+ * "小红书 RedKnot", section 3, first and fourth components: local heads keep only a window
+ * of KV (segmented per-head storage), which is what lets more sessions share a GPU.  Pages
+ * follow "PagedAttention & RadixAttention", section "The Solution: Fixed-size blocks":
+ * a token at position j lives in slot j % P of the page listed for logical page j / P.
+ *
+ * A decode step, per layer: rk_append_kv writes the new token's K and V, then
+ * rk_segpaged_decode attends to them.  Once per step, before the layers (so that the
+ * tables count as written before the layers' kernels, RK_ATTN_METADATA_STABLE), the
+ * tables of window-only local heads are advanced with rk_ring_advance.
+ * ------------------------------------------------------------------------------------ */
+typedef struct rk_append_args {
+  const void* k_new;           /* bf16 [B][Hkv][d], the new token's K per head segment */
+  const void* v_new;           /* bf16 [B][Hkv][d] */
+  const int32_t* pos;          /* int32 [B] position of the new token, >= 0 */
+  void* k_pool;                /* bf16 [n_pool_pages][P][d] */
+  void* v_pool;                /* bf16 [n_pool_pages][P][d] */
+  int64_t n_pool_pages;
+  const int32_t* page_table;   /* int32 [B*Hkv][max_pages], as for attention */
+  const int32_t* page_logical; /* int32 [B*Hkv][max_pages] ascending, or NULL (entry e is page e) */
+  const int32_t* n_pages;      /* int32 [B*Hkv] */
+  int32_t B, Hkv, d, P, max_pages;
+  int32_t* status;             /* optional device int32 error word, may be NULL */
+} rk_append_args;
+
+/* For every head segment s = b*Hkv + h, copy k_new[b][h] and v_new[b][h] bit for bit into
+ * slot pos[b] % P of the page the list gives for logical page pos[b] / P.  The list and its
+ * tables are only read.  Errors: RK_ERR_INVALID_ARG (NULL pointers with B*Hkv > 0, negative
+ * sizes, a pointer of k_new / v_new / k_pool / v_pool not 16-byte aligned), RK_ERR_UNSUPPORTED
+ * (d, P), RK_ERR_CUDA; on the device, a position whose page is not listed, a negative position,
+ * n_pages outside [0, max_pages] or a page id outside the pool skips that head segment and sets
+ * RK_ERR_DEVICE_BOUNDS. */
+RK_API rk_status rk_append_kv(const rk_append_args* args, rk_stream_t stream);
+
+typedef struct rk_ring_args {
+  const int32_t* pos;          /* int32 [B] position of the token about to be appended */
+  int32_t* page_table;         /* int32 [B*Hkv][max_pages], updated in place */
+  int32_t* page_logical;       /* int32 [B*Hkv][max_pages] ascending, updated in place (required) */
+  const int32_t* n_pages;      /* int32 [B*Hkv] (unchanged by the call) */
+  const int32_t* ring;         /* int32 [B*Hkv] ring size R > 0 of a window-only local head, 0 for
+                                  any other head segment (left alone) */
+  const int32_t* window;       /* int32 [B*Hkv] window W of the ring heads */
+  const int32_t* sink;         /* int32 [B*Hkv] sink S, or NULL for all zero */
+  int32_t B, Hkv, P, max_pages;
+  int32_t* status;             /* optional device int32 error word, may be NULL */
+} rk_ring_args;
+
+/* Advance the page ring of every head segment with ring[s] = R > 0.  Its list is the sink
+ * pages (logical pages below ceil(S/P)) followed by R window pages.  When pos[b] / P is
+ * above its last logical page, the first window entry -- the oldest page, which must end at
+ * or before position pos[b] - W, i.e. lie wholly outside the new token's window -- gives its
+ * physical page to logical page pos[b] / P: the window entries move down by one and the new
+ * page takes the last entry.  R = ceil(W/P) + 1 window pages ending at the page before
+ * pos[b] / P always satisfy this.  Several layers can be advanced in one call by laying
+ * their tables out as extra sequences.  Errors: RK_ERR_INVALID_ARG (NULL pointers with
+ * B*Hkv > 0, negative sizes), RK_ERR_UNSUPPORTED (P), RK_ERR_CUDA; on the device, a ring
+ * that is not full or whose oldest page is still inside the window, or n_pages outside
+ * [1, max_pages], leaves that head segment unchanged and sets RK_ERR_DEVICE_BOUNDS. */
+RK_API rk_status rk_ring_advance(const rk_ring_args* args, rk_stream_t stream);
 
 /* Static text for a status code. */
 RK_API const char* rk_status_string(rk_status status);

@@ -33,6 +33,11 @@ What it computes, and where the pages state it:
       o = sum_{j in V(p)} softmax_j(q . k_j * scale) v_j,   lse = log sum_j e^{q.k_j*scale}
   with scale = 1/sqrt(d) and query head h reading KV head h // (Hq/Hkv).
 * Split combine (standard FlashAttention split-KV merge of partial (m, l, o)).
+* Decode-time storage ("小红书 RedKnot" section 3, first and fourth components: local
+  heads keep only a window of KV; pages as in "PagedAttention & RadixAttention"): the
+  new token's K/V go to slot pos % P of the page listed for logical page pos // P; a
+  window-only local head reuses the page of its oldest window entry once the window has
+  left it (append_rows, ring_advance).
 
 Readings of silent points are listed in the repository's design notes; the
 pins that tie each function to something other than itself live in
@@ -306,3 +311,52 @@ def attention_flops(batch) -> int:
             for i in range(nq):
                 pairs += len(visible_set(cls, W, S, L, L - nq + i, listed))
     return 4 * d * G * pairs
+
+
+# ----------------------------------------------------------------------------- decode storage
+def append_rows(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.ndarray, page_logical: np.ndarray,
+                n_pages: np.ndarray, pos: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, Hkv: int, P: int):
+    """Copies of the pools with the new token of every head segment stored: segment
+    s = b*Hkv + h writes k_new[b, h] / v_new[b, h] (bf16 bits, unchanged) to slot pos[b] % P
+    of the physical page its list gives for logical page pos[b] // P."""
+    k_out, v_out = np.array(k_pool, copy=True), np.array(v_pool, copy=True)
+    B = len(pos)
+    for b in range(B):
+        for h in range(Hkv):
+            s = b * Hkv + h
+            lp = int(pos[b]) // P
+            listed = [int(x) for x in page_logical[s, :int(n_pages[s])]]
+            e = listed.index(lp)                     # the page must be listed
+            phys = int(page_table[s, e])
+            k_out[phys, int(pos[b]) % P] = k_new[b, h]
+            v_out[phys, int(pos[b]) % P] = v_new[b, h]
+    return k_out, v_out
+
+
+def ring_advance(page_table: np.ndarray, page_logical: np.ndarray, n_pages: np.ndarray, ring: np.ndarray,
+                 window: np.ndarray, sink: np.ndarray, pos: np.ndarray, Hkv: int, P: int):
+    """Copies of the tables after the page ring of each window-only local head (ring[s] > 0)
+    has made room for the token at pos[b]: if logical page pos // P is not listed yet, the
+    oldest window page (the first entry after the sink pages) leaves the window -- it must
+    end at or before pos - W -- and its physical page holds the new logical page, which
+    becomes the last entry."""
+    tab, lg = np.array(page_table, copy=True), np.array(page_logical, copy=True)
+    for s in range(len(ring)):
+        R = int(ring[s])
+        if R <= 0:
+            continue
+        p = int(pos[s // Hkv])
+        n = int(n_pages[s])
+        entries = list(zip(lg[s, :n].tolist(), tab[s, :n].tolist()))   # (logical, physical)
+        if entries[-1][0] >= p // P:
+            continue
+        sink_pages = -(-int(sink[s]) // P)
+        sinks = [x for x in entries if x[0] < sink_pages]
+        win = [x for x in entries if x[0] >= sink_pages]
+        assert len(win) == R, "the ring holds R window pages"
+        oldest_lp, oldest_phys = win[0]
+        assert (oldest_lp + 1) * P - 1 <= p - int(window[s]), "the oldest page is outside the window"
+        new = sinks + win[1:] + [(p // P, oldest_phys)]
+        lg[s, :n] = [x[0] for x in new]
+        tab[s, :n] = [x[1] for x in new]
+    return tab, lg

@@ -12,7 +12,11 @@ INCLUDE = os.path.join(ROOT, "include")
 
 ATTN_FIELDS = ["q", "cu_seqlens_q", "seq_len", "k_pool", "v_pool", "n_pool_pages", "page_table", "page_logical",
                "n_pages", "head_class", "window", "sink", "B", "Hq", "Hkv", "d", "P", "max_pages", "total_q", "max_q",
-               "scale", "out", "lse", "status", "flags"]
+               "scale", "out", "lse", "status", "flags", "k_new", "v_new"]
+APPEND_FIELDS = ["k_new", "v_new", "pos", "k_pool", "v_pool", "n_pool_pages", "page_table", "page_logical", "n_pages",
+                 "B", "Hkv", "d", "P", "max_pages", "status"]
+RING_FIELDS = ["pos", "page_table", "page_logical", "n_pages", "ring", "window", "sink", "B", "Hkv", "P", "max_pages",
+               "status"]
 ROPE_FIELDS = ["k_src", "n_src_pages", "k_dst", "n_dst_pages", "src_tables", "n_src_entries", "dst_tables",
                "n_dst_entries", "runs", "n_runs", "max_tok", "P", "d", "theta", "style", "status"]
 RUN_FIELDS = ["src_tab_off", "src_tab_len", "dst_tab_off", "dst_tab_len", "pos_off0", "pos_on0", "n_tok", "reserved"]
@@ -23,7 +27,8 @@ def _probe(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "rk_api.h"', "int main(void) {"]
-    for struct, fields in (("rk_attn_args", ATTN_FIELDS), ("rk_rope_args", ROPE_FIELDS), ("rk_rope_run", RUN_FIELDS)):
+    for struct, fields in (("rk_attn_args", ATTN_FIELDS), ("rk_rope_args", ROPE_FIELDS), ("rk_rope_run", RUN_FIELDS),
+                           ("rk_append_args", APPEND_FIELDS), ("rk_ring_args", RING_FIELDS)):
         lines.append('  printf("%s sizeof %%zu\\n", sizeof(%s));' % (struct, struct))
         for f in fields:
             lines.append('  printf("%s %s %%zu\\n", offsetof(%s, %s));' % (struct, f, struct, f))
@@ -44,7 +49,8 @@ def test_ctypes_mirrors_match_the_c_header(tmp_path):
     import head_aware_paged_rope_b300._binding as B
     got = _probe(tmp_path)
     for struct, cls, fields in (("rk_attn_args", B.AttnArgs, ATTN_FIELDS), ("rk_rope_args", B.RopeArgs, ROPE_FIELDS),
-                                ("rk_rope_run", B.RopeRun, RUN_FIELDS)):
+                                ("rk_rope_run", B.RopeRun, RUN_FIELDS), ("rk_append_args", B.AppendArgs, APPEND_FIELDS),
+                                ("rk_ring_args", B.RingArgs, RING_FIELDS)):
         assert [n for n, _ in cls._fields_] == fields, struct
         assert ctypes.sizeof(cls) == got[(struct, "sizeof")], struct
         for f in fields:

@@ -376,16 +376,68 @@ def test_decode_workspace_reused_across_shapes(rk):
             assert int(ws[256:28928].count_nonzero().item()) == 0
 
 
+def _ring_decode_steps(rk, w, kp, k_host, check_steps):
+    """Decode with appended tokens over window-only local heads, as the 128K stack runs it:
+    per step rk_ring_advance and rk_segpaged_decode (which stores the new token itself) on
+    the GPU, and the oracle's ring and append on the host; the outputs of `check_steps`
+    are compared."""
+    a = w.attn
+    st = _status()
+    dev = {k: to_device(v, "cuda") for k, v in dict(tab=w.dec_page_table, lg=w.dec_page_logical, n=w.dec_n_pages,
+                                                     ring=w.ring, window=a.window, sink=a.sink, cls=a.head_class,
+                                                     vp=a.v_pool).items()}
+    v_host = a.v_pool
+    tab, lg = w.dec_page_table, w.dec_page_logical
+    out = torch.empty((a.B, a.Hq, a.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((a.B, a.Hq), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+    for s in range(max(check_steps) + 1):
+        pos = (a.seq_len + s).astype(np.int32)
+        pos_d, seq_d = to_device(pos, "cuda"), to_device(pos + 1, "cuda")
+        rk.ring_advance(rk.ring_args(pos_d, dev["tab"], dev["lg"], dev["n"], dev["ring"], dev["window"], dev["sink"],
+                                     Hkv=a.Hkv, P=a.P, status=st))
+        q = to_device(w.decode_q[s], "cuda")
+        kn, vn = to_device(w.decode_k[s], "cuda"), to_device(w.decode_v[s], "cuda")
+        rk.segpaged_decode(rk.attn_args(q, seq_d, kp, dev["vp"], dev["tab"], dev["lg"], dev["n"], dev["cls"],
+                                        dev["window"], dev["sink"], out, lse=lse, status=st, total_q=a.B, max_q=1,
+                                        flags=rk.RK_ATTN_METADATA_STABLE, k_new=kn, v_new=vn), workspace=ws)
+        tab, lg = O.ring_advance(tab, lg, w.dec_n_pages, w.ring, a.window, a.sink, pos, a.Hkv, a.P)
+        k_host, v_host = O.append_rows(k_host, v_host, tab, lg, w.dec_n_pages, pos, w.decode_k[s], w.decode_v[s],
+                                       a.Hkv, a.P)
+        if s in check_steps:
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0
+            assert np.array_equal(dev["tab"].cpu().numpy(), tab) and np.array_equal(dev["lg"].cpu().numpy(), lg)
+            gk, gv = bf16_bits(kp), bf16_bits(dev["vp"])
+            for h in range(a.Hkv):                   # this step's rows, at the slots the host's tables give
+                e = int(np.searchsorted(lg[h, :int(w.dec_n_pages[h])], int(pos[0]) // a.P))
+                assert np.array_equal(gk[int(tab[h, e]), int(pos[0]) % a.P], w.decode_k[s][0, h])
+                assert np.array_equal(gv[int(tab[h, e]), int(pos[0]) % a.P], w.decode_v[s][0, h])
+            d = dataclasses.replace(a, q=w.decode_q[s], cu_seqlens_q=np.arange(a.B + 1, dtype=np.int32),
+                                    seq_len=pos + 1, k_pool=k_host, v_pool=v_host, page_table=tab, page_logical=lg,
+                                    n_pages=w.dec_n_pages)
+            _compare(d, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
 def test_stack_small_prefill_then_decode(rk):
-    w = synth.stack_layer(0, n_segments=4, seg_tokens=1024, n_suffix=100, n_decode=4)
+    w = synth.stack_layer(0, n_segments=4, seg_tokens=1024, n_suffix=100, n_decode=40)
     kp = _gpu_rope(rk, w)
     oracle_pool = _check_rope(w, bf16_bits(kp))
     a = dataclasses.replace(w.attn, k_pool=oracle_pool)
     out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
     _compare(a, out, lse)
+    _ring_decode_steps(rk, w, kp, oracle_pool, (0, 17, 39))
+
+
+def test_stack_small_prestored_decode(rk):
+    # the same layer with every token stored in advance (no ring, no appends)
+    w = synth.stack_layer(0, n_segments=4, seg_tokens=1024, n_suffix=100, n_decode=4, ring_decode=False)
+    kp = _gpu_rope(rk, w)
+    oracle_pool = _check_rope(w, bf16_bits(kp))
+    a = dataclasses.replace(w.attn, k_pool=oracle_pool)
     for step in (0, 3):
         d = synth.decode_batch_from(dataclasses.replace(w, attn=a), step)
-        out, lse = _gpu_attn(rk, d, decode=True, flags=rk.RK_ATTN_METADATA_STABLE)
+        out, lse = _gpu_attn(rk, d, decode=True, flags=rk.RK_ATTN_METADATA_STABLE, k_pool=kp)
         _compare(d, out, lse)
 
 
@@ -422,10 +474,7 @@ def test_stack_layer_full_size_sampled(rk):
     a = dataclasses.replace(w.attn, k_pool=oracle_pool)
     out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
     _compare(a, out, lse, rows=_sample_rows(a, 7, per_head=16))
-    for step in (0, 31, 63):
-        d = synth.decode_batch_from(dataclasses.replace(w, attn=a), step)
-        out, lse = _gpu_attn(rk, d, decode=True)
-        _compare(d, out, lse)
+    _ring_decode_steps(rk, w, kp, oracle_pool, (0, 31, 63))
 
 
 # ------------------------------------------------------------------------- group sizes and pairings

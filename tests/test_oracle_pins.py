@@ -328,3 +328,67 @@ def test_retrieval_head_on_a_sparse_list_equals_hand_indexed_attention():
         got_o, got_l = res[(t, 0)]
         assert np.allclose(got_o, o, atol=1e-13)
         assert np.allclose(got_l, np.log(np.exp(s).sum(axis=1)), atol=1e-12)
+
+
+# ------------------------------------------------------------------ decode storage
+def test_append_rows_follows_the_worked_block_table():
+    """The generated tokens of the worked example ("fathers" at t = 7, "brought" at t = 8)
+    land in the physical block and slot the example prints."""
+    g = _load("vllm_block_table.json")
+    P = g["block_size"]
+    tab = np.array([g["block_table"]], np.int32)
+    lg = np.arange(3, dtype=np.int32)[None]
+    k = np.zeros((g["n_physical_blocks"], P, 2), np.uint16)
+    for tok in g["tokens"][7:]:
+        new = np.array([[[1000 + tok["t"], 7]]], np.uint16)
+        k2, v2 = O.append_rows(k, k, tab, lg, np.array([3]), np.array([tok["t"]]), new, new, 1, P)
+        assert np.array_equal(k2[tok["physical"], tok["slot"]], new[0, 0])
+        assert np.count_nonzero(k2 != k) == 2                    # that row, nothing else
+
+
+def test_ring_advance_worked_example():
+    g = _load("page_ring.json")
+    P, W, S, R = g["P"], g["W"], g["S"], g["R"]
+    tab = np.array([g["initial"]["physical"]], np.int32)
+    lg = np.array([g["initial"]["logical"]], np.int32)
+    n = np.array([len(g["initial"]["logical"])], np.int32)
+    k = np.zeros((8, P, 1), np.uint16)
+    for step in g["after"]:
+        tab, lg = O.ring_advance(tab, lg, n, np.array([R]), np.array([W]), np.array([S]), np.array([step["pos"]]), 1, P)
+        assert lg[0].tolist() == step["logical"] and tab[0].tolist() == step["physical"]
+        new = np.array([[[step["pos"]]]], np.uint16)
+        k, _ = O.append_rows(k, k, tab, lg, n, np.array([step["pos"]]), new, new, 1, P)
+        assert k[step["slot"][0], step["slot"][1], 0] == step["pos"]
+
+
+def test_ring_keeps_every_window_visible_over_a_long_decode():
+    """Invariants over 3000 appended tokens for several (P, W, S): the list stays ascending,
+    holds the same physical pages (the ring reuses only its own), and lists every position
+    of the newest token's window and of the sink; each appended token stays readable until
+    it leaves the window."""
+    for P, W, S in ((16, 512, 0), (16, 256, 4), (32, 100, 0), (4, 6, 2), (16, 16, 0), (16, 1, 0)):
+        R = -(-W // P) + 1
+        start = 4 * P + 8 * W                                   # the first decode position
+        sink_pages = list(range(-(-S // P)))
+        hi = start // P + (start % P != 0)                      # one past the page holding start - 1
+        win_pages = list(range(hi - R, hi))
+        lg = np.array([sink_pages + win_pages], np.int32)
+        tab = np.arange(lg.shape[1], dtype=np.int32)[None] + 40
+        n = np.array([lg.shape[1]], np.int32)
+        phys0 = set(tab[0].tolist())
+        written = {}
+        k = np.zeros((40 + lg.shape[1], P, 1), np.uint16)
+        for pos in range(start, start + 3000):
+            tab, lg = O.ring_advance(tab, lg, n, np.array([R]), np.array([W]), np.array([S]), np.array([pos]), 1, P)
+            assert np.all(np.diff(lg[0]) > 0) and set(tab[0].tolist()) == phys0
+            new = np.array([[[pos % 60000]]], np.uint16)
+            k, _ = O.append_rows(k, k, tab, lg, n, np.array([pos]), new, new, 1, P)
+            written[pos] = pos % 60000
+            listed = set(O.listed_positions(lg[0], int(n[0]), P).tolist())
+            vis = O.visible_set(O.LOCAL, W, S, pos + 1, pos, np.array(sorted(listed)))
+            want = [j for j in range(pos + 1) if j > pos - W or j < S]
+            assert vis.tolist() == want
+            for j in range(max(0, pos - W + 1), pos + 1):       # appended tokens still in the window
+                if j in written:
+                    e = int(np.searchsorted(lg[0], j // P))
+                    assert k[tab[0, e], j % P, 0] == written[j]

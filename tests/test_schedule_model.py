@@ -11,66 +11,102 @@ MERGE_FAN = 12      # kMergeFan
 MAX_GRID = 1024     # kDecMaxGrid
 
 
+SHORT = 8           # kShortTiles
+
+
 def owner(t, T, gs):
     return ((t + 1) * gs + T - 1) // T - 1
 
 
-def split_slot(c, cta0, tile0, T, gs):
-    return 2 * c + 1 if (c == cta0 and c * T // gs < tile0) else 2 * c
+def share_cut(c, T, gs, tile0, nt):
+    """First tile of CTA c's share: c*T/gs, moved to the nearer end (ties: its start) of the
+    segment it falls in when that segment has at most SHORT tiles."""
+    if c <= 0:
+        return 0
+    if c >= gs:
+        return T
+    raw = c * T // gs
+    s = int(np.searchsorted(tile0, raw, side="right")) - 1        # last segment with tile0 <= raw
+    t0, n = int(tile0[s]), int(nt[s])
+    if raw <= t0 or raw >= t0 + n or n > SHORT:
+        return raw
+    return t0 if raw - t0 <= t0 + n - raw else t0 + n
+
+
+def split_slot(c, cta0, c0_later):
+    return 2 * c + 1 if (c == cta0 and c0_later) else 2 * c
 
 
 def decode_schedule(nt, grid):
-    """Per head segment: (tile0, cta0, n_splits); per (segment, CTA) piece: the slot the
-    producer gives it (2c for the CTA's first portion, 2c+1 for a later one)."""
+    """Per head segment: (tile0, cta0, n_splits, c0_later) as the producer derives them; per
+    (segment, CTA) piece of the shares: the slot the producer gives it (2c for the CTA's
+    first portion, 2c+1 for a later one)."""
     nt = np.asarray(nt, dtype=np.int64)
     tile0 = np.concatenate([[0], np.cumsum(nt)[:-1]])
     T = int(nt.sum())
     gs = min(grid, T)
+    cuts = [share_cut(c, T, gs, tile0, nt) for c in range(gs + 1)]
     segs, pieces = [], {}
     for s, (t0, n) in enumerate(zip(tile0, nt)):
         if n == 0:
             segs.append(None)
             continue
-        c0, c1 = owner(int(t0), T, gs), owner(int(t0 + n - 1), T, gs)
-        segs.append((int(t0), c0, c1 - c0 + 1))
+        if n > SHORT:
+            c0, c1 = owner(int(t0), T, gs), owner(int(t0 + n - 1), T, gs)
+        else:
+            c0 = c1 = -1
+        later = int(c1 > c0 and cuts[c0] < t0)
+        segs.append((int(t0), c0, c1 - c0 + 1, later))
     for c in range(gs):
-        tb, te = c * T // gs, (c + 1) * T // gs
+        tb, te = cuts[c], cuts[c + 1]
         first = True
         for s, (t0, n) in enumerate(zip(tile0, nt)):
             if n == 0 or t0 + n <= tb or t0 >= te:
                 continue
             pieces[(s, c)] = 2 * c + (0 if first else 1)
             first = False
-    return T, gs, segs, pieces
+    return T, gs, cuts, segs, pieces
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(60))
 def test_decode_shares_slots_and_counters(seed):
     rng = np.random.default_rng(seed)
-    grid = int(rng.choice([1, 3, 8, 148]))
+    grid = int(rng.choice([1, 3, 8, 40, 148]))
     nseg = int(rng.integers(1, 400))
-    kind = seed % 4
+    kind = seed % 5
     if kind == 0:
         nt = rng.integers(0, 6, nseg)                       # short (local) segments, some empty
     elif kind == 1:
         nt = rng.integers(0, 3, nseg); nt[rng.integers(nseg)] = int(rng.integers(200, 1200))   # one long head
     elif kind == 2:
         nt = rng.integers(1, 80, nseg)
-    else:
+    elif kind == 3:
         nt = np.zeros(nseg, np.int64); nt[rng.integers(nseg)] = int(rng.integers(1, 3000))
-    T, gs, segs, pieces = decode_schedule(nt, grid)
-    # every tile has exactly one owner and the shares tile [0, T)
-    owners = [owner(t, T, gs) for t in range(T)]
-    for c in range(gs):
-        tb, te = c * T // gs, (c + 1) * T // gs
-        assert te > tb and all(owners[t] == c for t in range(tb, te))
+    else:                                                   # windows of 5 tiles and a few long heads
+        nt = np.full(nseg, 5, np.int64); nt[rng.integers(nseg, size=3)] = rng.integers(9, 1100, 3)
+    T, gs, cuts, segs, pieces = decode_schedule(nt, grid)
+    # the cuts are monotone and the shares tile [0, T)
+    assert cuts[0] == 0 and cuts[-1] == T and all(a <= b for a, b in zip(cuts, cuts[1:]))
+    tile0 = np.concatenate([[0], np.cumsum(nt)[:-1]])
+    for s, (t0, n) in enumerate(zip(tile0, nt)):
+        held = [c for c in range(gs) if n and cuts[c] < t0 + n and cuts[c + 1] > t0]
+        if n == 0:
+            continue
+        if n <= SHORT:                                      # short segments: one CTA, no split
+            assert len(held) == 1 and segs[s][2] == 1
+        else:                                               # long ones: the CTAs c*T/gs gives
+            t0_, c0, k, _ = segs[s]
+            assert held == list(range(c0, c0 + k))
+            for t in range(int(t0), int(t0 + n)):
+                c = owner(t, T, gs)
+                assert cuts[c] <= t < cuts[c + 1]
     # slots: the kernel's split_slot formula gives the producer's slot; all distinct, < 2*grid
     split_slots = {}
     for (s, c), slot in pieces.items():
-        t0, c0, n = segs[s]
-        assert c0 <= c < c0 + n
+        t0, c0, n, later = segs[s]
         if n > 1:
-            assert split_slot(c, c0, t0, T, gs) == slot
+            assert c0 <= c < c0 + n
+            assert split_slot(c, c0, later) == slot
             split_slots[(s, c)] = slot
     assert len(set(split_slots.values())) == len(split_slots)
     assert all(0 <= v < 2 * grid for v in split_slots.values())
@@ -80,19 +116,26 @@ def test_decode_shares_slots_and_counters(seed):
     for s, rec in enumerate(segs):
         if rec is None or rec[2] == 1:
             continue
-        t0, c0, n = rec
+        t0, c0, n, later = rec
         seg_ctr.append(c0)
         if n > MERGE_FAN:
             for q in range((n + MERGE_FAN - 1) // MERGE_FAN):
-                grp_ctr.append(split_slot(c0 + q * MERGE_FAN, c0, t0, T, gs))
+                grp_ctr.append(split_slot(c0 + q * MERGE_FAN, c0, later))
     assert len(set(seg_ctr)) == len(seg_ctr) and all(c < MAX_GRID for c in seg_ctr)
     assert len(set(grp_ctr)) == len(grp_ctr) and all(g < 2 * MAX_GRID for g in grp_ctr)
     # the pieces of a split segment are exactly its CTAs' slots
     for s, rec in enumerate(segs):
         if rec is not None and rec[2] > 1:
-            t0, c0, n = rec
+            t0, c0, n, later = rec
             assert sorted(v for (ss, c), v in split_slots.items() if ss == s) == \
-                sorted(split_slot(c, c0, t0, T, gs) for c in range(c0, c0 + n))
+                sorted(split_slot(c, c0, later) for c in range(c0, c0 + n))
+
+
+def test_short_windows_stay_whole_on_a_local_only_layer():
+    # eight local heads of five key tiles each over 148 CTAs: eight CTAs take one window each
+    T, gs, cuts, segs, pieces = decode_schedule([5] * 8, 148)
+    assert all(rec[2] == 1 for rec in segs)
+    assert sorted(cuts[c + 1] - cuts[c] for c in range(gs) if cuts[c + 1] > cuts[c]) == [5] * 8
 
 
 def prefill_items(n_vis, chunk):

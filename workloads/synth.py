@@ -158,6 +158,14 @@ class Workload:
     rope: Optional[RopeJob]
     theta: float
     decode_q: Optional[np.ndarray] = None   # uint16 [steps][B][Hq][d] for decode steps after the prefill
+    # decode with appended tokens (ring_decode): the K/V each step appends, and the tables the
+    # decode starts from -- window-only local heads keep a ring of their last `ring` window pages
+    decode_k: Optional[np.ndarray] = None   # uint16 [steps][B][Hkv][d]
+    decode_v: Optional[np.ndarray] = None   # uint16 [steps][B][Hkv][d]
+    dec_page_table: Optional[np.ndarray] = None     # int32 [B*Hkv][max_pages]
+    dec_page_logical: Optional[np.ndarray] = None   # int32 [B*Hkv][max_pages]
+    dec_n_pages: Optional[np.ndarray] = None        # int32 [B*Hkv]
+    ring: Optional[np.ndarray] = None               # int32 [B*Hkv]: ring pages of a window-only local head, else 0
 
 
 class _PageAllocator:
@@ -182,19 +190,26 @@ def _cdiv(a: int, b: int) -> int:
 
 def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, windows, sinks,
            seg_tokens, k_scale=None, retrieval_frac=0.25, retrieval_window=256,
-           local_window_only=False, pool_slack=1.0, n_decode=0, style=0, with_rope=True):
+           local_window_only=False, pool_slack=1.0, n_decode=0, style=0, with_rope=True, ring_decode=False):
     """Common builder.
 
     ctx_len[b]: context tokens (made of reusable segments of seg_tokens[b] each, the
     last one possibly shorter); n_suffix[b]: suffix queries; classes/windows/sinks:
     [B][Hkv].  Storage of every head segment is dense over [0, seq_len + n_decode);
-    what a head *lists* for attention depends on its class.
+    what a head *lists* for attention depends on its class.  With local_window_only,
+    local heads store (and list) only their sink pages and the pages covering the
+    windows of their queries.  With ring_decode as well, local heads store nothing for
+    the decode steps: each step appends its token (decode_k / decode_v), and a local
+    head starts the decode from its last ceil(W/P) + 1 window pages, which it reuses as
+    a ring (dec_* tables, ring); other heads have their decode pages allocated already.
     """
     ctx_len = np.asarray(ctx_len, dtype=np.int64)
     n_suffix = np.asarray(n_suffix, dtype=np.int64)
     seq_len = ctx_len + n_suffix                     # prefill length
     store_len = seq_len + n_decode                   # tokens stored per head segment
     pages_per_head = [_cdiv(int(s), P) for s in store_len]
+    if ring_decode:
+        local_window_only = True
 
     # page lists (logical indices) per head segment
     lists = []
@@ -207,7 +222,7 @@ def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, wi
                 first_q = int(seq_len[b] - n_suffix[b])
                 lo_pos = max(0, first_q - int(windows[b][h]) + 1)
                 lp = set(range(0, _cdiv(int(sinks[b][h]), P)))
-                lp.update(range(lo_pos // P, npg))
+                lp.update(range(lo_pos // P, _cdiv(int(seq_len[b]), P) if ring_decode else npg))
                 lists.append(np.array(sorted(lp), dtype=np.int32))
             elif c == RETRIEVAL:
                 n_ctx_pages = _cdiv(int(ctx_len[b]), P)
@@ -321,6 +336,21 @@ def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, wi
                 pages = src_tabs[r]
                 kf[pages] *= k_scale[h][None, None, :]
             k_src = f32_to_bf16_bits(kf)
+        if local_window_only:
+            # a window-only local head repositions only the tokens it stores: the run is cut
+            # to the stored logical pages (sink pages, then the window pages)
+            cut = []
+            for r, (b, h, pos_on0, n, npg) in zip(runs, src_list):
+                if int(classes[b][h]) != LOCAL:
+                    cut.append(r)
+                    continue
+                st = stored[b * Hkv + h]
+                lo_s, hi_s = pos_on0, pos_on0 + n
+                for a0, a1 in _page_ranges(st):
+                    x0, x1 = max(lo_s, a0 * P), min(hi_s, a1 * P)
+                    if x0 < x1:
+                        cut.append([r[0], r[1], r[2], r[3], x0 - pos_on0, x0, x1 - x0, 0])
+            runs = cut
         rope = RopeJob(k_src=k_src,
                        src_tables=np.concatenate(src_tabs).astype(np.int32) if src_tabs else np.zeros(1, np.int32),
                        dst_tables=np.concatenate(dst_tabs).astype(np.int32),
@@ -330,7 +360,42 @@ def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, wi
     decode_q = None
     if n_decode:
         decode_q = _normal_bf16(rng, (n_decode, B, Hq, d))
-    return Workload(name=name, attn=attn, rope=rope, theta=theta, decode_q=decode_q)
+    wl = Workload(name=name, attn=attn, rope=rope, theta=theta, decode_q=decode_q)
+    if ring_decode and n_decode:
+        wl.decode_k = _normal_bf16(rng, (n_decode, B, Hkv, d))
+        wl.decode_v = _normal_bf16(rng, (n_decode, B, Hkv, d))
+        tab, lg, nn = page_table.copy(), page_logical.copy(), n_pages.copy()
+        ring = np.zeros(B * Hkv, dtype=np.int32)
+        for b in range(B):
+            for h in range(Hkv):
+                i = b * Hkv + h
+                if int(classes[b][h]) != LOCAL:
+                    continue
+                R = _cdiv(int(windows[b][h]), P) + 1
+                n = int(n_pages[i])
+                n_sink = int(np.count_nonzero(page_logical[i, :n] < _cdiv(int(sinks[b][h]), P)))
+                if n - n_sink < R:
+                    raise ValueError("the prefill lists fewer window pages than the ring needs")
+                keep = list(range(n_sink)) + list(range(n - R, n))
+                tab[i, :] = -1
+                lg[i, :] = -1
+                tab[i, :len(keep)] = page_table[i, keep]
+                lg[i, :len(keep)] = page_logical[i, keep]
+                nn[i] = len(keep)
+                ring[i] = R
+        wl.dec_page_table, wl.dec_page_logical, wl.dec_n_pages, wl.ring = tab, lg, nn, ring
+    return wl
+
+
+def _page_ranges(pages) -> List:
+    """Maximal runs [a, b) of consecutive logical pages in a sorted page list."""
+    out = []
+    for x in (int(v) for v in pages):
+        if out and out[-1][1] == x:
+            out[-1][1] = x + 1
+        else:
+            out.append([x, x + 1])
+    return out
 
 
 # --------------------------------------------------------------------------------------
@@ -398,16 +463,21 @@ def stack_classes(seed: int = 1004, n_layers: int = 8, Hkv: int = 8, global_frac
 def stack_layer(layer: int, seed: int = 1004, n_layers: int = 8, n_segments: int = 32,
                 seg_tokens: int = 4096, n_suffix: int = 1024, n_decode: int = 64, Hq: int = 64,
                 Hkv: int = 8, d: int = 128, P: int = 16, window: int = 512,
-                global_frac: float = 0.04, theta: float = 1e6) -> Workload:
+                global_frac: float = 0.04, theta: float = 1e6, ring_decode: bool = True) -> Workload:
     """One layer of the 128K long-context stack: n_segments x seg_tokens context, suffix
-    prefill of n_suffix tokens, then n_decode decode steps whose K/V tokens are already
-    stored (step s sees seq_len = ctx + n_suffix + s + 1)."""
+    prefill of n_suffix tokens, then n_decode decode steps (step s appends the token at
+    position ctx + n_suffix + s and sees seq_len = ctx + n_suffix + s + 1).  With ring_decode
+    (the default) local heads store only their window -- the pages covering the windows of
+    the suffix queries, so only the tail of the last segment is repositioned for them --
+    and recycle a ring of ceil(W/P) + 1 pages during the decode; without it every head
+    stores every token and the decode tokens are stored in advance."""
     classes = stack_classes(seed, n_layers, Hkv, global_frac)[layer]
     rng = np.random.default_rng([seed, layer])
     windows = [[0 if c == GLOBAL else window for c in classes]]
     return _build(f"stack_layer{layer}", rng, B=1, Hq=Hq, Hkv=Hkv, d=d, P=P, theta=theta,
                   ctx_len=[n_segments * seg_tokens], n_suffix=[n_suffix], classes=[classes],
-                  windows=windows, sinks=[[0] * Hkv], seg_tokens=[seg_tokens], n_decode=n_decode)
+                  windows=windows, sinks=[[0] * Hkv], seg_tokens=[seg_tokens], n_decode=n_decode,
+                  ring_decode=ring_decode)
 
 
 def mixed_classes(seed: int = 1005, B: int = 8, lengths=(2048, 4096, 8192, 16384),
@@ -436,13 +506,26 @@ def mixed_classes(seed: int = 1005, B: int = 8, lengths=(2048, 4096, 8192, 16384
 
 
 def decode_batch_from(wl: Workload, step: int) -> AttnBatch:
-    """The decode launch at `step` after a prefill workload built with n_decode > 0:
-    one query per sequence at position seq_len + step."""
+    """The decode launch at `step` after a prefill workload built with n_decode > 0 whose
+    decode tokens are stored in advance: one query per sequence at position seq_len + step."""
+    if wl.ring is not None:
+        raise ValueError("this workload appends its decode tokens: its tables change every step")
     a = wl.attn
     B = a.B
     return dataclasses.replace(
         a, q=np.ascontiguousarray(wl.decode_q[step]), cu_seqlens_q=np.arange(B + 1, dtype=np.int32),
         seq_len=(a.seq_len + step + 1).astype(np.int32), name=f"{a.name}_decode{step}")
+
+
+def dense_listing(batch: AttnBatch, n_tokens) -> AttnBatch:
+    """The same launch with every head listing every logical page below n_tokens[b] / P,
+    for counting work: a window-only head that lists its whole window (as the page ring
+    guarantees) has the same visible keys as with a full list."""
+    B, Hkv, P = batch.B, batch.Hkv, batch.P
+    n = np.repeat([_cdiv(int(x), P) for x in n_tokens], Hkv).astype(np.int32)
+    mp = max(int(n.max()), 1)
+    lg = np.tile(np.arange(mp, dtype=np.int32), (B * Hkv, 1))
+    return dataclasses.replace(batch, page_logical=lg, page_table=np.zeros_like(lg), n_pages=n)
 
 
 WORKLOADS = {
