@@ -56,6 +56,8 @@ class AttnArgs(ctypes.Structure):
         ("P", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_q", ctypes.c_int32),
         ("scale", ctypes.c_float), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("status", ctypes.c_void_p),
         ("flags", ctypes.c_int32), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("k_rot", ctypes.c_void_p), ("rot_coef", ctypes.c_void_p), ("n_rot", ctypes.c_int32),
+        ("rot_style", ctypes.c_int32),
     ]
 
 
@@ -78,6 +80,14 @@ class RingArgs(ctypes.Structure):
     ]
 
 
+class SparseFfnArgs(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p), ("importance", ctypes.c_void_p), ("T", ctypes.c_int32), ("d_model", ctypes.c_int32),
+        ("d_ff", ctypes.c_int32), ("keep", ctypes.c_int32), ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
+        ("w_down", ctypes.c_void_p), ("out", ctypes.c_void_p), ("kept", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
 def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"librk.so not built at {path}; run python -m head_aware_paged_rope_b300.build")
@@ -94,10 +104,17 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.rk_rope_coefficients.restype = ctypes.c_int
+    lib.rk_rope_coefficients.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                         ctypes.c_void_p, ctypes.c_void_p]
     lib.rk_append_kv.restype = ctypes.c_int
     lib.rk_append_kv.argtypes = [ctypes.POINTER(AppendArgs), ctypes.c_void_p]
     lib.rk_ring_advance.restype = ctypes.c_int
     lib.rk_ring_advance.argtypes = [ctypes.POINTER(RingArgs), ctypes.c_void_p]
+    lib.rk_sparse_ffn_workspace_size.restype = ctypes.c_size_t
+    lib.rk_sparse_ffn_workspace_size.argtypes = [ctypes.POINTER(SparseFfnArgs)]
+    lib.rk_sparse_ffn.restype = ctypes.c_int
+    lib.rk_sparse_ffn.argtypes = [ctypes.POINTER(SparseFfnArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     lib.rk_status_string.restype = ctypes.c_char_p
     lib.rk_status_string.argtypes = [ctypes.c_int]
     lib.rk_version.restype = ctypes.c_int32
@@ -141,6 +158,14 @@ def _check(code: int, where: str) -> None:
         raise RkError(code, where)
 
 
+def rope_coefficients(deltas: torch.Tensor, d: int, theta: float, stream=None) -> torch.Tensor:
+    """fp32 [n][d/2][4] coefficient rows of the turns by `deltas` (int32 device tensor)."""
+    coef = torch.empty((deltas.numel(), d // 2, 4), dtype=torch.float32, device=deltas.device)
+    _check(LIB.rk_rope_coefficients(_ptr(deltas), deltas.numel(), d, float(theta), _ptr(coef), _stream(stream)),
+           "rk_rope_coefficients")
+    return coef
+
+
 def rope_workspace_size(n_runs: int, d: int) -> int:
     return int(LIB.rk_rope_workspace_size(n_runs, d))
 
@@ -162,7 +187,7 @@ def rope_reposition(k_src: torch.Tensor, k_dst: torch.Tensor, src_tables: torch.
 
 def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, head_class, window, sink, out,
               *, cu_seqlens_q=None, lse=None, status=None, total_q: int, max_q: int, scale: float = 0.0,
-              flags: int = 0, k_new=None, v_new=None) -> AttnArgs:
+              flags: int = 0, k_new=None, v_new=None, k_rot=None, rot_coef=None, rot_style: int = 0) -> AttnArgs:
     B = seq_len.shape[0]
     Hq, d = q.shape[1], q.shape[2]
     Hkv = n_pages.shape[0] // max(B, 1)
@@ -172,7 +197,8 @@ def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, hea
                     window=_ptr(window), sink=_ptr(sink), B=B, Hq=Hq, Hkv=Hkv, d=d, P=k_pool.shape[1],
                     max_pages=page_table.shape[1], total_q=int(total_q), max_q=int(max_q), scale=float(scale),
                     out=_ptr(out), lse=_ptr(lse), status=_ptr(status), flags=int(flags), k_new=_ptr(k_new),
-                    v_new=_ptr(v_new))
+                    v_new=_ptr(v_new), k_rot=_ptr(k_rot), rot_coef=_ptr(rot_coef),
+                    n_rot=0 if rot_coef is None else int(rot_coef.shape[0]), rot_style=int(rot_style))
 
 
 def segpaged_prefill_workspace_size(args: AttnArgs) -> int:
@@ -223,6 +249,22 @@ def ring_args(pos, page_table, page_logical, n_pages, ring, window, sink, *, Hkv
 
 def ring_advance(args: RingArgs, stream=None) -> None:
     _check(LIB.rk_ring_advance(ctypes.byref(args), _stream(stream)), "rk_ring_advance")
+
+
+def sparse_ffn_args(x, importance, w_gate, w_up, w_down, out, kept, *, keep: int, status=None) -> SparseFfnArgs:
+    """x: bf16 [T][d_model]; importance: fp32 [T]; w_gate/w_up: bf16 [d_ff][d_model];
+    w_down: bf16 [d_model][d_ff]; out: bf16 [T][d_model]; kept: int32 [keep]."""
+    T, d_model = x.shape
+    return SparseFfnArgs(x=_ptr(x), importance=_ptr(importance), T=T, d_model=d_model, d_ff=w_gate.shape[0],
+                         keep=int(keep), w_gate=_ptr(w_gate), w_up=_ptr(w_up), w_down=_ptr(w_down), out=_ptr(out),
+                         kept=_ptr(kept), status=_ptr(status))
+
+
+def sparse_ffn(args: SparseFfnArgs, *, device=None, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    n = int(LIB.rk_sparse_ffn_workspace_size(ctypes.byref(args)))
+    ws = _workspace(n, device or torch.device("cuda"), workspace)
+    _check(LIB.rk_sparse_ffn(ctypes.byref(args), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)),
+           "rk_sparse_ffn")
 
 
 def version() -> int:

@@ -62,6 +62,11 @@ rk_status check_attn(const rk_attn_args* a, bool decode) {
   if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
   if (a->flags & ~(RK_ATTN_METADATA_STABLE | RK_ATTN_DIAG_EXPIRE_WAIT)) return RK_ERR_INVALID_ARG;
   if ((a->k_new != nullptr) != (a->v_new != nullptr) || (!decode && a->k_new)) return RK_ERR_INVALID_ARG;
+  if (a->k_rot) {
+    if (!decode) return RK_ERR_UNSUPPORTED;   // prefill reads repositioned pages (rk_rope_reposition)
+    if (!a->rot_coef || a->n_rot < 0 || (reinterpret_cast<uintptr_t>(a->rot_coef) & 15u) != 0) return RK_ERR_INVALID_ARG;
+    if (a->rot_style != RK_ROPE_HALF_SPLIT && a->rot_style != RK_ROPE_INTERLEAVED) return RK_ERR_UNSUPPORTED;
+  }
   return RK_OK;
 }
 
@@ -120,6 +125,10 @@ AttnParams make_params(const rk_attn_args* a, const AttnLayout& l) {
   p.flags = a->flags;
   p.k_new = static_cast<const __nv_bfloat16*>(a->k_new);
   p.v_new = static_cast<const __nv_bfloat16*>(a->v_new);
+  p.k_rot = a->k_rot;
+  p.rot_coef = static_cast<const float4*>(a->rot_coef);
+  p.n_rot = a->n_rot;
+  p.rot_style = a->rot_style;
   return p;
 }
 
@@ -263,6 +272,18 @@ rk_status rk_rope_reposition(const rk_rope_args* a, void* workspace, size_t work
   return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }
 
+rk_status rk_rope_coefficients(const int32_t* deltas, int32_t n, int32_t d, double theta, void* coef,
+                               rk_stream_t stream) {
+  if (n < 0) return RK_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return RK_ERR_UNSUPPORTED;
+  if (!(theta > 1.0) || !std::isfinite(theta)) return RK_ERR_INVALID_ARG;
+  if (n == 0) return RK_OK;
+  if (!deltas || !coef || (reinterpret_cast<uintptr_t>(coef) & 15u) != 0) return RK_ERR_INVALID_ARG;
+  if (n > 65535) return RK_ERR_UNSUPPORTED;
+  return rk::launch_rope_coefficients(deltas, n, d, theta, coef, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RK_OK : RK_ERR_CUDA;
+}
+
 size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* a) {
   if (rk::check_attn(a, false) != RK_OK) return 0;
   if (a->B == 0 || a->total_q == 0) return 0;
@@ -305,6 +326,35 @@ rk_status rk_ring_advance(const rk_ring_args* a, rk_stream_t stream) {
     return RK_ERR_INVALID_ARG;
   if (int64_t(a->B) * a->Hkv >= (int64_t(1) << 31) / 32) return RK_ERR_UNSUPPORTED;
   return rk::launch_ring_advance(*a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
+}
+
+namespace {
+rk_status check_ffn(const rk_sparse_ffn_args* a) {
+  if (!a) return RK_ERR_INVALID_ARG;
+  if (a->T < 0 || a->d_model <= 0 || a->d_ff <= 0 || a->keep < 0 || a->keep > a->T) return RK_ERR_INVALID_ARG;
+  if (a->d_model % 256 != 0 || a->d_ff % 128 != 0 || a->T > 65536) return RK_ERR_UNSUPPORTED;
+  if (a->T == 0) return RK_OK;
+  if (!a->x || !a->importance || !a->out || (a->keep > 0 && (!a->w_gate || !a->w_up || !a->w_down || !a->kept)))
+    return RK_ERR_INVALID_ARG;
+  const auto al16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  if (!al16(a->x) || !al16(a->out) || !al16(a->w_gate) || !al16(a->w_up) || !al16(a->w_down)) return RK_ERR_INVALID_ARG;
+  return RK_OK;
+}
+}  // namespace
+
+size_t rk_sparse_ffn_workspace_size(const rk_sparse_ffn_args* a) {
+  if (check_ffn(a) != RK_OK || a->keep == 0) return 0;
+  return rk::sparse_ffn_ws_bytes(a->keep, a->d_model, a->d_ff);
+}
+
+rk_status rk_sparse_ffn(const rk_sparse_ffn_args* a, void* ws, size_t bytes, rk_stream_t stream) {
+  const rk_status st = check_ffn(a);
+  if (st != RK_OK || a->T == 0) return st;
+  if (a->keep > 0) {
+    const size_t need = rk::sparse_ffn_ws_bytes(a->keep, a->d_model, a->d_ff);
+    if (!ws || bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RK_ERR_WORKSPACE;
+  }
+  return rk::launch_sparse_ffn(*a, ws, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }
 
 const char* rk_status_string(rk_status s) {

@@ -71,8 +71,10 @@ __global__ __launch_bounds__(kWarps * 32) void append_kv_kernel(const rk_append_
 // after the sink pages) gives its physical page to it -- the window entries move down by
 // one and the new logical page takes the last entry.
 __global__ __launch_bounds__(kWarps * 32) void ring_advance_kernel(const rk_ring_args a) {
-  sm100::grid_dependency_wait();     // the tables: earlier readers and writers are complete
-  sm100::grid_launch_dependents();
+  // the tables: earlier readers and writers are complete.  No early start for the kernels
+  // after this one: decode calls may read the tables before their predecessor completes
+  // (RK_ATTN_METADATA_STABLE), so nothing may start before these writes are done.
+  sm100::grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = blockIdx.x * kWarps + warp;
   if (seg >= a.B * a.Hkv) return;

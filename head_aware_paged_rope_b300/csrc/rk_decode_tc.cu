@@ -95,6 +95,10 @@ struct DecShared {
   int lp[6][8];             // logical page of each page slot of a stage (-1: none)
   int pid[6][8];            // physical page of each page slot of a stage (-1: none, zeros are copied)
   int cmd[6];               // per stage: 0 stop, 1 copy
+  int app_row[6];           // per stage: the tile row that takes the new token (k_new / v_new), or -1
+  int rot[6][8];            // per page slot of a stage: coefficient row of its K turn, or -1
+  int any_rot[6];           // some page of the stage is turned
+  int app_seg[6];           // its head segment
   float red[2][4][kN];      // per-warp tile maxima (double-buffered by tile parity)
   float redl[4][kN];        // per-warp denominators
   float lse2[kN];
@@ -310,7 +314,7 @@ __device__ __forceinline__ void merge_splits(int n, int c_first, int stride, int
   }
 }
 
-template <int D, int NG, bool FUSED>
+template <int D, int NG, bool FUSED, bool ROT>
 __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                  AttnParams p, DecWorkspace ws) {
   using LY = DecLayout<D>;
@@ -463,15 +467,17 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const int t_end = my.tile_end;
     // raw page id / logical page of entry v_begin + grp*32 + lane of segment s (present: listed)
     auto fetch = [&](int s, const DecSeg& sd, int v_begin, int v_end, int grp, int& raw_page, int& raw_lp,
-                     bool& present) {
+                     int& raw_rot, bool& present) {
       const int v = v_begin + grp * kGrp + lane;
       present = s < nseg && v < v_end;
       raw_page = -1;
       raw_lp = -1;
+      raw_rot = -1;
       if (present) {
         const int en = seg_entry(sd, v);
         raw_page = __ldg(p.page_table + int64_t(s) * p.max_pages + en);
         raw_lp = p.page_logical ? __ldg(p.page_logical + int64_t(s) * p.max_pages + en) : en;
+        if constexpr (ROT) raw_rot = __ldg(p.k_rot + int64_t(s) * p.max_pages + en);
       }
     };
     auto load_seg = [&](int s) {
@@ -519,10 +525,14 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     bool ok = true;
     DecSeg cur = load_seg(t < t_end ? seg : nseg);
     while (t < t_end && cur.n_tiles == 0 && seg < nseg) cur = load_seg(++seg);
-    int raw_page, raw_lp;
+    int raw_page, raw_lp, raw_rot;
     bool present;
-    fetch(seg, cur, (t < t_end && seg < nseg) ? (t - cur.tile0) * EPT : 0, cur.n_vis, 0, raw_page, raw_lp, present);
-    if (early) grid_dependency_wait();
+    fetch(seg, cur, (t < t_end && seg < nseg) ? (t - cur.tile0) * EPT : 0, cur.n_vis, 0, raw_page, raw_lp, raw_rot,
+          present);
+    // with stable metadata the page ids are published before the preceding kernel completes
+    // (the copy warps wait for it before copying); q is read after that wait, just before the
+    // first step that may block on the pipeline
+    bool waited = !early;
     for (int k = 0; ok; ++k) {
       const int slot = k % kRing;
       if (k >= kRing) {
@@ -568,7 +578,14 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       const bool more = cur.tile0 + lt1 < t_end;
       int nseg_idx = seg + 1;
       DecSeg nxt = load_seg(more ? nseg_idx : nseg);
-      {   // Q rows of the group -> buffer qn & 1, free once the MMAs of portion qn - 2 are done
+      bool q_done = false;
+      // Q rows of the group -> buffer qn & 1, free once the MMAs of portion qn - 2 are done
+      auto load_q = [&]() -> bool {
+        if (q_done) return true;
+        if (!waited) {
+          grid_dependency_wait();
+          waited = true;
+        }
         bool got = true;
         if (lane == 0) {
           const int b = qn & 1;
@@ -583,43 +600,23 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             last_q_parity = (qn >> 1) & 1;
           }
         }
-        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        q_done = true;
         ++qn;
-      }
-      if (p.k_new && po.v_end == cur.n_vis) {
-        // this portion ends with the segment's last visible entry: store the new token (at
-        // the query position) into its slot before any copy of the portion's tiles is
-        // published -- the copy warps read it after the stage's release below
-        const int e = seg_entry(cur, cur.n_vis - 1);
-        const int pg = __ldg(p.page_table + int64_t(po.seg) * p.max_pages + e);
-        const int lp = p.page_logical ? __ldg(p.page_logical + int64_t(po.seg) * p.max_pages + e) : e;
-        if (lp == po.pos / P && pg >= 0 && pg < p.n_pool_pages) {
-          constexpr int CH = D / 8;                        // 16-byte chunks of a row
-          if (lane < 2 * CH) {
-            const int c = lane % CH;
-            const uint4* src = reinterpret_cast<const uint4*>(lane < CH ? p.k_new : p.v_new) + int64_t(po.seg) * CH + c;
-            uint4* dst = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(lane < CH ? p.k_pool : p.v_pool)) +
-                         (int64_t(pg) * P + po.pos % P) * CH + c;
-            *dst = __ldg(src);
-          }
-          __threadfence_block();
-        } else if (lane == 0) {
-          report(p.status, RK_ERR_DEVICE_BOUNDS);
-        }
-        __syncwarp();
-      }
+        return __shfl_sync(0xffffffffu, got, 0);
+      };
+      const int lt_first = po.v_begin / EPT;            // tile of the segment the portion starts at
       const int tpg = kGrp / EPT;                       // tiles per group
       const int n_grp = (po.n_kt + tpg - 1) / tpg;
       for (int grp = 0; ok && grp < n_grp; ++grp) {
-        int raw_page_n, raw_lp_n;
+        int raw_page_n, raw_lp_n, raw_rot_n;
         bool present_n;
         if (grp + 1 < n_grp) {
-          fetch(seg, cur, po.v_begin, po.v_end, grp + 1, raw_page_n, raw_lp_n, present_n);
+          fetch(seg, cur, po.v_begin, po.v_end, grp + 1, raw_page_n, raw_lp_n, raw_rot_n, present_n);
         } else if (more) {
           while (nxt.n_tiles == 0 && nseg_idx < nseg) nxt = load_seg(++nseg_idx);   // segments with nothing visible
-          fetch(nseg_idx, nxt, 0, nxt.n_vis, 0, raw_page_n, raw_lp_n, present_n);
+          fetch(nseg_idx, nxt, 0, nxt.n_vis, 0, raw_page_n, raw_lp_n, raw_rot_n, present_n);
         } else {
-          raw_page_n = raw_lp_n = -1;
+          raw_page_n = raw_lp_n = raw_rot_n = -1;
           present_n = false;
         }
         // this group's page ids go to the copy warps, one stage (tile) at a time
@@ -627,25 +624,47 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         if (present && !page_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
         const int pidv = page_ok ? raw_page : -1;
         const int lpv = page_ok ? raw_lp : -1;
+        const bool rot_ok = raw_rot >= -1 && raw_rot < p.n_rot;
+        if (page_ok && !rot_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
+        const int rotv = page_ok && rot_ok ? raw_rot : -1;
         const int tiles = min(tpg, po.n_kt - grp * tpg);
         for (int jt = 0; jt < tiles; ++jt, ++gg) {
           const int st = gg % NS;
-          int lps[8], pids[8];
+          int lps[8], pids[8], rots[8];
 #pragma unroll
           for (int pg = 0; pg < 8; ++pg) {
             lps[pg] = __shfl_sync(0xffffffffu, lpv, (jt * EPT + pg) & 31);
             pids[pg] = __shfl_sync(0xffffffffu, pidv, (jt * EPT + pg) & 31);
+            rots[pg] = __shfl_sync(0xffffffffu, rotv, (jt * EPT + pg) & 31);
           }
+          // the segment's last tile holds the query position, where the new token goes
+          int app_r = -1;
+          if (p.k_new && lt_first + grp * tpg + jt == cur.n_tiles - 1) {
+            const int pg = (cur.n_vis - 1) % EPT;
+            int lpa = -1, pia = -1;
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              if (x == pg) { lpa = lps[x]; pia = pids[x]; }
+            if (lpa == po.pos / P && pia >= 0) app_r = pg * P + po.pos % P;
+            else if (lane == 0) report(p.status, RK_ERR_DEVICE_BOUNDS);
+          }
+          if (gg >= NS && !load_q()) { ok = false; break; }   // the wait below may block: q first
           bool got = true;
           if (lane == 0) {
             if (gg >= NS) got = wait_or_abort(sh, smem_addr(&sh.kv_empty[st]), ((gg / NS) - 1) & 1);
             if (got) {
 #pragma unroll
+              int any = 0;
               for (int pg = 0; pg < 8; ++pg) {
                 sh.lp[st][pg] = pg < EPT ? lps[pg] : -1;
                 sh.pid[st][pg] = pg < EPT ? pids[pg] : -1;
+                sh.rot[st][pg] = pg < EPT ? rots[pg] : -1;
+                any |= (pg < EPT && rots[pg] >= 0) ? 1 : 0;
               }
+              sh.any_rot[st] = any;
               sh.cmd[st] = 1;
+              sh.app_row[st] = app_r;
+              sh.app_seg[st] = po.seg;
               mbar_arrive(smem_addr(&sh.desc_full[st]));
             }
           }
@@ -653,8 +672,10 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         }
         raw_page = raw_page_n;
         raw_lp = raw_lp_n;
+        raw_rot = raw_rot_n;
         present = present_n;
       }
+      if (ok && !load_q()) ok = false;
       t = cur.tile0 + lt1;
       seg = nseg_idx;
       cur = nxt;
@@ -686,11 +707,75 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const char* kb = reinterpret_cast<const char*>(p.k_pool);
     const char* vb = reinterpret_cast<const char*>(p.v_pool);
     const int pshift = P == 16 ? 4 : 5;
+    // Repositioning on load: K rows of pages with a coefficient row are turned in shared memory
+    // once this thread's copies of the stage have landed (each thread turns the chunks it
+    // copied; the partner chunk of a half-split pair is the lane CH/2 away), then the stage
+    // is released with a plain arrival.  The turn is rotate_pair, as in the RoPE kernel.
+    constexpr int HCH = CH / 2;                       // chunks per half of a row
+    const bool a_lane = c16 < HCH;
+    int cur_rot = -1;
+    float4 cf[8];
+    auto turn_stage = [&](int st) {
+      const int app = sh.app_row[st];
+#pragma unroll
+      for (int i = 0; i < 32 / RPI; ++i) {
+        const int r = cw * 32 + i * RPI + rsub;
+        const int rot = sh.rot[st][r >> pshift];
+        const uint32_t addr = sK + st * LY::kStageBytes + half * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4);
+        uint4 x;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w) : "r"(addr));
+        const bool go = rot >= 0 && r != app;
+        if (go && rot != cur_rot) {   // coefficient rows change only between segments
+          cur_rot = rot;
+          const int i0 = p.rot_style == RK_ROPE_HALF_SPLIT ? 8 * (c16 % HCH) : 4 * c16;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (p.rot_style == RK_ROPE_HALF_SPLIT || k < 4) cf[k] = __ldg(p.rot_coef + int64_t(rot) * (D / 2) + i0 + k);
+        }
+        uint4 y = x;
+        if (p.rot_style == RK_ROPE_HALF_SPLIT) {
+          uint4 o;                                    // the partner chunk (same row, other half)
+          o.x = __shfl_xor_sync(0xffffffffu, x.x, HCH);
+          o.y = __shfl_xor_sync(0xffffffffu, x.y, HCH);
+          o.z = __shfl_xor_sync(0xffffffffu, x.z, HCH);
+          o.w = __shfl_xor_sync(0xffffffffu, x.w, HCH);
+          if (go) {
+            const uint4 xa = a_lane ? x : o, xb = a_lane ? o : x;
+            float r8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t ua = (k >> 1) == 0 ? xa.x : (k >> 1) == 1 ? xa.y : (k >> 1) == 2 ? xa.z : xa.w;
+              const uint32_t ub = (k >> 1) == 0 ? xb.x : (k >> 1) == 1 ? xb.y : (k >> 1) == 2 ? xb.z : xb.w;
+              float ya, yb;
+              rotate_pair((k & 1) ? bf16hi(ua) : bf16lo(ua), (k & 1) ? bf16hi(ub) : bf16lo(ub), cf[k], ya, yb);
+              r8[k] = a_lane ? ya : yb;
+            }
+            y.x = pack_bf16(r8[0], r8[1]); y.y = pack_bf16(r8[2], r8[3]);
+            y.z = pack_bf16(r8[4], r8[5]); y.w = pack_bf16(r8[6], r8[7]);
+          }
+        } else if (go) {                              // pairs (2i, 2i+1) inside the chunk
+          float r8[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t u = k == 0 ? x.x : k == 1 ? x.y : k == 2 ? x.z : x.w;
+            rotate_pair(bf16lo(u), bf16hi(u), cf[k], r8[2 * k], r8[2 * k + 1]);
+          }
+          y.x = pack_bf16(r8[0], r8[1]); y.y = pack_bf16(r8[2], r8[3]);
+          y.z = pack_bf16(r8[4], r8[5]); y.w = pack_bf16(r8[6], r8[7]);
+        }
+        if (go) st_shared_v4(addr, y);
+      }
+      fence_proxy_async_smem();   // the turned rows (generic proxy) before the MMA reads them
+      mbar_arrive(smem_addr(&sh.kv_full[st]));
+    };
+    int pending = -1;                                 // stage whose turn waits for its copies
+    if (early) grid_dependency_wait();   // the pools (and k_new / v_new) are read and written from here on
     for (uint32_t gg = 0;; ++gg) {
       const int st = gg % NS;
       if (!wait_or_abort(sh, smem_addr(&sh.desc_full[st]), (gg / NS) & 1)) break;
       const int cmd = sh.cmd[st];
       if (cmd == 0) break;
+      const int app_r = sh.app_row[st];
 #pragma unroll
       for (int i = 0; i < 32 / RPI; ++i) {
         const int r = cw * 32 + i * RPI + rsub;       // key of the tile
@@ -698,12 +783,39 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         const uint32_t doff = st * LY::kStageBytes + half * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4);
         const int64_t soff = pid >= 0 ? ((int64_t(pid) << pshift) + (r & (P - 1))) * (D * 2) + c16 * 16 : 0;
         const uint32_t nb = pid >= 0 ? 16u : 0u;
-        cp_async16(sK + doff, kb + soff, nb);
-        cp_async16(sV + doff, vb + soff, nb);
+        if (r == app_r) {
+          // the new token: copied from k_new / v_new, and stored into its pool slot for later steps
+          const int64_t noff = int64_t(sh.app_seg[st]) * (D * 2) + c16 * 16;
+          const char* kn = reinterpret_cast<const char*>(p.k_new) + noff;
+          const char* vn = reinterpret_cast<const char*>(p.v_new) + noff;
+          cp_async16(sK + doff, kn, 16u);
+          cp_async16(sV + doff, vn, 16u);
+          *reinterpret_cast<uint4*>(const_cast<char*>(kb) + soff) = __ldg(reinterpret_cast<const uint4*>(kn));
+          *reinterpret_cast<uint4*>(const_cast<char*>(vb) + soff) = __ldg(reinterpret_cast<const uint4*>(vn));
+        } else {
+          cp_async16(sK + doff, kb + soff, nb);
+          cp_async16(sV + doff, vb + soff, nb);
+        }
       }
-      cp_async_arrive(smem_addr(&sh.kv_full[st]));
+      if constexpr (ROT) {
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (pending >= 0) {   // the previous stage's copies have landed once at most this one is open
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+          __syncwarp();
+          turn_stage(pending);
+          pending = -1;
+        }
+        if (sh.any_rot[st]) pending = st;
+        else cp_async_arrive(smem_addr(&sh.kv_full[st]));
+      } else {
+        cp_async_arrive(smem_addr(&sh.kv_full[st]));
+      }
     }
     cp_async_wait_all();   // nothing may land in shared memory after the CTA leaves
+    if (pending >= 0 && !aborted(sh)) {
+      __syncwarp();
+      turn_stage(pending);
+    }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -1117,20 +1229,24 @@ cudaError_t launch_t(const AttnParams& p, const DecWorkspace& ws, cudaStream_t s
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, NG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         LY::kSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_tc_kernel<D, NG, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               LY::kSmem);
+    cudaError_t e = cudaSuccess;
+    for (auto* k : {decode_tc_kernel<D, NG, true, false>, decode_tc_kernel<D, NG, false, false>,
+                    decode_tc_kernel<D, NG, true, true>, decode_tc_kernel<D, NG, false, true>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(ws.grid), dim3(kThreads), LY::kSmem, stream, attr);
-  if (fused) return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, true>, mq, p, ws);
+  // the turn on load is compiled only into the kernels that use it
+  const bool rot = p.k_rot != nullptr;
+  if (fused)
+    return rot ? cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, true, true>, mq, p, ws)
+               : cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, true, false>, mq, p, ws);
   cudaError_t e = launch_plan_decode(p, ws, stream);
   if (e != cudaSuccess) return e;
-  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, false>, mq, p, ws);
+  e = rot ? cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, false, true>, mq, p, ws)
+          : cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, NG, false, false>, mq, p, ws);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t cfg2 = pdl_config(dim3(4 * ws.grid), dim3(256), 0, stream, attr2);

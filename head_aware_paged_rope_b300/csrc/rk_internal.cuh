@@ -42,6 +42,21 @@ __device__ __forceinline__ float fast_log2(float x) {
   return y;
 }
 
+// ------------------------------------------------------------------ RoPE turn of one channel pair
+// (xa, xb) turned by the angle whose cos / sin are split into a head with 16 significant bits
+// and an fp32 tail, cf = (c_hi, c_lo, s_hi, s_lo): for bf16 inputs the head products are exact
+// in fp32, so the result carries only the final fp32 rounding even when the products cancel.
+// Used by the RoPE kernel and by the attention kernels that turn K as they read it, so both
+// produce the same bf16 values.
+__device__ __forceinline__ void rotate_pair(float xa, float xb, const float4& cf, float& ya, float& yb) {
+  const float hi_a = fmaf(xa, cf.x, -(xb * cf.z));   // xa*c_hi - xb*s_hi (both products exact)
+  const float lo_a = fmaf(xa, cf.y, -(xb * cf.w));
+  const float hi_b = fmaf(xa, cf.z, xb * cf.x);      // xa*s_hi + xb*c_hi
+  const float lo_b = fmaf(xa, cf.w, xb * cf.y);
+  ya = hi_a + lo_a;
+  yb = hi_b + lo_b;
+}
+
 // ------------------------------------------------------------------ attention work list
 // A unit is one (head segment, query tile): the queries [tok0, tok0+ntok) of one sequence
 // against one KV head.  Its visible page-list entries form at most two ranges (sink pages
@@ -111,6 +126,10 @@ struct AttnParams {
   int32_t flags;       // RK_ATTN_* bits
   const __nv_bfloat16* k_new;   // decode: the new token's K / V per head segment, or null
   const __nv_bfloat16* v_new;
+  const int32_t* k_rot;         // per listed entry: coefficient row of its K turn, -1 none; or null
+  const float4* rot_coef;       // [n_rot][d/2] (c_hi, c_lo, s_hi, s_lo)
+  int32_t n_rot;
+  int32_t rot_style;
 };
 
 // Workspace carve-up for the attention calls.
@@ -327,7 +346,11 @@ cudaError_t launch_decode_tc(const AttnParams& p, const DecWorkspace& ws, cudaSt
 bool encode_tmap_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                       const cuuint32_t* box);
 cudaError_t launch_rope(const rk_rope_args& a, void* workspace, cudaStream_t stream);
+cudaError_t launch_rope_coefficients(const int32_t* deltas, int n, int d, double theta, void* coef,
+                                     cudaStream_t stream);
 cudaError_t launch_append_kv(const rk_append_args& a, cudaStream_t stream);
+size_t sparse_ffn_ws_bytes(int keep, int d_model, int d_ff);
+cudaError_t launch_sparse_ffn(const rk_sparse_ffn_args& a, void* ws, cudaStream_t stream);
 cudaError_t launch_ring_advance(const rk_ring_args& a, cudaStream_t stream);
 
 int device_sm_count();

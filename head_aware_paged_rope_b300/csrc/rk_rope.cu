@@ -21,13 +21,9 @@ namespace {
 
 using namespace sm100;
 
-__global__ void rope_coeff_kernel(const rk_rope_run* __restrict__ runs, int n_runs, int d,
-                                  double theta, float4* __restrict__ coef) {
-  const int run = blockIdx.x;
-  const int i = threadIdx.x;
-  if (run >= n_runs || i >= d / 2) return;
-  const rk_rope_run r = runs[run];
-  const double delta = double((long long)r.pos_on0 - (long long)r.pos_off0);
+// cos / sin of delta * theta^(-2i/d) in double precision, each split into a head with 16
+// significant bits (so that head * bf16 is exact in fp32) and an fp32 tail.
+__device__ __forceinline__ float4 rope_coeff(double delta, int i, int d, double theta) {
   const double w = pow(theta, -2.0 * double(i) / double(d));
   double s, c;
   sincos(delta * w, &s, &c);
@@ -35,7 +31,24 @@ __global__ void rope_coeff_kernel(const rk_rope_run* __restrict__ runs, int n_ru
   const float s_hi = __uint_as_float(__float_as_uint(__double2float_rn(s)) & 0xFFFFFF00u);
   const float c_lo = __double2float_rn(c - double(c_hi));
   const float s_lo = __double2float_rn(s - double(s_hi));
-  coef[size_t(run) * (d / 2) + i] = make_float4(c_hi, c_lo, s_hi, s_lo);
+  return make_float4(c_hi, c_lo, s_hi, s_lo);
+}
+
+__global__ void rope_coeff_kernel(const rk_rope_run* __restrict__ runs, int n_runs, int d,
+                                  double theta, float4* __restrict__ coef) {
+  const int run = blockIdx.x;
+  const int i = threadIdx.x;
+  if (run >= n_runs || i >= d / 2) return;
+  const rk_rope_run r = runs[run];
+  coef[size_t(run) * (d / 2) + i] = rope_coeff(double((long long)r.pos_on0 - (long long)r.pos_off0), i, d, theta);
+}
+
+__global__ void rope_coeff_delta_kernel(const int32_t* __restrict__ deltas, int n, int d, double theta,
+                                        float4* __restrict__ coef) {
+  const int r = blockIdx.x;
+  const int i = threadIdx.x;
+  if (r >= n || i >= d / 2) return;
+  coef[size_t(r) * (d / 2) + i] = rope_coeff(double(deltas[r]), i, d, theta);
 }
 
 __device__ __forceinline__ void st_stream(void* p, uint4 v) {
@@ -46,16 +59,6 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
 __device__ __forceinline__ float u32_elem(const uint4& v, int k) {
   const uint32_t w = (k >> 1) == 0 ? v.x : (k >> 1) == 1 ? v.y : (k >> 1) == 2 ? v.z : v.w;
   return (k & 1) ? bf16hi(w) : bf16lo(w);
-}
-
-// Rotation of one pair with split coefficients; see the file comment.
-__device__ __forceinline__ void rotate_pair(float xa, float xb, const float4& cf, float& ya, float& yb) {
-  const float hi_a = fmaf(xa, cf.x, -(xb * cf.z));   // xa*c_hi - xb*s_hi (both products exact)
-  const float lo_a = fmaf(xa, cf.y, -(xb * cf.w));
-  const float hi_b = fmaf(xa, cf.z, xb * cf.x);      // xa*s_hi + xb*c_hi
-  const float lo_b = fmaf(xa, cf.w, xb * cf.y);
-  ya = hi_a + lo_a;
-  yb = hi_b + lo_b;
 }
 
 // Kernel 2 is persistent (two CTAs per SM).  The runs' tokens are cut into blocks of kRows
@@ -345,6 +348,12 @@ cudaError_t launch_apply(const rk_rope_args& a, const float4* coef, cudaStream_t
 
 }  // namespace
 
+
+cudaError_t launch_rope_coefficients(const int32_t* deltas, int n, int d, double theta, void* coef,
+                                     cudaStream_t stream) {
+  rope_coeff_delta_kernel<<<n, d / 2, 0, stream>>>(deltas, n, d, theta, static_cast<float4*>(coef));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope(const rk_rope_args& a, void* workspace, cudaStream_t stream) {
   if (a.n_runs == 0) return cudaSuccess;

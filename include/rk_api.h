@@ -132,6 +132,17 @@ RK_API size_t rk_rope_workspace_size(int32_t n_runs, int32_t d);
 RK_API rk_status rk_rope_reposition(const rk_rope_args* args, void* workspace, size_t workspace_bytes,
                              rk_stream_t stream);
 
+/* Rotation coefficients for repositioning on load (rk_attn_args.k_rot): row r of `coef`
+ * (device, fp32 [n][d/2][4], 16-byte aligned, caller-owned) describes the turn by deltas[r]
+ * (online minus offline position, device int32 [n]): for pair i, cos and sin of
+ * deltas[r] * theta^(-2i/d) in double precision, each split into a head with 16 significant
+ * bits and an fp32 tail -- exactly the values rk_rope_reposition computes for a run with
+ * that delta, so that rotating on load gives the same bf16 K.  Errors: RK_ERR_INVALID_ARG
+ * (n < 0, NULL or misaligned pointers with n > 0, theta <= 1 or not finite),
+ * RK_ERR_UNSUPPORTED (d, n > 65535), RK_ERR_CUDA. */
+RK_API rk_status rk_rope_coefficients(const int32_t* deltas, int32_t n, int32_t d, double theta, void* coef,
+                                      rk_stream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * SegPagedAttention
  *
@@ -178,14 +189,34 @@ typedef struct rk_attn_args {
                                   position seq_len[b] - 1, stored into its page slot before the
                                   keys are read (as rk_append_kv would, within the same kernel) */
   const void* v_new;           /* decode only, or NULL: bf16 [B][Hkv][d], its V; both or neither */
+  const int32_t* k_rot;        /* or NULL: int32 [B*Hkv][max_pages], per listed entry the row of
+                                  rot_coef whose turn is applied to that page's K rows as they are
+                                  read (repositioning on load), or -1 for none */
+  const void* rot_coef;        /* with k_rot: fp32 [n_rot][d/2][4] from rk_rope_coefficients, 16-byte aligned */
+  int32_t n_rot;               /* with k_rot: rows of rot_coef; an entry outside [-1, n_rot) is skipped
+                                  (K used unturned) and reported as RK_ERR_DEVICE_BOUNDS */
+  int32_t rot_style;           /* with k_rot: RK_ROPE_HALF_SPLIT or RK_ROPE_INTERLEAVED */
 } rk_attn_args;
 
+/* Repositioning on load ("RedKnot" article, RoPE and SegPagedAttention paragraphs): with
+ * k_rot, a page of a reusable segment can be listed as it was cached offline -- its K still
+ * turned by the offline positions -- and the kernels turn each of its K rows by the entry's
+ * coefficient row before use.  With coefficients from rk_rope_coefficients for delta = online
+ * minus offline position, the K the kernels use is bit for bit the bf16 K that
+ * rk_rope_reposition would have written, so the attention output is the same as repositioning
+ * first; no repositioned copy is written.  All tokens of such a page must share the delta
+ * (segments that start on a page boundary of both the offline and the online positions).
+ * Decode only: rk_segpaged_prefill returns RK_ERR_UNSUPPORTED for a non-NULL k_rot -- a
+ * prefill reads every K tile once per query tile and is bound by the tensor cores, so it
+ * reads pages repositioned once by rk_rope_reposition instead; decode reads each K row once
+ * and is bound by memory, so the turn costs no time there. */
+
 /* The table and length arrays (cu_seqlens_q, seq_len, page_table, page_logical, n_pages,
- * head_class, window, sink) were written by work that completed before the kernel
- * preceding this call on `stream` began -- e.g. copied once at the start of a decode
- * step, before the layers run.  The decode kernel then plans its work from them while
- * that kernel is still finishing, and waits for it only before reading q and the pools
- * and before writing.  Without the flag nothing is read before the preceding work has
+ * head_class, window, sink, k_rot) were written by work that completed before the kernel
+ * preceding this call on `stream` began, or by an rk_ring_advance earlier on the stream --
+ * e.g. copied or advanced once at the start of a decode step, before the layers run.  The
+ * decode kernel then plans its work from them while that kernel is still finishing, and
+ * waits for it only before reading q and the pools and before writing.  Without the flag nothing is read before the preceding work has
  * completed.  Ignored by prefill. */
 #define RK_ATTN_METADATA_STABLE 1
 
@@ -254,10 +285,11 @@ RK_API rk_status rk_segpaged_decode_noalloc(const rk_attn_args* args, rk_stream_
  * follow "PagedAttention & RadixAttention", section "The Solution: Fixed-size blocks":
  * a token at position j lives in slot j % P of the page listed for logical page j / P.
  *
- * A decode step, per layer: rk_append_kv writes the new token's K and V, then
- * rk_segpaged_decode attends to them.  Once per step, before the layers (so that the
- * tables count as written before the layers' kernels, RK_ATTN_METADATA_STABLE), the
- * tables of window-only local heads are advanced with rk_ring_advance.
+ * A decode step, per layer: rk_append_kv writes the new token's K and V (or the decode call
+ * does, with k_new / v_new), then rk_segpaged_decode attends to them.  Once per step, before
+ * the layers, the tables of window-only local heads are advanced with rk_ring_advance.  No
+ * kernel enqueued after rk_ring_advance starts before it has completed, so the decode calls
+ * that follow it may pass RK_ATTN_METADATA_STABLE.
  * ------------------------------------------------------------------------------------ */
 typedef struct rk_append_args {
   const void* k_new;           /* bf16 [B][Hkv][d], the new token's K per head segment */
@@ -307,6 +339,43 @@ typedef struct rk_ring_args {
  * that is not full or whose oldest page is still inside the window, or n_pages outside
  * [1, max_pages], leaves that head segment unchanged and sets RK_ERR_DEVICE_BOUNDS. */
 RK_API rk_status rk_ring_advance(const rk_ring_args* args, rk_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Token-level sparse FFN
+ *
+ * "小红书 RedKnot", section 3, third component (elastic / sparse FFN): the tokens are ranked
+ * by their attention importance and only the `keep` most important go through the
+ * feed-forward network; the others skip it (their FFN output is zero, so a residual add
+ * leaves them as they were).  The FFN is the gated form of the Qwen / Llama models the
+ * pages evaluate:  FFN(x) = W_down (silu(W_gate x) * (W_up x)),  silu(g) = g / (1 + e^-g).
+ *
+ *   kept = the `keep` tokens with the largest importance (equal scores: the lower token
+ *          index first; NaN ranks below every number), in ascending token order
+ *   out[t][:] = FFN(x[t])  for t in kept,   0 otherwise                            (bf16)
+ * Accumulation is fp32; the gated activation is rounded to bf16 before W_down.
+ * ------------------------------------------------------------------------------------ */
+typedef struct rk_sparse_ffn_args {
+  const void* x;             /* bf16 [T][d_model] */
+  const float* importance;   /* fp32 [T] */
+  int32_t T, d_model, d_ff;
+  int32_t keep;              /* tokens that go through the FFN, 0 <= keep <= T */
+  const void* w_gate;        /* bf16 [d_ff][d_model] */
+  const void* w_up;          /* bf16 [d_ff][d_model] */
+  const void* w_down;        /* bf16 [d_model][d_ff] */
+  void* out;                 /* bf16 [T][d_model], written whole */
+  int32_t* kept;             /* int32 [keep], written */
+  int32_t* status;           /* optional device int32 error word, may be NULL */
+} rk_sparse_ffn_args;
+
+/* Workspace bytes: the gathered rows and the activation ([keep][d_model] + [keep][d_ff] bf16). */
+RK_API size_t rk_sparse_ffn_workspace_size(const rk_sparse_ffn_args* args);
+
+/* Errors: RK_ERR_INVALID_ARG (NULL pointers, sizes out of range, pointers not 16-byte
+ * aligned), RK_ERR_UNSUPPORTED (d_model not a multiple of 256, d_ff not a multiple of 128,
+ * T above 65536), RK_ERR_WORKSPACE, RK_ERR_CUDA; a wait that exceeds its limit sets
+ * RK_ERR_TIMEOUT in *status. */
+RK_API rk_status rk_sparse_ffn(const rk_sparse_ffn_args* args, void* workspace, size_t workspace_bytes,
+                               rk_stream_t stream);
 
 /* Static text for a status code. */
 RK_API const char* rk_status_string(rk_status status);

@@ -38,6 +38,9 @@ What it computes, and where the pages state it:
   new token's K/V go to slot pos % P of the page listed for logical page pos // P; a
   window-only local head reuses the page of its oldest window entry once the window has
   left it (append_rows, ring_advance).
+* Token-level sparse FFN ("小红书 RedKnot" section 3, third component): the tokens of
+  highest attention importance go through the gated FFN, the others skip it
+  (select_tokens, gated_ffn, sparse_ffn).
 
 Readings of silent points are listed in the repository's design notes; the
 pins that tie each function to something other than itself live in
@@ -360,3 +363,43 @@ def ring_advance(page_table: np.ndarray, page_logical: np.ndarray, n_pages: np.n
         lg[s, :n] = [x[0] for x in new]
         tab[s, :n] = [x[1] for x in new]
     return tab, lg
+
+
+# ----------------------------------------------------------------------------- sparse FFN
+# "小红书 RedKnot", section 3, third component: tokens ranked by attention importance; only
+# the most important go through the FFN, the others skip it.  The FFN is the gated form of
+# the Qwen / Llama models the pages evaluate.
+def silu(g: np.ndarray) -> np.ndarray:
+    """g * sigmoid(g) = g / (1 + e^-g), in float64."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def select_tokens(importance: np.ndarray, keep: int) -> np.ndarray:
+    """The `keep` tokens with the largest importance (equal scores: lower index first; NaN
+    below every number), in ascending token order."""
+    imp = np.asarray(importance, dtype=np.float64)
+    key = np.where(np.isnan(imp), -np.inf, imp)
+    idx = np.arange(len(imp))
+    nan_last = np.isnan(imp).astype(np.int64)
+    order = np.lexsort((idx, nan_last, -key))        # by score descending, NaN after, then index
+    return np.sort(order[:keep])
+
+
+def gated_ffn(x: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray) -> np.ndarray:
+    """W_down (silu(W_gate x) * (W_up x)) for each row x, all in float64."""
+    g = x @ w_gate.T
+    u = x @ w_up.T
+    return (silu(g) * u) @ w_down.T
+
+
+def sparse_ffn(x_bits, importance, keep, w_gate_bits, w_up_bits, w_down_bits, rows=None):
+    """(kept tokens, {token: FFN output row in float64}) for the kept tokens in `rows` (all
+    kept tokens when rows is None); every other token's output is zero."""
+    kept = select_tokens(importance, keep)
+    want = kept if rows is None else np.array([t for t in rows if t in set(kept.tolist())], dtype=np.int64)
+    if len(want) == 0:
+        return kept, {}
+    y = gated_ffn(bf16_to_f64(x_bits[want]), bf16_to_f64(w_gate_bits), bf16_to_f64(w_up_bits),
+                  bf16_to_f64(w_down_bits))
+    return kept, {int(t): y[i] for i, t in enumerate(want)}

@@ -12,7 +12,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 ATTN_FIELDS = ["q", "cu_seqlens_q", "seq_len", "k_pool", "v_pool", "n_pool_pages", "page_table", "page_logical",
                "n_pages", "head_class", "window", "sink", "B", "Hq", "Hkv", "d", "P", "max_pages", "total_q", "max_q",
-               "scale", "out", "lse", "status", "flags", "k_new", "v_new"]
+               "scale", "out", "lse", "status", "flags", "k_new", "v_new", "k_rot", "rot_coef", "n_rot", "rot_style"]
 APPEND_FIELDS = ["k_new", "v_new", "pos", "k_pool", "v_pool", "n_pool_pages", "page_table", "page_logical", "n_pages",
                  "B", "Hkv", "d", "P", "max_pages", "status"]
 RING_FIELDS = ["pos", "page_table", "page_logical", "n_pages", "ring", "window", "sink", "B", "Hkv", "P", "max_pages",

@@ -216,3 +216,78 @@ def test_decode_with_appends_over_recycled_pages(rk, flags, fused):
                                         seq_len=pos + 1, k_pool=k_host, v_pool=v_host, page_table=tab,
                                         page_logical=lg, n_pages=wl.dec_n_pages)
             _compare(batch, out.float().cpu().numpy(), lse.cpu().numpy())
+
+
+# ------------------------------------------------------------------------- repositioning on load
+@pytest.mark.parametrize("style", [0, 1])
+def test_decode_repositions_on_load_bit_identically(rk, style):
+    """Decode over the offline pages with their turn applied as they are read (k_rot with
+    rk_rope_coefficients) gives, bit for bit, the output of rk_rope_reposition followed by
+    decode over the repositioned pages; and it matches the oracle ("RedKnot" article, RoPE
+    and SegPagedAttention paragraphs: cached K turned back and forward, pages read per head)."""
+    layer = next(l for l, c in enumerate(synth.stack_classes()) if 0 in c)     # holds a global head
+    wl = synth.stack_layer(layer, n_segments=5, seg_tokens=1024, n_suffix=100, n_decode=6)
+    if style:
+        wl.rope.style = 1
+    a = wl.attn
+    view = synth.reposition_on_load_view(wl)
+    st = _status()
+    # path A: reposition, then decode
+    kp_a = to_device(a.k_pool, "cuda")
+    rope_to_device(wl.rope, "cuda").run(rk, kp_a, status=st)
+    # path B: the offline pages, turned on load
+    kp_b = to_device(view.k_pool, "cuda")
+    coef = rk.rope_coefficients(to_device(view.deltas, "cuda"), a.d, wl.theta)
+    k_rot = to_device(view.dec_k_rot, "cuda")
+    r = wl.rope
+    written = O.paged_rope_reposition(r.k_src, r.src_tables, r.dst_tables, r.runs, wl.theta, r.P, r.style)
+    k_host, v_host = O.apply_rope_to_pool(a.k_pool, written), a.v_pool
+    paths = {}
+    for name, kp in (("A", kp_a), ("B", kp_b)):
+        dv = _ring_args_dev(rk, wl, st)
+        vp = to_device(a.v_pool, "cuda")
+        cls, win, sink = (to_device(x, "cuda") for x in (a.head_class, a.window, a.sink))
+        ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+        outs = []
+        for s in range(wl.decode_k.shape[0]):
+            pos = (a.seq_len + s).astype(np.int32)
+            pos_d, seq = to_device(pos, "cuda"), to_device(pos + 1, "cuda")
+            rk.ring_advance(rk.ring_args(pos_d, dv["tab"], dv["lg"], dv["n"], dv["ring"], dv["window"], dv["sink"],
+                                         Hkv=a.Hkv, P=a.P, status=st))
+            out = torch.empty((a.B, a.Hq, a.d), dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty((a.B, a.Hq), dtype=torch.float32, device="cuda")
+            extra = dict(k_rot=k_rot, rot_coef=coef, rot_style=style) if name == "B" else {}
+            rk.segpaged_decode(rk.attn_args(to_device(wl.decode_q[s], "cuda"), seq, kp, vp, dv["tab"], dv["lg"],
+                                            dv["n"], cls, win, sink, out, lse=lse, status=st, total_q=a.B, max_q=1,
+                                            flags=1, k_new=to_device(wl.decode_k[s], "cuda"),
+                                            v_new=to_device(wl.decode_v[s], "cuda"), **extra), workspace=ws)
+            outs.append((out, lse))
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        paths[name] = [(o.view(torch.int16).cpu().numpy(), l.cpu().numpy()) for o, l in outs]
+    for (oa, la), (ob, lb) in zip(paths["A"], paths["B"]):
+        assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+    # and against the oracle at the last step
+    tab, lg = wl.dec_page_table, wl.dec_page_logical
+    for s in range(wl.decode_k.shape[0]):
+        pos = (a.seq_len + s).astype(np.int32)
+        tab, lg = O.ring_advance(tab, lg, wl.dec_n_pages, wl.ring, a.window, a.sink, pos, a.Hkv, a.P)
+        k_host, v_host = O.append_rows(k_host, v_host, tab, lg, wl.dec_n_pages, pos, wl.decode_k[s], wl.decode_v[s],
+                                       a.Hkv, a.P)
+    batch = dataclasses.replace(a, q=wl.decode_q[s], cu_seqlens_q=np.arange(a.B + 1, dtype=np.int32), seq_len=pos + 1,
+                                k_pool=k_host, v_pool=v_host, page_table=tab, page_logical=lg, n_pages=wl.dec_n_pages)
+    ob, lb = paths["B"][-1]
+    _compare(batch, ob.view(np.uint16).astype(np.uint32).__lshift__(16).view(np.float32), lb)
+
+
+def test_prefill_rejects_repositioning_on_load(rk):
+    w = synth.tiny_prefill()
+    from workloads.device import attn_to_device
+    da = attn_to_device(w.attn, "cuda")
+    coef = torch.zeros((1, 32, 4), dtype=torch.float32, device="cuda")
+    k_rot = torch.full(tuple(w.attn.page_table.shape), -1, dtype=torch.int32, device="cuda")
+    args = da.args(rk)
+    args.k_rot, args.rot_coef, args.n_rot = k_rot.data_ptr(), coef.data_ptr(), 1
+    with pytest.raises(rk.RkError) as e:
+        rk.segpaged_prefill(args)
+    assert e.value.code == 2

@@ -392,3 +392,59 @@ def test_ring_keeps_every_window_visible_over_a_long_decode():
                 if j in written:
                     e = int(np.searchsorted(lg[0], j // P))
                     assert k[tab[0, e], j % P, 0] == written[j]
+
+
+# ------------------------------------------------------------------ sparse FFN
+@pytest.mark.parametrize("case", _load("token_selection.json")["cases"])
+def test_token_selection_hand_cases(case):
+    imp = np.array([float(v) for v in case["importance"]], dtype=np.float32)
+    assert O.select_tokens(imp, case["keep"]).tolist() == case["kept"]
+
+
+def test_token_selection_brute_force():
+    # against every subset of the right size: the chosen one has the largest sorted scores,
+    # and among equal ones the lexicographically smallest index set
+    import itertools
+    rng = np.random.default_rng(21)
+    for _ in range(200):
+        T = int(rng.integers(1, 8))
+        imp = rng.integers(0, 4, T).astype(np.float32)          # many ties
+        keep = int(rng.integers(0, T + 1))
+        best = max(itertools.combinations(range(T), keep),
+                   key=lambda c: (sorted(imp[list(c)].tolist(), reverse=True), [-i for i in c]))
+        assert O.select_tokens(imp, keep).tolist() == list(best)
+
+
+def test_silu_closed_forms():
+    x = np.array([-30.0, -2.0, -0.5, 0.0, 0.5, 2.0, 30.0])
+    y = O.silu(x)
+    assert y[3] == 0.0 and abs(y[-1] - 30.0) < 1e-10 and abs(y[0]) < 1e-10
+    assert np.allclose(O.silu(-x), y - x, atol=1e-11)   # silu(-x) = silu(x) - x (cancels near x = 30)
+    assert abs(O.silu(np.array([1.0]))[0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+
+
+def test_gated_ffn_hand_example():
+    # d_model 2, d_ff 1: g = x . (1, 0) = 1, u = x . (0, 1) = 2, a = silu(1) * 2, y = (a, 2a)
+    x = np.array([[1.0, 2.0]])
+    y = O.gated_ffn(x, np.array([[1.0, 0.0]]), np.array([[0.0, 1.0]]), np.array([[1.0], [2.0]]))
+    a = 2.0 / (1.0 + math.exp(-1.0))
+    assert np.allclose(y, [[a, 2 * a]], atol=1e-15)
+
+
+def test_gated_ffn_matches_torch():
+    rng = np.random.default_rng(22)
+    x, wg, wu, wd = (rng.standard_normal(s) for s in ((5, 16), (24, 16), (24, 16), (16, 24)))
+    t = torch.from_numpy
+    ref = (torch.nn.functional.silu(t(x) @ t(wg).T) * (t(x) @ t(wu).T)) @ t(wd).T
+    assert np.allclose(O.gated_ffn(x, wg, wu, wd), ref.numpy(), atol=1e-12)
+
+
+def test_sparse_ffn_is_the_dense_ffn_on_kept_rows_and_zero_elsewhere():
+    w = synth.sparse_ffn_workload(T=40, d_model=16, d_ff=32, keep_frac=0.3)
+    kept, rows = O.sparse_ffn(w.x, w.importance, w.keep, w.w_gate, w.w_up, w.w_down)
+    dense = O.gated_ffn(O.bf16_to_f64(w.x), O.bf16_to_f64(w.w_gate), O.bf16_to_f64(w.w_up), O.bf16_to_f64(w.w_down))
+    assert len(kept) == w.keep and set(rows) == set(kept.tolist())
+    for t, y in rows.items():
+        assert np.array_equal(y, dense[t]) or np.allclose(y, dense[t], atol=1e-12)
+    top = np.argsort(-w.importance.astype(np.float64), kind="stable")[:w.keep]
+    assert sorted(top.tolist()) == kept.tolist()

@@ -137,6 +137,7 @@ class RopeJob:
     P: int
     d: int
     style: int = 0             # 0 half-split pairs (i, i+d/2), 1 interleaved (2i, 2i+1)
+    run_seg: Optional[np.ndarray] = None   # int32 [n_runs] head segment (b*Hkv + h) of each run
 
     @property
     def n_runs(self) -> int:
@@ -324,10 +325,12 @@ def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, wi
                 src_list.append((b, h, pos_on0, n, npg))
                 n_src_pages += npg
         src_alloc = _PageAllocator(rng, n_src_pages)
+        run_seg = []
         for (b, h, pos_on0, n, npg) in src_list:
             pages = src_alloc.take(npg)
             src_tabs.append(pages)
             runs.append([src_off, npg, dst_index[(b, h)], len(storage[b * Hkv + h]), 0, pos_on0, n, 0])
+            run_seg.append(b * Hkv + h)
             src_off += npg
         k_src = _normal_bf16(rng, (max(n_src_pages, 1), P, d))
         if k_scale is not None:
@@ -339,10 +342,11 @@ def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, wi
         if local_window_only:
             # a window-only local head repositions only the tokens it stores: the run is cut
             # to the stored logical pages (sink pages, then the window pages)
-            cut = []
+            cut, cut_seg = [], []
             for r, (b, h, pos_on0, n, npg) in zip(runs, src_list):
                 if int(classes[b][h]) != LOCAL:
                     cut.append(r)
+                    cut_seg.append(b * Hkv + h)
                     continue
                 st = stored[b * Hkv + h]
                 lo_s, hi_s = pos_on0, pos_on0 + n
@@ -350,12 +354,13 @@ def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, wi
                     x0, x1 = max(lo_s, a0 * P), min(hi_s, a1 * P)
                     if x0 < x1:
                         cut.append([r[0], r[1], r[2], r[3], x0 - pos_on0, x0, x1 - x0, 0])
-            runs = cut
+                        cut_seg.append(b * Hkv + h)
+            runs, run_seg = cut, cut_seg
         rope = RopeJob(k_src=k_src,
                        src_tables=np.concatenate(src_tabs).astype(np.int32) if src_tabs else np.zeros(1, np.int32),
                        dst_tables=np.concatenate(dst_tabs).astype(np.int32),
                        runs=np.asarray(runs, dtype=np.int32).reshape(-1, RUN_FIELDS),
-                       theta=theta, P=P, d=d, style=style)
+                       theta=theta, P=P, d=d, style=style, run_seg=np.asarray(run_seg, dtype=np.int32))
 
     decode_q = None
     if n_decode:
@@ -385,6 +390,58 @@ def _build(name, rng, *, B, Hq, Hkv, d, P, theta, ctx_len, n_suffix, classes, wi
                 ring[i] = R
         wl.dec_page_table, wl.dec_page_logical, wl.dec_n_pages, wl.ring = tab, lg, nn, ring
     return wl
+
+
+@dataclasses.dataclass
+class OnLoadView:
+    """Inputs of attention that repositions K as it reads it (zero-copy reuse): the K pool
+    with every repositioned page holding its offline rows instead, the per-entry coefficient
+    rows (k_rot, -1 for pages read as they are) of the prefill and decode tables, and the
+    delta of each coefficient row."""
+    k_pool: np.ndarray          # uint16 [n_pages][P][d]
+    deltas: np.ndarray          # int32 [n_rot]: online minus offline position
+    k_rot: np.ndarray           # int32 [B*Hkv][max_pages] for attn.page_logical
+    dec_k_rot: Optional[np.ndarray] = None   # int32 for dec_page_logical
+
+
+def reposition_on_load_view(wl: Workload) -> OnLoadView:
+    """Rearrange a workload for repositioning on load: each page a RoPE run writes gets the
+    offline page the run reads (bits copied, no arithmetic), and the entries listing it get
+    the run's coefficient row.  Runs must start on a page boundary of both positions and
+    fill whole pages (a page holds one run's tokens)."""
+    r, a, P = wl.rope, wl.attn, wl.rope.P
+    k_pool = np.array(a.k_pool, copy=True)
+    deltas, row_of = [], {}
+    page_rot = {}                                   # (segment, logical page) -> coefficient row
+    for run, seg in zip(r.runs, r.run_seg):
+        s_off, s_len, d_off, d_len, p_off0, p_on0, n = (int(x) for x in run[:7])
+        if p_off0 % P or p_on0 % P:
+            raise ValueError("a run starts inside a page")
+        delta = p_on0 - p_off0
+        if delta not in row_of:
+            row_of[delta] = len(deltas)
+            deltas.append(delta)
+        for j in range(_cdiv(n, P)):
+            rows = min(P, n - j * P)
+            if rows < P:   # the rest of the page holds other tokens, which must not be turned
+                raise ValueError("a run ends inside a page")
+            dst = int(r.dst_tables[d_off + p_on0 // P + j])
+            src = int(r.src_tables[s_off + p_off0 // P + j])
+            k_pool[dst, :rows] = r.k_src[src, :rows]
+            page_rot[(int(seg), p_on0 // P + j)] = row_of[delta]
+
+    def rot_table(logical, n_pages):
+        out = np.full(logical.shape, -1, dtype=np.int32)
+        for s in range(logical.shape[0]):
+            for e in range(int(n_pages[s])):
+                out[s, e] = page_rot.get((s, int(logical[s, e])), -1)
+        return out
+
+    view = OnLoadView(k_pool=k_pool, deltas=np.asarray(deltas, dtype=np.int32),
+                      k_rot=rot_table(a.page_logical, a.n_pages))
+    if wl.dec_page_logical is not None:
+        view.dec_k_rot = rot_table(wl.dec_page_logical, wl.dec_n_pages)
+    return view
 
 
 def _page_ranges(pages) -> List:
@@ -535,3 +592,32 @@ WORKLOADS = {
     "stack_layer": stack_layer,
     "mixed_classes": mixed_classes,
 }
+
+
+@dataclasses.dataclass
+class FfnWorkload:
+    """Inputs of one sparse FFN call: token rows, importance scores and synthetic weights."""
+    x: np.ndarray              # uint16 [T][d_model]
+    importance: np.ndarray     # float32 [T]
+    w_gate: np.ndarray         # uint16 [d_ff][d_model]
+    w_up: np.ndarray           # uint16 [d_ff][d_model]
+    w_down: np.ndarray         # uint16 [d_model][d_ff]
+    keep: int
+
+
+def sparse_ffn_workload(seed: int = 1006, T: int = 4096, d_model: int = 5120, d_ff: int = 25600,
+                        keep_frac: float = 0.5, ties: bool = False) -> FfnWorkload:
+    """Token rows x ~ N(0, 1), weights ~ N(0, 1/fan_in) (so that activations stay of order
+    one), importance ~ LogNormal(0, 1) per token -- a stand-in for attention mass, which is
+    positive and heavy-tailed; with `ties`, scores are rounded to 1/8 so that many are equal.
+    Shapes default to the Qwen3-32B feed-forward block (d_model 5120, d_ff 25600) over a
+    4096-token segment, half of it kept."""
+    rng = np.random.default_rng(seed)
+    x = _normal_bf16(rng, (T, d_model))
+    w_gate = _normal_bf16(rng, (d_ff, d_model), scale=np.float32(1.0 / np.sqrt(d_model)))
+    w_up = _normal_bf16(rng, (d_ff, d_model), scale=np.float32(1.0 / np.sqrt(d_model)))
+    w_down = _normal_bf16(rng, (d_model, d_ff), scale=np.float32(1.0 / np.sqrt(d_ff)))
+    imp = np.exp(rng.standard_normal(T)).astype(np.float32)
+    if ties:
+        imp = (np.round(imp * 8) / 8).astype(np.float32)
+    return FfnWorkload(x=x, importance=imp, w_gate=w_gate, w_up=w_up, w_down=w_down, keep=int(round(keep_frac * T)))
