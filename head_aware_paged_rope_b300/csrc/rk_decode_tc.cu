@@ -624,9 +624,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         if (present && !page_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
         const int pidv = page_ok ? raw_page : -1;
         const int lpv = page_ok ? raw_lp : -1;
-        const bool rot_ok = raw_rot >= -1 && raw_rot < p.n_rot;
-        if (page_ok && !rot_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
-        const int rotv = page_ok && rot_ok ? raw_rot : -1;
+        int rotv = -1;
+        if constexpr (ROT) {
+          const bool rot_ok = raw_rot >= -1 && raw_rot < p.n_rot;
+          if (page_ok && !rot_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
+          rotv = page_ok && rot_ok ? raw_rot : -1;
+        }
         const int tiles = min(tpg, po.n_kt - grp * tpg);
         for (int jt = 0; jt < tiles; ++jt, ++gg) {
           const int st = gg % NS;
@@ -635,7 +638,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           for (int pg = 0; pg < 8; ++pg) {
             lps[pg] = __shfl_sync(0xffffffffu, lpv, (jt * EPT + pg) & 31);
             pids[pg] = __shfl_sync(0xffffffffu, pidv, (jt * EPT + pg) & 31);
-            rots[pg] = __shfl_sync(0xffffffffu, rotv, (jt * EPT + pg) & 31);
+            rots[pg] = ROT ? __shfl_sync(0xffffffffu, rotv, (jt * EPT + pg) & 31) : -1;
           }
           // the segment's last tile holds the query position, where the new token goes
           int app_r = -1;
@@ -655,13 +658,16 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
             if (got) {
 #pragma unroll
               int any = 0;
+#pragma unroll
               for (int pg = 0; pg < 8; ++pg) {
                 sh.lp[st][pg] = pg < EPT ? lps[pg] : -1;
                 sh.pid[st][pg] = pg < EPT ? pids[pg] : -1;
-                sh.rot[st][pg] = pg < EPT ? rots[pg] : -1;
-                any |= (pg < EPT && rots[pg] >= 0) ? 1 : 0;
+                if constexpr (ROT) {
+                  sh.rot[st][pg] = pg < EPT ? rots[pg] : -1;
+                  any |= (pg < EPT && rots[pg] >= 0) ? 1 : 0;
+                }
               }
-              sh.any_rot[st] = any;
+              if constexpr (ROT) sh.any_rot[st] = any;
               sh.cmd[st] = 1;
               sh.app_row[st] = app_r;
               sh.app_seg[st] = po.seg;
@@ -775,27 +781,28 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       if (!wait_or_abort(sh, smem_addr(&sh.desc_full[st]), (gg / NS) & 1)) break;
       const int cmd = sh.cmd[st];
       if (cmd == 0) break;
+      // the new token (row app_r, if this stage holds it) is copied from k_new / v_new
       const int app_r = sh.app_row[st];
+      const int64_t noff = int64_t(sh.app_seg[st]) * (D * 2) + c16 * 16;
+      const char* kn = reinterpret_cast<const char*>(p.k_new) + noff;
+      const char* vn = reinterpret_cast<const char*>(p.v_new) + noff;
 #pragma unroll
       for (int i = 0; i < 32 / RPI; ++i) {
         const int r = cw * 32 + i * RPI + rsub;       // key of the tile
         const int pid = sh.pid[st][r >> pshift];
         const uint32_t doff = st * LY::kStageBytes + half * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4);
         const int64_t soff = pid >= 0 ? ((int64_t(pid) << pshift) + (r & (P - 1))) * (D * 2) + c16 * 16 : 0;
-        const uint32_t nb = pid >= 0 ? 16u : 0u;
-        if (r == app_r) {
-          // the new token: copied from k_new / v_new, and stored into its pool slot for later steps
-          const int64_t noff = int64_t(sh.app_seg[st]) * (D * 2) + c16 * 16;
-          const char* kn = reinterpret_cast<const char*>(p.k_new) + noff;
-          const char* vn = reinterpret_cast<const char*>(p.v_new) + noff;
-          cp_async16(sK + doff, kn, 16u);
-          cp_async16(sV + doff, vn, 16u);
-          *reinterpret_cast<uint4*>(const_cast<char*>(kb) + soff) = __ldg(reinterpret_cast<const uint4*>(kn));
-          *reinterpret_cast<uint4*>(const_cast<char*>(vb) + soff) = __ldg(reinterpret_cast<const uint4*>(vn));
-        } else {
-          cp_async16(sK + doff, kb + soff, nb);
-          cp_async16(sV + doff, vb + soff, nb);
-        }
+        const bool app = r == app_r;
+        const uint32_t nb = (pid >= 0 || app) ? 16u : 0u;
+        cp_async16(sK + doff, app ? kn : kb + soff, nb);
+        cp_async16(sV + doff, app ? vn : vb + soff, nb);
+      }
+      if (app_r >= 0 && app_r / 32 == cw && (app_r % 32) % RPI == rsub) {
+        // and stored into its pool slot for the later steps (the lanes that copied that row)
+        const int pid = sh.pid[st][app_r >> pshift];
+        const int64_t soff = ((int64_t(pid) << pshift) + (app_r & (P - 1))) * (D * 2) + c16 * 16;
+        *reinterpret_cast<uint4*>(const_cast<char*>(kb) + soff) = __ldg(reinterpret_cast<const uint4*>(kn));
+        *reinterpret_cast<uint4*>(const_cast<char*>(vb) + soff) = __ldg(reinterpret_cast<const uint4*>(vn));
       }
       if constexpr (ROT) {
         asm volatile("cp.async.commit_group;" ::: "memory");
