@@ -52,7 +52,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cases", action="store_true", help="skip the decode-microbenchmark and layer-prefill parts")
-    ap.add_argument("--case", choices=["rag_prefill", "stack_prefill", "decode_microbench", "stack_decode", "rag_rope"],
+    ap.add_argument("--case", choices=["rag_prefill", "stack_prefill", "decode_microbench", "stack_decode", "rag_rope",
+                                       "sparse_ffn"],
                     help="run one call of one workload --steps times (for profiling) instead of the step")
     ap.add_argument("--layer", type=int, default=None,
                     help="with --case stack_*: the layer (default: the first layer holding a global head)")
@@ -315,7 +316,8 @@ class LayerState:
                 head_class=da.head_class.data_ptr(), window=da.window.data_ptr(), sink=da.sink.data_ptr(), B=1,
                 Hq=a.Hq, Hkv=a.Hkv, d=a.d, P=a.P, max_pages=tab.shape[1], total_q=1, max_q=1, scale=0.0,
                 out=self.dec_out[s].data_ptr(), lse=self.dec_lse[s].data_ptr(), status=self.status.data_ptr(),
-                flags=rk.RK_ATTN_METADATA_STABLE, k_new=self.dec_k[s].data_ptr(), v_new=self.dec_v[s].data_ptr()))
+                flags=rk.RK_ATTN_METADATA_STABLE | rk.RK_ATTN_POOLS_STABLE, k_new=self.dec_k[s].data_ptr(),
+                v_new=self.dec_v[s].data_ptr()))
         self.dec_ws = torch.zeros(max(1, rk.segpaged_decode_workspace_size(self.dec_args[0])), dtype=torch.uint8,
                                   device=dev)
 
@@ -516,6 +518,37 @@ def time_masked_comparison(torch, rk, dev, steps, warmup):
             "unmasked_path": "torch scaled_dot_product_attention is_causal=True on the same dense K/V"}
 
 
+def time_sparse_ffn(torch, rk, dev, steps, warmup):
+    """The token-level sparse FFN on the Qwen3-32B feed-forward block (d_model 5120, d_ff
+    25600) over a 4096-token segment, half the tokens kept: selection, gather, and the two
+    GEMMs.  FLOPs = 2 * keep * d_model * 3 d_ff (the three weight matrices)."""
+    from workloads import synth
+    from workloads.device import to_device
+    w = synth.sparse_ffn_workload()
+    x = to_device(w.x, dev)
+    out = torch.empty_like(x)
+    kept = torch.empty(w.keep, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    args = rk.sparse_ffn_args(x, torch.from_numpy(w.importance).to(dev), to_device(w.w_gate, dev),
+                              to_device(w.w_up, dev), to_device(w.w_down, dev), out, kept, keep=w.keep, status=st)
+    ws = torch.empty(int(rk.LIB.rk_sparse_ffn_workspace_size(ctypes.byref(args))), dtype=torch.uint8, device=dev)
+    for _ in range(max(warmup, 3)):
+        rk.sparse_ffn(args, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(5, steps // 5)
+    e0.record()
+    for _ in range(n):
+        rk.sparse_ffn(args, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ms = e0.elapsed_time(e1) / n
+    flops = 2 * w.keep * w.x.shape[1] * 3 * w.w_gate.shape[0]
+    return {"workload": f"Qwen3-32B FFN block (d_model 5120, d_ff 25600), {len(w.importance)} tokens, {w.keep} kept",
+            "ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "flops": flops}
+
+
 def time_cases(torch, rk, dev, steps, warmup):
     """The decode microbenchmark (one call) and the isolated 128K layer prefill, each timed
     like `--case` (calls captured in a graph, pools rotated past L2)."""
@@ -611,6 +644,8 @@ def ours_main(args, world, rank, local):
     parts["prefill"]["frac_bf16_sustained"] = parts["prefill"]["TFLOP/s"] / peaks["bf16_tflops_sustained"]
     if not args.no_cases:
         parts["masked_comparison"] = time_masked_comparison(torch, rk, dev, args.steps, args.warmup)
+        parts["sparse_ffn"] = time_sparse_ffn(torch, rk, dev, args.steps, args.warmup)
+        parts["sparse_ffn"]["frac_bf16_burst"] = parts["sparse_ffn"]["TFLOP/s"] / peaks["bf16_tflops"]
         for name, v in time_cases(torch, rk, dev, args.steps, args.warmup).items():
             if "GB/s" in v:
                 v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
@@ -712,6 +747,18 @@ def build_case(torch, rk, dev, case, layer):
     from workloads import synth
     from workloads.device import attn_to_device, rope_to_device, to_device
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    if case == "sparse_ffn":
+        w = synth.sparse_ffn_workload()
+        x = to_device(w.x, dev)
+        out = torch.empty_like(x)
+        kept = torch.empty(w.keep, dtype=torch.int32, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        args = rk.sparse_ffn_args(x, torch.from_numpy(w.importance).to(dev), to_device(w.w_gate, dev),
+                                  to_device(w.w_up, dev), to_device(w.w_down, dev), out, kept, keep=w.keep, status=st)
+        ws = torch.empty(int(rk.LIB.rk_sparse_ffn_workspace_size(ctypes.byref(args))), dtype=torch.uint8, device=dev)
+        flops = 2 * w.keep * w.x.shape[1] * 3 * w.w_gate.shape[0]
+        return ([lambda: rk.sparse_ffn(args, workspace=ws), st], flops / 1e12, "TFLOP/s",
+                "Qwen3-32B FFN block (d_model 5120, d_ff 25600), 4096 tokens, 2048 kept")
     classes = synth.stack_classes()
     glob_layer = next(l for l, c in enumerate(classes) if 0 in c)
     if case == "rag_prefill" or case == "rag_rope":
@@ -743,7 +790,8 @@ def build_case(torch, rk, dev, case, layer):
         return calls, roofline.rope_bytes(wl.rope) / 1e9, "GB/s", label + ", RoPE"
     decode = case in ("decode_microbench", "stack_decode")
     da = attn_to_device(wl.attn, dev)
-    base = da.args(rk, decode=decode, status=st, flags=rk.RK_ATTN_METADATA_STABLE if decode else 0)
+    base = da.args(rk, decode=decode, status=st,
+                   flags=(rk.RK_ATTN_METADATA_STABLE | rk.RK_ATTN_POOLS_STABLE) if decode else 0)
     n = (rk.segpaged_decode_workspace_size if decode else rk.segpaged_prefill_workspace_size)(base)
     ws = torch.zeros(n, dtype=torch.uint8, device=dev)
     fn = rk.segpaged_decode if decode else rk.segpaged_prefill

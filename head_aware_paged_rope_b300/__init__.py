@@ -10,7 +10,7 @@ _EXPORTS = (
     "AppendArgs", "RingArgs", "rope_coefficients", "SparseFfnArgs", "sparse_ffn_args", "sparse_ffn", "append_args", "append_kv", "ring_args", "ring_advance", "AttnArgs", "RkError", "RopeArgs", "RopeRun", "LIB", "attn_args", "rope_reposition", "rope_workspace_size",
     "segpaged_decode", "segpaged_decode_workspace_size", "segpaged_prefill", "segpaged_prefill_workspace_size",
     "status_string", "version", "RK_CLASS_DENSE", "RK_CLASS_GLOBAL", "RK_CLASS_LOCAL", "RK_CLASS_RETRIEVAL",
-    "RK_ROPE_HALF_SPLIT", "RK_ROPE_INTERLEAVED", "RK_ATTN_METADATA_STABLE", "RK_ATTN_DIAG_EXPIRE_WAIT",
+    "RK_ROPE_HALF_SPLIT", "RK_ROPE_INTERLEAVED", "RK_ATTN_METADATA_STABLE", "RK_ATTN_POOLS_STABLE", "RK_ATTN_DIAG_EXPIRE_WAIT",
 )
 
 

@@ -20,6 +20,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librk.so")
 RK_CLASS_GLOBAL, RK_CLASS_LOCAL, RK_CLASS_RETRIEVAL, RK_CLASS_DENSE = range(4)
 RK_ROPE_HALF_SPLIT, RK_ROPE_INTERLEAVED = 0, 1
 RK_ATTN_METADATA_STABLE = 1
+RK_ATTN_POOLS_STABLE = 2
 RK_ATTN_DIAG_EXPIRE_WAIT = 1 << 30
 
 
@@ -139,6 +140,13 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return t.data_ptr()
 
 
+def _keep(struct, *tensors):
+    """The struct holds raw device pointers: keep the tensors they point into alive as long as
+    the struct is (a temporary tensor would otherwise be freed and its memory reused)."""
+    struct._tensors = tuple(t for t in tensors if t is not None)
+    return struct
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -191,14 +199,16 @@ def attn_args(q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, hea
     B = seq_len.shape[0]
     Hq, d = q.shape[1], q.shape[2]
     Hkv = n_pages.shape[0] // max(B, 1)
-    return AttnArgs(q=_ptr(q), cu_seqlens_q=_ptr(cu_seqlens_q), seq_len=_ptr(seq_len), k_pool=_ptr(k_pool),
+    return _keep(AttnArgs(q=_ptr(q), cu_seqlens_q=_ptr(cu_seqlens_q), seq_len=_ptr(seq_len), k_pool=_ptr(k_pool),
                     v_pool=_ptr(v_pool), n_pool_pages=k_pool.shape[0], page_table=_ptr(page_table),
                     page_logical=_ptr(page_logical), n_pages=_ptr(n_pages), head_class=_ptr(head_class),
                     window=_ptr(window), sink=_ptr(sink), B=B, Hq=Hq, Hkv=Hkv, d=d, P=k_pool.shape[1],
                     max_pages=page_table.shape[1], total_q=int(total_q), max_q=int(max_q), scale=float(scale),
                     out=_ptr(out), lse=_ptr(lse), status=_ptr(status), flags=int(flags), k_new=_ptr(k_new),
                     v_new=_ptr(v_new), k_rot=_ptr(k_rot), rot_coef=_ptr(rot_coef),
-                    n_rot=0 if rot_coef is None else int(rot_coef.shape[0]), rot_style=int(rot_style))
+                    n_rot=0 if rot_coef is None else int(rot_coef.shape[0]), rot_style=int(rot_style)),
+                 q, seq_len, k_pool, v_pool, page_table, page_logical, n_pages, head_class, window, sink, out,
+                 cu_seqlens_q, lse, status, k_new, v_new, k_rot, rot_coef)
 
 
 def segpaged_prefill_workspace_size(args: AttnArgs) -> int:
@@ -228,10 +238,11 @@ def segpaged_decode(args: AttnArgs, *, device=None, workspace: Optional[torch.Te
 def append_args(k_new, v_new, pos, k_pool, v_pool, page_table, page_logical, n_pages, *, status=None) -> AppendArgs:
     """k_new/v_new: bf16 [B][Hkv][d]; pos: int32 [B]; tables as for attention."""
     B, Hkv, d = k_new.shape
-    return AppendArgs(k_new=_ptr(k_new), v_new=_ptr(v_new), pos=_ptr(pos), k_pool=_ptr(k_pool), v_pool=_ptr(v_pool),
-                      n_pool_pages=k_pool.shape[0], page_table=_ptr(page_table), page_logical=_ptr(page_logical),
-                      n_pages=_ptr(n_pages), B=B, Hkv=Hkv, d=d, P=k_pool.shape[1], max_pages=page_table.shape[1],
-                      status=_ptr(status))
+    return _keep(AppendArgs(k_new=_ptr(k_new), v_new=_ptr(v_new), pos=_ptr(pos), k_pool=_ptr(k_pool),
+                            v_pool=_ptr(v_pool), n_pool_pages=k_pool.shape[0], page_table=_ptr(page_table),
+                            page_logical=_ptr(page_logical), n_pages=_ptr(n_pages), B=B, Hkv=Hkv, d=d,
+                            P=k_pool.shape[1], max_pages=page_table.shape[1], status=_ptr(status)),
+                 k_new, v_new, pos, k_pool, v_pool, page_table, page_logical, n_pages, status)
 
 
 def append_kv(args: AppendArgs, stream=None) -> None:
@@ -242,9 +253,10 @@ def ring_args(pos, page_table, page_logical, n_pages, ring, window, sink, *, Hkv
               status=None) -> RingArgs:
     """Tables [B*Hkv][max_pages] (several layers may be stacked as extra sequences); pos: int32 [B]."""
     B = pos.shape[0]
-    return RingArgs(pos=_ptr(pos), page_table=_ptr(page_table), page_logical=_ptr(page_logical),
+    return _keep(RingArgs(pos=_ptr(pos), page_table=_ptr(page_table), page_logical=_ptr(page_logical),
                     n_pages=_ptr(n_pages), ring=_ptr(ring), window=_ptr(window), sink=_ptr(sink), B=B, Hkv=Hkv,
-                    P=P, max_pages=page_table.shape[1], status=_ptr(status))
+                    P=P, max_pages=page_table.shape[1], status=_ptr(status)),
+                 pos, page_table, page_logical, n_pages, ring, window, sink, status)
 
 
 def ring_advance(args: RingArgs, stream=None) -> None:
@@ -255,9 +267,10 @@ def sparse_ffn_args(x, importance, w_gate, w_up, w_down, out, kept, *, keep: int
     """x: bf16 [T][d_model]; importance: fp32 [T]; w_gate/w_up: bf16 [d_ff][d_model];
     w_down: bf16 [d_model][d_ff]; out: bf16 [T][d_model]; kept: int32 [keep]."""
     T, d_model = x.shape
-    return SparseFfnArgs(x=_ptr(x), importance=_ptr(importance), T=T, d_model=d_model, d_ff=w_gate.shape[0],
+    return _keep(SparseFfnArgs(x=_ptr(x), importance=_ptr(importance), T=T, d_model=d_model, d_ff=w_gate.shape[0],
                          keep=int(keep), w_gate=_ptr(w_gate), w_up=_ptr(w_up), w_down=_ptr(w_down), out=_ptr(out),
-                         kept=_ptr(kept), status=_ptr(status))
+                         kept=_ptr(kept), status=_ptr(status)),
+                 x, importance, w_gate, w_up, w_down, out, kept, status)
 
 
 def sparse_ffn(args: SparseFfnArgs, *, device=None, workspace: Optional[torch.Tensor] = None, stream=None) -> None:

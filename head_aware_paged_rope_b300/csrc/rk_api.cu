@@ -60,7 +60,7 @@ rk_status check_attn(const rk_attn_args* a, bool decode) {
   if (a->n_pool_pages * int64_t(a->P) >= (int64_t(1) << 31) || int64_t(a->total_q) * a->Hq >= (int64_t(1) << 31))
     return RK_ERR_UNSUPPORTED;   // row coordinates of the tensor maps are int32
   if (!std::isfinite(a->scale)) return RK_ERR_INVALID_ARG;
-  if (a->flags & ~(RK_ATTN_METADATA_STABLE | RK_ATTN_DIAG_EXPIRE_WAIT)) return RK_ERR_INVALID_ARG;
+  if (a->flags & ~(RK_ATTN_METADATA_STABLE | RK_ATTN_POOLS_STABLE | RK_ATTN_DIAG_EXPIRE_WAIT)) return RK_ERR_INVALID_ARG;
   if ((a->k_new != nullptr) != (a->v_new != nullptr) || (!decode && a->k_new)) return RK_ERR_INVALID_ARG;
   if (a->k_rot) {
     if (!decode) return RK_ERR_UNSUPPORTED;   // prefill reads repositioned pages (rk_rope_reposition)

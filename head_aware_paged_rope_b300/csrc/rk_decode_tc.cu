@@ -775,7 +775,9 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       mbar_arrive(smem_addr(&sh.kv_full[st]));
     };
     int pending = -1;                                 // stage whose turn waits for its copies
-    if (early) grid_dependency_wait();   // the pools (and k_new / v_new) are read and written from here on
+    // the pools (and k_new / v_new) are read and written from here on; with stable pools the
+    // copies start while the preceding kernel is still finishing
+    if (early && !(p.flags & RK_ATTN_POOLS_STABLE)) grid_dependency_wait();
     for (uint32_t gg = 0;; ++gg) {
       const int st = gg % NS;
       if (!wait_or_abort(sh, smem_addr(&sh.desc_full[st]), (gg / NS) & 1)) break;

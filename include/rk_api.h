@@ -220,6 +220,16 @@ typedef struct rk_attn_args {
  * completed.  Ignored by prefill. */
 #define RK_ATTN_METADATA_STABLE 1
 
+/* Decode, with RK_ATTN_METADATA_STABLE: the K and V pools, k_new and v_new were written by
+ * work that completed before the kernel preceding this call began (earlier decode steps,
+ * or other layers' pools written by the preceding kernels), and no kernel that may still
+ * be running when this call starts reads the slot this call's k_new / v_new are stored
+ * into.  The decode kernel then starts reading the pools while the preceding kernel is
+ * still finishing; it still waits for that kernel before reading q and before writing its
+ * outputs.  In a decode step where each call stores its own new token (k_new / v_new), the
+ * calls of the layers after rk_ring_advance satisfy this. */
+#define RK_ATTN_POOLS_STABLE 2
+
 /* Diagnostic, decode only: the first CTA of the decode kernel also waits for a word of the
  * workspace header that nothing sets, so that its bounded wait (1 s) runs out.  The call
  * then ends with RK_ERR_TIMEOUT in the status word, the way a wait that never completes

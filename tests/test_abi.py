@@ -108,12 +108,14 @@ def test_workspace_size_grows_with_queries(rk):
 
 
 def test_unknown_flag_bits_are_rejected(rk):
-    a = _attn_args(rk, flags=2)
+    a = _attn_args(rk, flags=4)
     assert rk.LIB.rk_segpaged_prefill(ctypes.byref(a), None, 0, None) == 1
     d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_METADATA_STABLE | 4)
     assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 1
     d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_METADATA_STABLE)
     assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 6           # valid flag: workspace next
+    d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_METADATA_STABLE | rk.RK_ATTN_POOLS_STABLE)
+    assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 6
     d = _attn_args(rk, cu_seqlens_q=None, total_q=2, max_q=1, flags=rk.RK_ATTN_DIAG_EXPIRE_WAIT)
     assert rk.LIB.rk_segpaged_decode(ctypes.byref(d), None, 0, None) == 6           # the diagnostic bit is known
 
@@ -153,3 +155,21 @@ def test_oracle_is_not_imported_by_the_product_path():
             "assert not any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules), 'oracle imported'" % ROOT)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_argument_structs_keep_their_tensors_alive(rk):
+    # the structs hold raw pointers; every builder passes the tensors it points into to
+    # _keep, which ties their lifetime to the struct's
+    import inspect
+    import weakref
+    import head_aware_paged_rope_b300._binding as B
+
+    class T:
+        pass
+    t = T()
+    w = weakref.ref(t)
+    s = B._keep(B.RingArgs(), t, None)
+    del t
+    assert w() is not None and s._tensors == (w(),)
+    for f in (B.attn_args, B.append_args, B.ring_args, B.sparse_ffn_args):
+        assert "return _keep(" in inspect.getsource(f)

@@ -164,7 +164,7 @@ def _compare(batch, out, lse, rows=None):
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["append_kv", "k_new"])
-@pytest.mark.parametrize("flags", [0, 1])
+@pytest.mark.parametrize("flags", [0, 1, 3])
 def test_decode_with_appends_over_recycled_pages(rk, flags, fused):
     """RoPE (runs cut to what window-only heads store), prefill, then per step: ring
     advance, append, decode -- compared with the oracle at the first, a middle and the last

@@ -261,9 +261,10 @@ def test_prefill_device_bounds_check(rk):
 
 
 # ------------------------------------------------------------------------- decode
-@pytest.mark.parametrize("flags", [0, 1])
+@pytest.mark.parametrize("flags", [0, 1, 3])
 def test_decode_microbench_full_size(rk, flags):
-    # flags 1: RK_ATTN_METADATA_STABLE (work planned before the preceding kernel completes)
+    # flags 1: RK_ATTN_METADATA_STABLE (work planned before the preceding kernel completes);
+    # 3: also RK_ATTN_POOLS_STABLE (the pools read before it completes)
     w = synth.decode_microbench()
     out, lse = _gpu_attn(rk, w.attn, decode=True, flags=flags)
     _compare(w.attn, out, lse)
@@ -400,7 +401,8 @@ def _ring_decode_steps(rk, w, kp, k_host, check_steps):
         kn, vn = to_device(w.decode_k[s], "cuda"), to_device(w.decode_v[s], "cuda")
         rk.segpaged_decode(rk.attn_args(q, seq_d, kp, dev["vp"], dev["tab"], dev["lg"], dev["n"], dev["cls"],
                                         dev["window"], dev["sink"], out, lse=lse, status=st, total_q=a.B, max_q=1,
-                                        flags=rk.RK_ATTN_METADATA_STABLE, k_new=kn, v_new=vn), workspace=ws)
+                                        flags=rk.RK_ATTN_METADATA_STABLE | rk.RK_ATTN_POOLS_STABLE, k_new=kn,
+                                        v_new=vn), workspace=ws)
         tab, lg = O.ring_advance(tab, lg, w.dec_n_pages, w.ring, a.window, a.sink, pos, a.Hkv, a.P)
         k_host, v_host = O.append_rows(k_host, v_host, tab, lg, w.dec_n_pages, pos, w.decode_k[s], w.decode_v[s],
                                        a.Hkv, a.P)
