@@ -23,11 +23,17 @@
 // inside the kernel; beyond that, plan_decode_kernel (rk_plan.cu) plans and
 // combine_decode_tc_kernel merges.  A share is walked as "portions" (the part of one
 // segment inside the share).
-//   warp 4   producer: walks the share, pushes each portion into a 2-entry ring, loads its
-//            G query rows (TMA) into one of two Q buffers, and gathers each tile page by
-//            page (one TMA box per page and 64 channels) from the shared K and V pools
-//            through the page table into a ring of kStages stages.  Segment records and
-//            page ids are requested one step ahead of their use.
+//   warp 4   controller: walks the share, pushes each portion into a 2-entry ring, loads its
+//            G query rows (TMA) into one of two Q buffers, and for every tile publishes into
+//            a stage descriptor the physical page of each of its pages (from the page table),
+//            the coefficient row of each page turned on load (k_rot), and the row that holds
+//            the appended token (k_new / v_new).  Segment records and page ids are requested
+//            one step ahead of their use.
+//   warps 6-9 copy: gather each tile's K and V rows from the shared pools into a ring of
+//            kStages stages with 16-byte cp.async copies, straight into the swizzled layout
+//            the MMA reads (the appended row comes from k_new / v_new and is also stored into
+//            its pool slot); with k_rot they turn the K rows of listed offline pages in shared
+//            memory before releasing the stage.
 //   warp 5   MMA issuer (one thread): issues whichever of S^T(j) (data landed, S buffer
 //            free) or O^T += V^T P^T (P^T written) is ready, so neither waits on the other.
 //   warps 0-3 softmax: thread t owns key t of the tile (TMEM lane t): masks it, finds the

@@ -9,18 +9,22 @@
 // page list of one unit: 256 query rows of one
 // KV head (GQA-packed: 256/G tokens x the G query heads), processed as two 128-row tiles
 // A and B that share every K/V tile loaded, which halves the K/V traffic per FLOP.
-// One CTA per SM, 10 warps:
+// One CTA per SM, 12 warps (three warpgroups):
 //   warp 8   producer: TMA loads the two Q tiles once per item, then for every 128-key
 //            tile gathers its pages (8 of 16 tokens or 4 of 32) from the shared pools
 //            through the page table, one box per page and 64 channels, into separate K
 //            and V rings (a K stage is freed as soon as both S tiles are computed);
 //   warp 9   MMA issuer (one thread): S_A = Q_A K^T and S_B = Q_B K^T into TMEM, then
 //            O_A += P_A V and O_B += P_B V with P read straight from TMEM;
+//   warps 10-11 idle (they complete the third warpgroup, whose registers go to the softmax);
 //   warps 0-3 / 4-7  softmax of tile A / B: thread r owns row r (TMEM lane r), loads its S
-//            row, masks the edge, keeps a running maximum that moves only when it grows by
-//            more than 2^8 (then the row of O is rescaled in TMEM), writes P = 2^(S - m) as
-//            bf16 pairs over the first half of its S columns, and at the end of the item
-//            normalises its O row and stores it (or a split partial).
+//            row once into registers, masks the edge, keeps a running maximum that moves
+//            only when it grows by more than 2^8 (then the row of O is rescaled in TMEM),
+//            writes P = 2^(S - m) as bf16 pairs over the first half of its S columns, and at
+//            the end of the item normalises its O row and stores it (or a split partial).
+// Registers: the block is launched with 168 per thread (12 warps x 168 = the 64K file); the
+// producer / MMA warpgroup drops to kRegsLow and the two softmax warpgroups rise to kRegsHigh
+// (2 x 128 x kRegsHigh + 128 x kRegsLow = 384 x 168), which holds a whole 128-score row.
 // TMEM: S_A cols 0-127, S_B 128-255, O_A 256-383, O_B 384-511.  The two softmax groups
 // work on S_A and S_B while the tensor core computes the other tile.  All waits are bounded.
 #include "rk_internal.cuh"
@@ -35,7 +39,11 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 384;
+constexpr int kRegsLaunch = 168;             // 65536 / 384, rounded down to a multiple of 8
+constexpr int kRegsHigh = 208;               // softmax warpgroups
+constexpr int kRegsLow = 88;                 // producer + MMA warpgroup
+static_assert(2 * 128 * kRegsHigh + 128 * kRegsLow == kTcThreads * kRegsLaunch, "register split must match the launch");
 constexpr int kTileRows = 128;
 constexpr int kUnitRows = 256;
 constexpr int kKeysTc = 128;
@@ -146,183 +154,189 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
   const int n_items = ws.header->n_items;
   const int64_t oob_row = p.n_pool_pages * P;      // a row index past the pool: TMA fills zeros
 
-  if (warp == 8) {
-    // ---------------------------------------------------------------- producer
-    uint32_t gg = 0, qn = 0;
-    int last_k = -1, last_v = -1;
-    uint32_t last_k_par = 0, last_v_par = 0, last_q_par = 0;
-    bool q_pending = false, ok = true;
-    // items: blockIdx.x first, then from the counter (the next ticket is requested one item
-    // ahead); each is handed to the other roles through the 2-entry ring
-    int it = blockIdx.x, ticket = 0;
-    for (int k = 0; ok; ++k) {
-      if (k > 0) it = int(gridDim.x) + __shfl_sync(0xffffffffu, ticket, 0);   // requested one item ago
-      const int slot = k & 1;
-      bool gotr = true;
-      if (lane == 0 && k >= 2) gotr = wait_or_abort(bars, smem_addr(&bars.iq_empty[slot]), ((k >> 1) - 1) & 1);
-      if (!__shfl_sync(0xffffffffu, gotr, 0)) { ok = false; break; }
-      const bool valid = it < n_items;
-      if (lane == 0) {
-        bars.ring[slot] = valid ? it : -1;
-        mbar_arrive(smem_addr(&bars.iq_full[slot]));
-        if (valid) ticket = atomicAdd(&ws.header->counter, 1);
-      }
-      if (!valid) break;
-      const Item item = ws.items[it];
-      const Unit un = ws.units[item.unit];
-      const int n_kt = (item.v_end - item.v_begin + EPT - 1) / EPT;
-      if (n_kt == 0) continue;
-      const int h = un.seg % p.Hkv;
-      const int32_t* trow = p.page_table + int64_t(un.seg) * p.max_pages;
-      bool got = true;
-      if (lane == 0) {   // both Q tiles; the buffer is free once the previous item's S are computed
-        if (qn > 0) got = wait_or_abort(bars, smem_addr(&bars.q_empty), (qn - 1) & 1);
-        if (got) {
-          const uint32_t bar = smem_addr(&bars.q_full);
-          mbar_arrive_expect_tx(bar, 2 * LY::kTile);
-#pragma unroll
-          for (int x = 0; x < 2; ++x)
-#pragma unroll
-            for (int hf = 0; hf < HALVES; ++hf)
-              tma_load_3d(sQ + x * LY::kTile + hf * kHalf, &tmQ, hf * 64, h * G, un.tok0 + x * (kTileRows / G), bar);
-          q_pending = true;
-          last_q_par = qn & 1;
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-      ++qn;
-      // page ids of 32 list entries at a time, the next group requested one group ahead
-      constexpr int TPG = 32 / EPT;
-      const int n_grp = (n_kt + TPG - 1) / TPG;
-      auto fetch = [&](int grp, int& raw, bool& present) {
-        const int v = item.v_begin + grp * 32 + lane;
-        present = v < item.v_end;
-        raw = present ? __ldg(trow + unit_entry(un, v)) : -1;
-      };
-      int raw;
-      bool present;
-      fetch(0, raw, present);
-      for (int grp = 0; ok && grp < n_grp; ++grp) {
-        int raw_n = -1;
-        bool present_n = false;
-        if (grp + 1 < n_grp) fetch(grp + 1, raw_n, present_n);
-        const bool page_ok = present && raw >= 0 && raw < p.n_pool_pages;
-        if (present && !page_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
-        const int64_t row = page_ok ? int64_t(raw) * P : oob_row;
-        const int tiles = min(TPG, n_kt - grp * TPG);
-        for (int jt = 0; jt < tiles; ++jt, ++gg) {
-          const int sk = gg % NK, sv = gg % NV;
-          const int pg = lane - jt * EPT;
-          got = true;
-          if (lane == 0) {
-            if (gg >= NK) got = wait_or_abort(bars, smem_addr(&bars.k_empty[sk]), ((gg / NK) - 1) & 1);
-            if (got) {
-              mbar_arrive_expect_tx(smem_addr(&bars.k_full[sk]), LY::kTile);
-              last_k = sk;
-              last_k_par = (gg / NK) & 1;
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-          if (pg >= 0 && pg < EPT)
-#pragma unroll
-            for (int hf = 0; hf < HALVES; ++hf)
-              tma_load_2d(sK + sk * LY::kTile + hf * kHalf + pg * P * 128, &tmK, hf * 64, int(row),
-                          smem_addr(&bars.k_full[sk]));
-          if (lane == 0) {
-            if (gg >= NV) got = wait_or_abort(bars, smem_addr(&bars.v_empty[sv]), ((gg / NV) - 1) & 1);
-            if (got) {
-              mbar_arrive_expect_tx(smem_addr(&bars.v_full[sv]), LY::kTile);
-              last_v = sv;
-              last_v_par = (gg / NV) & 1;
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
-          if (pg >= 0 && pg < EPT)
-#pragma unroll
-            for (int hf = 0; hf < HALVES; ++hf)
-              tma_load_2d(sV + sv * LY::kTile + hf * kHalf + pg * P * 128, &tmV, hf * 64, int(row),
-                          smem_addr(&bars.v_full[sv]));
-        }
-        raw = raw_n;
-        present = present_n;
-      }
-    }
-    if (!ok && lane == 0) fail(bars, p.status);
-    // copies still in flight after an abort: let them land before the CTA exits (bounded)
-    if (lane == 0 && aborted(bars)) {
-      if (last_k >= 0) mbar_wait(smem_addr(&bars.k_full[last_k]), last_k_par);
-      if (last_v >= 0) mbar_wait(smem_addr(&bars.v_full[last_v]), last_v_par);
-      if (q_pending) mbar_wait(smem_addr(&bars.q_full), last_q_par);
-    }
-  } else if (warp == 9) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+  // each warpgroup changes its register budget inside its own branch, so that the compiler
+  // allocates every role's code against that role's budget
+  if (warp >= 8) {
+    regs_decrease<kRegsLow>();
+    if (warp == 8) {
+      // ---------------------------------------------------------------- producer
       uint32_t gg = 0, qn = 0;
-      bool ok = true, pending = false;
-      uint32_t pend_bar = 0, pend_par = 0;
+      int last_k = -1, last_v = -1;
+      uint32_t last_k_par = 0, last_v_par = 0, last_q_par = 0;
+      bool q_pending = false, ok = true;
+      // items: blockIdx.x first, then from the counter (the next ticket is requested one item
+      // ahead); each is handed to the other roles through the 2-entry ring
+      int it = blockIdx.x, ticket = 0;
       for (int k = 0; ok; ++k) {
-        if (!wait_or_abort(bars, smem_addr(&bars.iq_full[k & 1]), (k >> 1) & 1)) { ok = false; break; }
-        const int it = bars.ring[k & 1];
-        mbar_arrive(smem_addr(&bars.iq_empty[k & 1]));
-        if (it < 0) break;
+        if (k > 0) it = int(gridDim.x) + __shfl_sync(0xffffffffu, ticket, 0);   // requested one item ago
+        const int slot = k & 1;
+        bool gotr = true;
+        if (lane == 0 && k >= 2) gotr = wait_or_abort(bars, smem_addr(&bars.iq_empty[slot]), ((k >> 1) - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, gotr, 0)) { ok = false; break; }
+        const bool valid = it < n_items;
+        if (lane == 0) {
+          bars.ring[slot] = valid ? it : -1;
+          mbar_arrive(smem_addr(&bars.iq_full[slot]));
+          if (valid) ticket = atomicAdd(&ws.header->counter, 1);
+        }
+        if (!valid) break;
         const Item item = ws.items[it];
+        const Unit un = ws.units[item.unit];
         const int n_kt = (item.v_end - item.v_begin + EPT - 1) / EPT;
         if (n_kt == 0) continue;
-        if (!wait_or_abort(bars, smem_addr(&bars.q_full), qn & 1)) { ok = false; break; }
-        ++qn;
-        tc_fence_after();
-        // order per tile j: S_A(j), O_B += P_B V (j-1), S_B(j), O_A += P_A V (j): the softmax of
-        // one tile runs while the tensor core works for the other
-        auto qk = [&](int x, uint32_t g1, uint32_t kb) -> bool {
-          // S_x holds P_x of the previous tile until its value product has completed
-          if (g1 >= 1 && !wait_or_abort(bars, smem_addr(&bars.o_done[x]), (g1 - 1) & 1)) return false;
-          tc_fence_after();
-          const uint32_t qb = sQ + x * LY::kTile;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint64_t a = desc_sw128(qb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-            const uint64_t b = desc_sw128(kb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-            tc_mma_f16(tmem + x * kKeysTc, a, b, kIdescQK, k > 0 ? 1u : 0u);
+        const int h = un.seg % p.Hkv;
+        const int32_t* trow = p.page_table + int64_t(un.seg) * p.max_pages;
+        bool got = true;
+        if (lane == 0) {   // both Q tiles; the buffer is free once the previous item's S are computed
+          if (qn > 0) got = wait_or_abort(bars, smem_addr(&bars.q_empty), (qn - 1) & 1);
+          if (got) {
+            const uint32_t bar = smem_addr(&bars.q_full);
+            mbar_arrive_expect_tx(bar, 2 * LY::kTile);
+  #pragma unroll
+            for (int x = 0; x < 2; ++x)
+  #pragma unroll
+              for (int hf = 0; hf < HALVES; ++hf)
+                tma_load_3d(sQ + x * LY::kTile + hf * kHalf, &tmQ, hf * 64, h * G, un.tok0 + x * (kTileRows / G), bar);
+            q_pending = true;
+            last_q_par = qn & 1;
           }
-          tc_commit(smem_addr(&bars.s_full[x]));
-          return true;
-        };
-        auto pv = [&](int x, uint32_t g1, bool first) -> bool {
-          const int sv = g1 % NV;
-          if (!wait_or_abort(bars, smem_addr(&bars.v_full[sv]), (g1 / NV) & 1)) return false;
-          if (!wait_or_abort(bars, smem_addr(&bars.p_full[x]), g1 & 1)) return false;
-          tc_fence_after();
-          const uint32_t vb = sV + sv * LY::kTile;
-#pragma unroll
-          for (int k = 0; k < kKeysTc / 16; ++k) {
-            const uint64_t b = desc_sw128(vb + k * 2048, kHalf, 1024);
-            tc_mma_f16_ts(tmem + kColO + x * 128, tmem + x * kKeysTc + k * 8, b, kIdescPV, (!first || k > 0) ? 1u : 0u);
-          }
-          tc_commit(smem_addr(&bars.o_done[x]));
-          if (x == 1) tc_commit(smem_addr(&bars.v_empty[sv]));   // both value products of tile g1 issued
-          pending = true;
-          pend_bar = smem_addr(&bars.o_done[x]);
-          pend_par = g1 & 1;
-          return true;
-        };
-        const uint32_t g_first = gg;
-        for (int j = 0; j < n_kt; ++j, ++gg) {
-          const int sk = gg % NK;
-          if (!wait_or_abort(bars, smem_addr(&bars.k_full[sk]), (gg / NK) & 1)) { ok = false; break; }
-          const uint32_t kb = sK + sk * LY::kTile;
-          if (!qk(0, gg, kb)) { ok = false; break; }
-          if (j >= 1 && !pv(1, gg - 1, gg - 1 == g_first)) { ok = false; break; }
-          if (!qk(1, gg, kb)) { ok = false; break; }
-          tc_commit(smem_addr(&bars.k_empty[sk]));
-          if (j == n_kt - 1) tc_commit(smem_addr(&bars.q_empty));
-          if (!pv(0, gg, j == 0)) { ok = false; break; }
         }
-        if (ok && !pv(1, gg - 1, n_kt == 1)) ok = false;
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        ++qn;
+        // page ids of 32 list entries at a time, the next group requested one group ahead
+        constexpr int TPG = 32 / EPT;
+        const int n_grp = (n_kt + TPG - 1) / TPG;
+        auto fetch = [&](int grp, int& raw, bool& present) {
+          const int v = item.v_begin + grp * 32 + lane;
+          present = v < item.v_end;
+          raw = present ? __ldg(trow + unit_entry(un, v)) : -1;
+        };
+        int raw;
+        bool present;
+        fetch(0, raw, present);
+        for (int grp = 0; ok && grp < n_grp; ++grp) {
+          int raw_n = -1;
+          bool present_n = false;
+          if (grp + 1 < n_grp) fetch(grp + 1, raw_n, present_n);
+          const bool page_ok = present && raw >= 0 && raw < p.n_pool_pages;
+          if (present && !page_ok) report(p.status, RK_ERR_DEVICE_BOUNDS);
+          const int64_t row = page_ok ? int64_t(raw) * P : oob_row;
+          const int tiles = min(TPG, n_kt - grp * TPG);
+          for (int jt = 0; jt < tiles; ++jt, ++gg) {
+            const int sk = gg % NK, sv = gg % NV;
+            const int pg = lane - jt * EPT;
+            got = true;
+            if (lane == 0) {
+              if (gg >= NK) got = wait_or_abort(bars, smem_addr(&bars.k_empty[sk]), ((gg / NK) - 1) & 1);
+              if (got) {
+                mbar_arrive_expect_tx(smem_addr(&bars.k_full[sk]), LY::kTile);
+                last_k = sk;
+                last_k_par = (gg / NK) & 1;
+              }
+            }
+            if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+            if (pg >= 0 && pg < EPT)
+  #pragma unroll
+              for (int hf = 0; hf < HALVES; ++hf)
+                tma_load_2d(sK + sk * LY::kTile + hf * kHalf + pg * P * 128, &tmK, hf * 64, int(row),
+                            smem_addr(&bars.k_full[sk]));
+            if (lane == 0) {
+              if (gg >= NV) got = wait_or_abort(bars, smem_addr(&bars.v_empty[sv]), ((gg / NV) - 1) & 1);
+              if (got) {
+                mbar_arrive_expect_tx(smem_addr(&bars.v_full[sv]), LY::kTile);
+                last_v = sv;
+                last_v_par = (gg / NV) & 1;
+              }
+            }
+            if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+            if (pg >= 0 && pg < EPT)
+  #pragma unroll
+              for (int hf = 0; hf < HALVES; ++hf)
+                tma_load_2d(sV + sv * LY::kTile + hf * kHalf + pg * P * 128, &tmV, hf * 64, int(row),
+                            smem_addr(&bars.v_full[sv]));
+          }
+          raw = raw_n;
+          present = present_n;
+        }
       }
-      if (!ok) fail(bars, p.status);
-      if (pending && aborted(bars)) mbar_wait(pend_bar, pend_par);
+      if (!ok && lane == 0) fail(bars, p.status);
+      // copies still in flight after an abort: let them land before the CTA exits (bounded)
+      if (lane == 0 && aborted(bars)) {
+        if (last_k >= 0) mbar_wait(smem_addr(&bars.k_full[last_k]), last_k_par);
+        if (last_v >= 0) mbar_wait(smem_addr(&bars.v_full[last_v]), last_v_par);
+        if (q_pending) mbar_wait(smem_addr(&bars.q_full), last_q_par);
+      }
+    } else if (warp == 9) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        uint32_t gg = 0, qn = 0;
+        bool ok = true, pending = false;
+        uint32_t pend_bar = 0, pend_par = 0;
+        for (int k = 0; ok; ++k) {
+          if (!wait_or_abort(bars, smem_addr(&bars.iq_full[k & 1]), (k >> 1) & 1)) { ok = false; break; }
+          const int it = bars.ring[k & 1];
+          mbar_arrive(smem_addr(&bars.iq_empty[k & 1]));
+          if (it < 0) break;
+          const Item item = ws.items[it];
+          const int n_kt = (item.v_end - item.v_begin + EPT - 1) / EPT;
+          if (n_kt == 0) continue;
+          if (!wait_or_abort(bars, smem_addr(&bars.q_full), qn & 1)) { ok = false; break; }
+          ++qn;
+          tc_fence_after();
+          // order per tile j: S_A(j), O_B += P_B V (j-1), S_B(j), O_A += P_A V (j): the softmax of
+          // one tile runs while the tensor core works for the other
+          auto qk = [&](int x, uint32_t g1, uint32_t kb) -> bool {
+            // S_x holds P_x of the previous tile until its value product has completed
+            if (g1 >= 1 && !wait_or_abort(bars, smem_addr(&bars.o_done[x]), (g1 - 1) & 1)) return false;
+            tc_fence_after();
+            const uint32_t qb = sQ + x * LY::kTile;
+  #pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint64_t a = desc_sw128(qb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+              const uint64_t b = desc_sw128(kb + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+              tc_mma_f16(tmem + x * kKeysTc, a, b, kIdescQK, k > 0 ? 1u : 0u);
+            }
+            tc_commit(smem_addr(&bars.s_full[x]));
+            return true;
+          };
+          auto pv = [&](int x, uint32_t g1, bool first) -> bool {
+            const int sv = g1 % NV;
+            if (!wait_or_abort(bars, smem_addr(&bars.v_full[sv]), (g1 / NV) & 1)) return false;
+            if (!wait_or_abort(bars, smem_addr(&bars.p_full[x]), g1 & 1)) return false;
+            tc_fence_after();
+            const uint32_t vb = sV + sv * LY::kTile;
+  #pragma unroll
+            for (int k = 0; k < kKeysTc / 16; ++k) {
+              const uint64_t b = desc_sw128(vb + k * 2048, kHalf, 1024);
+              tc_mma_f16_ts(tmem + kColO + x * 128, tmem + x * kKeysTc + k * 8, b, kIdescPV, (!first || k > 0) ? 1u : 0u);
+            }
+            tc_commit(smem_addr(&bars.o_done[x]));
+            if (x == 1) tc_commit(smem_addr(&bars.v_empty[sv]));   // both value products of tile g1 issued
+            pending = true;
+            pend_bar = smem_addr(&bars.o_done[x]);
+            pend_par = g1 & 1;
+            return true;
+          };
+          const uint32_t g_first = gg;
+          for (int j = 0; j < n_kt; ++j, ++gg) {
+            const int sk = gg % NK;
+            if (!wait_or_abort(bars, smem_addr(&bars.k_full[sk]), (gg / NK) & 1)) { ok = false; break; }
+            const uint32_t kb = sK + sk * LY::kTile;
+            if (!qk(0, gg, kb)) { ok = false; break; }
+            if (j >= 1 && !pv(1, gg - 1, gg - 1 == g_first)) { ok = false; break; }
+            if (!qk(1, gg, kb)) { ok = false; break; }
+            tc_commit(smem_addr(&bars.k_empty[sk]));
+            if (j == n_kt - 1) tc_commit(smem_addr(&bars.q_empty));
+            if (!pv(0, gg, j == 0)) { ok = false; break; }
+          }
+          if (ok && !pv(1, gg - 1, n_kt == 1)) ok = false;
+        }
+        if (!ok) fail(bars, p.status);
+        if (pending && aborted(bars)) mbar_wait(pend_bar, pend_par);
+      }
     }
   } else {
+    regs_increase<kRegsHigh>();
     // ---------------------------------------------------------------- softmax + epilogue
     const int x = warp >> 2;                 // tile A (warps 0-3) or B (warps 4-7)
     const int r = tid & 127;                 // row of the tile = TMEM lane
@@ -409,29 +423,27 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
             pm[pg] = m;
           }
         }
-        // pass 1 over S in TMEM: the row maximum (64 columns per load round, 3-input max)
+        // the row's 128 scores, loaded from TMEM once; masked slots become -inf, which adds
+        // nothing to the maximum and gives exp2 = 0
         const float sc = p.scale_log2;
-        float mx = -INFINITY;
+        uint32_t v[kKeysTc];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t v[64];
-          tmem_ld32(tmem + lane_base + colS + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tmem + lane_base + colS + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
-          if (full) {
+        for (int q4 = 0; q4 < kKeysTc / 32; ++q4)
+          tmem_ld32(tmem + lane_base + colS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[q4 * 32]));
+        tmem_wait_ld();
+        if (!full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmax3(mx, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int c0 = h2 * 64 + 2 * i, c1 = c0 + 1;
-              const float a0 = (pm[c0 / P] >> (c0 % P)) & 1u ? __uint_as_float(v[2 * i]) : -INFINITY;
-              const float a1 = (pm[c1 / P] >> (c1 % P)) & 1u ? __uint_as_float(v[2 * i + 1]) : -INFINITY;
-              mx = fmax3(mx, a0, a1);
-            }
-          }
+          for (int c = 0; c < kKeysTc; ++c)
+            if (!((pm[c / P] >> (c % P)) & 1u)) v[c] = __float_as_uint(-INFINITY);
         }
-        mx *= sc;
+        float mx;
+        {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four independent chains
+#pragma unroll
+          for (int i = 0; i < kKeysTc / 2; ++i)
+            m4[i & 3] = fmax3(m4[i & 3], __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sc;
+        }
         const float m_new = fmaxf(m_ref, mx);
         const bool rescale = m_new > m_ref + kRescaleThreshold;   // false while both are -inf
         // O_x already holds earlier tiles of this item (their value products completed before
@@ -440,12 +452,12 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
           const float alpha = rescale ? fast_exp2(m_ref - m_new) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + colO + c * 32, v);
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + colO + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(tmem + lane_base + colO + c * 32, v);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tmem + lane_base + colO + c * 32, o);
           }
           tmem_wait_st();
         }
@@ -453,48 +465,23 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
           l_sum = (m_ref == -INFINITY) ? 0.f : l_sum * fast_exp2(m_ref - m_new);
           m_ref = m_new;
         }
-        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-        // pass 2: P = 2^(S - m) as bf16 pairs; the 32 scores of chunk c become packed columns
-        // 16c .. 16c+15, which only overwrite scores already read
-        const float nref = -ref;
-        float ps0 = 0.f, ps1 = 0.f;
+        const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
+        // P = 2^(S - m) as bf16 pairs: the 32 scores of chunk c become packed columns
+        // 16c .. 16c+15 (their scores are already in registers)
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t v[64];
-          tmem_ld32(tmem + lane_base + colS + h2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tmem + lane_base + colS + h2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_wait_ld();
+        for (int c = 0; c < kKeysTc / 32; ++c) {
+          uint32_t w[16];
 #pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const int c = h2 * 2 + c2;
-            uint32_t w[16];
-            if (full) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float e0 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i]), sc, nref));
-                const float e1 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i + 1]), sc, nref));
-                ps0 += e0;
-                ps1 += e1;
-                w[i] = pack_bf16(e0, e1);
-              }
-            } else {
-              const uint32_t bits = pm[(c * 32) / P] >> ((c * 32) % P);
-              const uint32_t cm = P == 16 ? (bits & 0xffffu) | (pm[(c * 32) / P + 1] << 16) : bits;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                float e0 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i]), sc, nref));
-                float e1 = fast_exp2(fmaf(__uint_as_float(v[c2 * 32 + 2 * i + 1]), sc, nref));
-                e0 = (cm >> (2 * i)) & 1u ? e0 : 0.f;
-                e1 = (cm >> (2 * i + 1)) & 1u ? e1 : 0.f;
-                ps0 += e0;
-                ps1 += e1;
-                w[i] = pack_bf16(e0, e1);
-              }
-            }
-            tmem_st16(tmem + lane_base + colS + c * 16, w);
+          for (int i = 0; i < 16; ++i) {
+            const float e0 = fast_exp2(fmaf(__uint_as_float(v[c * 32 + 2 * i]), sc, nref));
+            const float e1 = fast_exp2(fmaf(__uint_as_float(v[c * 32 + 2 * i + 1]), sc, nref));
+            ps[i & 3] += e0 + e1;
+            w[i] = pack_bf16(e0, e1);
           }
+          tmem_st16(tmem + lane_base + colS + c * 16, w);
         }
-        const float psum = ps0 + ps1;
+        const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         l_sum += psum;
         tmem_wait_st();
         tc_fence_before();
@@ -580,7 +567,13 @@ cudaError_t launch_tc(const AttnParams& p, const AttnWorkspace& ws, int grid, cu
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
+    // the warpgroups' register budgets add up to 384 x kRegsLaunch: a build launched with any
+    // other count could leave the softmax warpgroups waiting for registers, so refuse it
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, P>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(prefill_tc_kernel<D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
