@@ -236,7 +236,7 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
   const AttnWorkspace ws = make_ws(workspace, l);
   const int grid = std::max(1, std::min(l.max_items, sms));
   const int ept = prefill_tc_keys() / a->P;
-  cudaError_t e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * 2), 2, stream);
+  cudaError_t e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * kItemsPerCta), kMinChunkTiles, stream);
   if (e == cudaSuccess) e = launch_prefill_tc(p, ws, grid, stream);
   if (e == cudaSuccess) e = launch_combine(p, ws, stream);
   return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;

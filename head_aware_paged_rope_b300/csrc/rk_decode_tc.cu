@@ -662,7 +662,6 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           if (lane == 0) {
             if (gg >= NS) got = wait_or_abort(sh, smem_addr(&sh.kv_empty[st]), ((gg / NS) - 1) & 1);
             if (got) {
-#pragma unroll
               int any = 0;
 #pragma unroll
               for (int pg = 0; pg < 8; ++pg) {

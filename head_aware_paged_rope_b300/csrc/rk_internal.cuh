@@ -145,6 +145,10 @@ struct AttnWorkspace {
 };
 
 constexpr int kTargetItems = 2048;   // upper bound on items beyond one per unit
+// Prefill items: about kItemsPerCta per CTA, each at least kMinChunkTiles key tiles (finer
+// items balance the CTAs; each item also costs a start, an epilogue and a partial to merge).
+constexpr int kItemsPerCta = 8;
+constexpr int kMinChunkTiles = 12;
 
 // ------------------------------------------------------------------ decode work list
 // Decode is scheduled stream-K style: the key tiles (128 keys) of all head segments are
