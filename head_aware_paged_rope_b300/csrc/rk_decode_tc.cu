@@ -191,7 +191,7 @@ __device__ __forceinline__ float warp_reduce_cols(float (&v)[NG]) {
 }
 
 constexpr int kMergeFan = 12;   // partials one CTA merges at a time (single-launch path)
-constexpr int kAlignTiles = 2;  // segments this short are never split when there are enough CTAs
+constexpr int kAlignTiles = 8;  // all segments this short and no more of them than CTAs: one segment per CTA
 constexpr int kShortTiles = 8;  // single-launch path: segments this short are never split
 
 // Partial slot of CTA c for a split segment (two per CTA: its first and its last portion):

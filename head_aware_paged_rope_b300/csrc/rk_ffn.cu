@@ -118,6 +118,7 @@ __global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __rest
 // ------------------------------------------------------------------ GEMM
 constexpr int kGThreads = 192;
 constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kDownN = 256;                      // output columns of a down-projection tile
 constexpr int kStages = 4;
 constexpr int kATile = kBM * kBK * 2;            // 16 KB
 constexpr int kBTile = kBN * kBK * 2;            // 32 KB
@@ -170,9 +171,11 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
   __shared__ GemmShared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_addr(smem);
-  constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN, 0, 0);
   // MODE 0 covers 128 act columns per tile (256 accumulator columns: gate | up)
-  constexpr int kTileN = MODE == 0 ? kBN / 2 : kBN;
+  constexpr int kMmaN = MODE == 0 ? kBN : kDownN;
+  constexpr uint32_t kIdesc = idesc_bf16(kBM, kMmaN, 0, 0);
+  constexpr int kTileN = MODE == 0 ? kBN / 2 : kDownN;
+  constexpr int kLoadBytes = kATile + kMmaN * kBK * 2;
   const int m_tiles = (g.M + kBM - 1) / kBM, n_tiles = g.N / kTileN, k_steps = g.K / kBK;
   const int n_work = m_tiles * n_tiles;
 
@@ -216,7 +219,7 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
           const int s = it % kStages;
           if (it >= kStages && !g_wait(sh, smem_addr(&sh.empty[s]), ((it / kStages) - 1) & 1)) { ok = false; break; }
           const uint32_t bar = smem_addr(&sh.full[s]);
-          mbar_arrive_expect_tx(bar, kStageBytes);
+          mbar_arrive_expect_tx(bar, kLoadBytes);
           const uint32_t sa = sbase + s * kStageBytes, sb = sa + kATile;
           tma_load_2d(sa, &tmA, ks * kBK, m * kBM, bar);
           if (MODE == 0) {
@@ -339,7 +342,7 @@ cudaError_t launch_gemm(const void* A, int lda_rows, const void* B0, const void*
   const cuuint64_t astr[1] = {cuuint64_t(g.K) * 2};
   const cuuint32_t abox[2] = {kBK, kBM};
   const cuuint64_t bdims[2] = {cuuint64_t(g.K), cuuint64_t(b_rows)};
-  const cuuint32_t bbox[2] = {kBK, MODE == 0 ? uint32_t(kBN / 2) : uint32_t(kBN)};
+  const cuuint32_t bbox[2] = {kBK, MODE == 0 ? uint32_t(kBN / 2) : uint32_t(kDownN)};
   if (!encode_tmap_bf16(&ma, A, 2, adims, astr, abox) || !encode_tmap_bf16(&mb0, B0, 2, bdims, astr, bbox) ||
       !encode_tmap_bf16(&mb1, MODE == 0 ? B1 : B0, 2, bdims, astr, bbox))
     return cudaErrorInvalidValue;
@@ -351,7 +354,7 @@ cudaError_t launch_gemm(const void* A, int lda_rows, const void* B0, const void*
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const int tiles = ((g.M + kBM - 1) / kBM) * (g.N / (MODE == 0 ? kBN / 2 : kBN));
+  const int tiles = ((g.M + kBM - 1) / kBM) * (g.N / (MODE == 0 ? kBN / 2 : kDownN));
   const int grid = std::max(1, std::min(tiles, device_sm_count()));
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kGThreads), kGSmem, stream, attr);

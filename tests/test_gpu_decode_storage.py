@@ -16,6 +16,10 @@ from oracle import rk_oracle as O
 from workloads import synth
 from workloads.device import attn_to_device, bf16_bits, rope_to_device, to_device
 
+# a decode workspace large enough for every call of these tests (G <= 16, d 128, one CTA per SM):
+# counters, plan records and the partial and group slots of the work list
+DEC_WS_BYTES = 1 << 25
+
 pytestmark = pytest.mark.gpu
 
 ATOL, RTOL_L2, LSE_TOL = 3e-2, 5e-3, 1e-3
@@ -190,7 +194,7 @@ def test_decode_with_appends_over_recycled_pages(rk, flags, fused):
     pos_d = torch.empty(a.B, dtype=torch.int32, device="cuda")
     out = torch.empty((a.B, a.Hq, a.d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((a.B, a.Hq), dtype=torch.float32, device="cuda")
-    ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(DEC_WS_BYTES, dtype=torch.uint8, device="cuda")
     for s in range(n_dec):
         pos = (a.seq_len + s).astype(np.int32)
         pos_d.copy_(torch.from_numpy(pos))
@@ -247,7 +251,7 @@ def test_decode_repositions_on_load_bit_identically(rk, style):
         dv = _ring_args_dev(rk, wl, st)
         vp = to_device(a.v_pool, "cuda")
         cls, win, sink = (to_device(x, "cuda") for x in (a.head_class, a.window, a.sink))
-        ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(DEC_WS_BYTES, dtype=torch.uint8, device="cuda")
         outs = []
         for s in range(wl.decode_k.shape[0]):
             pos = (a.seq_len + s).astype(np.int32)

@@ -20,6 +20,10 @@ from oracle import rk_oracle as O
 from workloads import synth
 from workloads.device import attn_to_device, bf16_bits, rope_to_device, to_device
 
+# a decode workspace large enough for every call of these tests (G <= 16, d 128, one CTA per SM):
+# counters, plan records and the partial and group slots of the work list
+DEC_WS_BYTES = 1 << 25
+
 pytestmark = pytest.mark.gpu
 
 ATOL, RTOL_L2, LSE_TOL = 3e-2, 5e-3, 1e-3
@@ -391,7 +395,7 @@ def _ring_decode_steps(rk, w, kp, k_host, check_steps):
     tab, lg = w.dec_page_table, w.dec_page_logical
     out = torch.empty((a.B, a.Hq, a.d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((a.B, a.Hq), dtype=torch.float32, device="cuda")
-    ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(DEC_WS_BYTES, dtype=torch.uint8, device="cuda")
     for s in range(max(check_steps) + 1):
         pos = (a.seq_len + s).astype(np.int32)
         pos_d, seq_d = to_device(pos, "cuda"), to_device(pos + 1, "cuda")
