@@ -305,10 +305,11 @@ class LayerState:
         self.dec_v = to_device(wl.decode_v[:n_dec], dev)
         self.dec_out = torch.empty((n_dec, a.Hq, a.d), dtype=torch.bfloat16, device=dev)
         self.dec_lse = torch.empty((n_dec, a.Hq), dtype=torch.float32, device=dev)
-        tab, lg, nn = dec.tab[layer], dec.lg[layer], dec.n[layer]
+        nn = dec.n[layer]
         self.dec_args = []
         for s in range(n_dec):
             da = self.attn
+            tab, lg = dec.tab[s % 2][layer], dec.lg[s % 2][layer]
             self.dec_args.append(rk.AttnArgs(
                 q=self.dec_q[s].data_ptr(), cu_seqlens_q=None, seq_len=dec.seq[s].data_ptr(),
                 k_pool=da.k_pool.data_ptr(), v_pool=da.v_pool.data_ptr(), n_pool_pages=da.k_pool.shape[0],
@@ -333,8 +334,10 @@ class LayerState:
 
 class DecodeTables:
     """The decode page tables of all layers, stacked as [layers][B*Hkv][max_pages] (layers
-    as extra sequences of one rk_ring_advance call), their starting state (restored at the
-    start of every replayed decode phase), the ring sizes, and per-step positions."""
+    as extra sequences of one rk_ring_advance call), twice: step s decodes on buffer s % 2,
+    and before it the rings of step s + 1 are advanced out of place into the other buffer,
+    so that no decode call waits for a table update.  Also their starting state (restored at
+    the start of every replayed decode phase), the ring sizes, and per-step positions."""
 
     def __init__(self, rk, wls, dev, n_dec, torch):
         from workloads.device import to_device
@@ -348,7 +351,8 @@ class DecodeTables:
             tab[l, :, :w.dec_page_table.shape[1]] = w.dec_page_table
             lg[l, :, :w.dec_page_logical.shape[1]] = w.dec_page_logical
         self.tab0, self.lg0 = to_device(tab, dev), to_device(lg, dev)
-        self.tab, self.lg = self.tab0.clone(), self.lg0.clone()
+        self.tab = torch.stack([self.tab0, self.tab0])       # [2][layers][B*Hkv][max_pages]
+        self.lg = torch.stack([self.lg0, self.lg0])
         self.n = to_device(np.stack([w.dec_n_pages for w in wls]), dev)
         self.ring = to_device(np.concatenate([w.ring for w in wls]), dev)
         self.window = to_device(np.concatenate([w.attn.window for w in wls]), dev)
@@ -357,9 +361,14 @@ class DecodeTables:
         self.pos = torch.tensor([[base + s] * L for s in range(n_dec)], dtype=torch.int32, device=dev)
         self.seq = torch.tensor([[base + s + 1] for s in range(n_dec)], dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ring_args = [rk.ring_args(self.pos[s], self.tab.view(L * nseg, mp), self.lg.view(L * nseg, mp),
+        flat = lambda t, i: t[i].view(L * nseg, mp)
+        # step 0's rings, in place on buffer 0; then before step s, step s + 1's out of place
+        self.ring_first = rk.ring_args(self.pos[0], flat(self.tab, 0), flat(self.lg, 0), self.n.view(-1), self.ring,
+                                       self.window, self.sink, Hkv=a0.Hkv, P=a0.P, status=self.status)
+        self.ring_next = [rk.ring_args(self.pos[s + 1], flat(self.tab, (s + 1) % 2), flat(self.lg, (s + 1) % 2),
                                        self.n.view(-1), self.ring, self.window, self.sink, Hkv=a0.Hkv, P=a0.P,
-                                       status=self.status) for s in range(n_dec)]
+                                       status=self.status, src_page_table=flat(self.tab, s % 2),
+                                       src_page_logical=flat(self.lg, s % 2)) for s in range(n_dec - 1)]
 
     def host_inputs(self):
         return [self.tab0, self.lg0, self.n, self.ring, self.window, self.sink, self.pos, self.seq]
@@ -390,11 +399,14 @@ def enqueue(rk, layers, dec, stream_handle, phase):
                 _call(rk.LIB.rk_segpaged_prefill, L.prefill_args, L.prefill_ws, stream_handle)
                 n += 3
     if phase in ("step", "decode"):
-        dec.tab.copy_(dec.tab0)            # the rings start from the state after the prefill
-        dec.lg.copy_(dec.lg0)
+        dec.tab.copy_(dec.tab0.unsqueeze(0).expand_as(dec.tab))   # the rings start from the state after
+        dec.lg.copy_(dec.lg0.unsqueeze(0).expand_as(dec.lg))      # the prefill, in both buffers
+        _call2(rk.LIB.rk_ring_advance, dec.ring_first, stream_handle)
+        n += 1
         for s in range(layers[0].n_dec):
-            _call2(rk.LIB.rk_ring_advance, dec.ring_args[s], stream_handle)
-            n += 1
+            if s + 1 < layers[0].n_dec:   # the next step's tables, while this step decodes
+                _call2(rk.LIB.rk_ring_advance, dec.ring_next[s], stream_handle)
+                n += 1
             for L in layers:   # each decode call first stores its layer's new token (k_new / v_new)
                 _call(rk.LIB.rk_segpaged_decode, L.dec_args[s], L.dec_ws, stream_handle)
                 # one kernel for up to 512 head segments (B * Hkv), else planner + attention + merge
@@ -636,8 +648,9 @@ def ours_main(args, world, rank, local):
     parts["decode"].update({"GB/s": bytes_decode / (parts["decode"]["ms"] * 1e-3) / 1e9, "bytes": bytes_decode,
                             "TFLOP/s": flops_decode / (parts["decode"]["ms"] * 1e-3) / 1e12,
                             "calls": args.layers * args.decode_steps,
-                            "note": "per step: one rk_ring_advance for all layers, then per layer one "
-                                    "rk_segpaged_decode that also stores the layer's new token (k_new / v_new)"})
+                            "note": "per step: one rk_ring_advance (all layers) that prepares the next step's "
+                                    "tables in the other buffer, then per layer one rk_segpaged_decode that also "
+                                    "stores the layer's new token (k_new / v_new)"})
     parts["rope"]["frac_hbm"] = parts["rope"]["GB/s"] / peaks["hbm_gbs"]
     parts["decode"]["frac_hbm"] = parts["decode"]["GB/s"] / peaks["hbm_gbs"]
     parts["prefill"]["frac_bf16_burst"] = parts["prefill"]["TFLOP/s"] / peaks["bf16_tflops"]

@@ -78,6 +78,7 @@ class RingArgs(ctypes.Structure):
         ("n_pages", ctypes.c_void_p), ("ring", ctypes.c_void_p), ("window", ctypes.c_void_p),
         ("sink", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("P", ctypes.c_int32),
         ("max_pages", ctypes.c_int32), ("status", ctypes.c_void_p),
+        ("src_page_table", ctypes.c_void_p), ("src_page_logical", ctypes.c_void_p),
     ]
 
 
@@ -250,13 +251,16 @@ def append_kv(args: AppendArgs, stream=None) -> None:
 
 
 def ring_args(pos, page_table, page_logical, n_pages, ring, window, sink, *, Hkv: int, P: int,
-              status=None) -> RingArgs:
-    """Tables [B*Hkv][max_pages] (several layers may be stacked as extra sequences); pos: int32 [B]."""
+              status=None, src_page_table=None, src_page_logical=None) -> RingArgs:
+    """Tables [B*Hkv][max_pages] (several layers may be stacked as extra sequences); pos: int32 [B].
+    With src_page_table / src_page_logical the lists are advanced from those tables into
+    page_table / page_logical (out of place) instead of in place."""
     B = pos.shape[0]
     return _keep(RingArgs(pos=_ptr(pos), page_table=_ptr(page_table), page_logical=_ptr(page_logical),
                     n_pages=_ptr(n_pages), ring=_ptr(ring), window=_ptr(window), sink=_ptr(sink), B=B, Hkv=Hkv,
-                    P=P, max_pages=page_table.shape[1], status=_ptr(status)),
-                 pos, page_table, page_logical, n_pages, ring, window, sink, status)
+                    P=P, max_pages=page_table.shape[1], status=_ptr(status),
+                    src_page_table=_ptr(src_page_table), src_page_logical=_ptr(src_page_logical)),
+                 pos, page_table, page_logical, n_pages, ring, window, sink, status, src_page_table, src_page_logical)
 
 
 def ring_advance(args: RingArgs, stream=None) -> None:

@@ -324,6 +324,10 @@ rk_status rk_ring_advance(const rk_ring_args* a, rk_stream_t stream) {
   if (a->B == 0 || a->Hkv == 0) return RK_OK;
   if (!a->pos || !a->page_table || !a->page_logical || !a->n_pages || !a->ring || !a->window)
     return RK_ERR_INVALID_ARG;
+  if (!a->src_page_table != !a->src_page_logical) return RK_ERR_INVALID_ARG;   // both or neither
+  if (a->src_page_table && (a->src_page_table == a->page_table || a->src_page_logical == a->page_logical ||
+                            a->src_page_table == a->page_logical || a->src_page_logical == a->page_table))
+    return RK_ERR_INVALID_ARG;
   if (int64_t(a->B) * a->Hkv >= (int64_t(1) << 31) / 32) return RK_ERR_UNSUPPORTED;
   return rk::launch_ring_advance(*a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }

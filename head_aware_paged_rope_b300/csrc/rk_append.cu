@@ -71,9 +71,13 @@ __global__ __launch_bounds__(kWarps * 32) void append_kv_kernel(const rk_append_
 // after the sink pages) gives its physical page to it -- the window entries move down by
 // one and the new logical page takes the last entry.
 __global__ __launch_bounds__(kWarps * 32) void ring_advance_kernel(const rk_ring_args a) {
-  // the tables: earlier readers and writers are complete.  No early start for the kernels
-  // after this one: decode calls may read the tables before their predecessor completes
-  // (RK_ATTN_METADATA_STABLE), so nothing may start before these writes are done.
+  // In place, decode calls after this one may read the tables before their predecessor
+  // completes (RK_ATTN_METADATA_STABLE), so nothing after it starts before these writes are
+  // done.  Out of place, the destination is read only by later steps: the next kernels may
+  // start at once.  Either way the earlier readers and writers of the tables are complete
+  // before anything is written.
+  const bool copy = a.src_page_table != nullptr;
+  if (copy) sm100::grid_launch_dependents();
   sm100::grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = blockIdx.x * kWarps + warp;
@@ -87,34 +91,52 @@ __global__ __launch_bounds__(kWarps * 32) void ring_advance_kernel(const rk_ring
     if (lane == 0) report(a.status, RK_ERR_DEVICE_BOUNDS);
     return;
   }
-  int32_t* trow = a.page_table + int64_t(seg) * a.max_pages;
-  int32_t* lrow = a.page_logical + int64_t(seg) * a.max_pages;
+  const int64_t off = int64_t(seg) * a.max_pages;
+  int32_t* trow = a.page_table + off;
+  int32_t* lrow = a.page_logical + off;
+  const int32_t* st = copy ? a.src_page_table + off : trow;
+  const int32_t* sl = copy ? a.src_page_logical + off : lrow;
   const int lp = pos / a.P;
-  const int last = lrow[n - 1];
-  if (last >= lp) return;                     // the page is listed already
+  bool advance = sl[n - 1] < lp;              // else the page is listed already
   const int S = a.sink ? a.sink[seg] : 0;
   const int sink_pages = S > 0 ? (S - 1) / a.P + 1 : 0;
   int e_sink = 0;                             // leading entries that are sink pages
-  while (e_sink < n && lrow[e_sink] < sink_pages) ++e_sink;
-  const int W = a.window[seg];
-  // the ring is full and its oldest page lies wholly before the new token's window
-  const bool ok = n - e_sink == R && (int64_t(lrow[e_sink]) + 1) * a.P - 1 <= int64_t(pos) - W;
-  if (!ok) {
-    if (lane == 0) report(a.status, RK_ERR_DEVICE_BOUNDS);
-    return;
+  while (e_sink < n && sl[e_sink] < sink_pages) ++e_sink;
+  if (advance) {
+    const int W = a.window[seg];
+    // the ring is full and its oldest page lies wholly before the new token's window
+    const bool ok = n - e_sink == R && (int64_t(sl[e_sink]) + 1) * a.P - 1 <= int64_t(pos) - W;
+    if (!ok) {
+      if (lane == 0) report(a.status, RK_ERR_DEVICE_BOUNDS);
+      advance = false;                        // the list stays as it was
+    }
   }
-  const int phys = trow[e_sink];
-  for (int base = e_sink; base < n - 1; base += 32) {   // move entries down, 32 at a time
+  if (!copy && !advance) return;
+  const int phys = advance ? st[e_sink] : 0;
+  // entry e of the new list: the window entries move down by one and the freed page takes
+  // the new logical page (out of place, every entry is written); 32 entries at a time, all
+  // reads of a round before its writes
+  for (int base = copy ? 0 : e_sink; base < n; base += 32) {
     const int e = base + lane;
     int t = 0, l = 0;
-    if (e < n - 1) { t = trow[e + 1]; l = lrow[e + 1]; }
+    if (e < n) {
+      if (!advance || e < e_sink) {
+        t = st[e];
+        l = sl[e];
+      } else if (e < n - 1) {
+        t = st[e + 1];
+        l = sl[e + 1];
+      } else {
+        t = phys;
+        l = lp;
+      }
+    }
     __syncwarp();
-    if (e < n - 1) { trow[e] = t; lrow[e] = l; }
+    if (e < n) {
+      trow[e] = t;
+      lrow[e] = l;
+    }
     __syncwarp();
-  }
-  if (lane == 0) {
-    trow[n - 1] = phys;
-    lrow[n - 1] = lp;
   }
 }
 

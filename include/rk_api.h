@@ -335,6 +335,9 @@ typedef struct rk_ring_args {
   const int32_t* sink;         /* int32 [B*Hkv] sink S, or NULL for all zero */
   int32_t B, Hkv, P, max_pages;
   int32_t* status;             /* optional device int32 error word, may be NULL */
+  const int32_t* src_page_table;   /* or NULL (in place): int32 [B*Hkv][max_pages], the tables to
+                                      advance from; the advanced lists go to page_table */
+  const int32_t* src_page_logical; /* with src_page_table: int32 [B*Hkv][max_pages]; both or neither */
 } rk_ring_args;
 
 /* Advance the page ring of every head segment with ring[s] = R > 0.  Its list is the sink
@@ -347,7 +350,19 @@ typedef struct rk_ring_args {
  * their tables out as extra sequences.  Errors: RK_ERR_INVALID_ARG (NULL pointers with
  * B*Hkv > 0, negative sizes), RK_ERR_UNSUPPORTED (P), RK_ERR_CUDA; on the device, a ring
  * that is not full or whose oldest page is still inside the window, or n_pages outside
- * [1, max_pages], leaves that head segment unchanged and sets RK_ERR_DEVICE_BOUNDS. */
+ * [1, max_pages], leaves that head segment unchanged and sets RK_ERR_DEVICE_BOUNDS.
+ *
+ * Out of place (src_page_table / src_page_logical given): entries [0, n_pages) of every ring
+ * head's row are read from the source tables and written, advanced (or unchanged), to
+ * page_table / page_logical; rows of other head segments are neither read nor written, so
+ * both copies must hold them.  Source and destination must not overlap.  The call then lets
+ * the kernels after it start before it completes (programmatic dependent launch) and waits
+ * for the kernels before it only before it writes.  This serves double-buffered decode
+ * steps: before step s, advance step s's tables into the other buffer for step s + 1, then
+ * run step s's decode calls on step s's buffer.  The decode calls of step s + 1 may then
+ * pass RK_ATTN_METADATA_STABLE: each decode CTA holds a whole SM and waits for the kernel
+ * before it before it exits, so a kernel enqueued before the previous decode call's
+ * predecessor has completed whenever a decode call begins. */
 RK_API rk_status rk_ring_advance(const rk_ring_args* args, rk_stream_t stream);
 
 /* ------------------------------------------------------------------------------------

@@ -173,3 +173,14 @@ def test_argument_structs_keep_their_tensors_alive(rk):
     assert w() is not None and s._tensors == (w(),)
     for f in (B.attn_args, B.append_args, B.ring_args, B.sparse_ffn_args):
         assert "return _keep(" in inspect.getsource(f)
+
+
+def test_ring_advance_source_tables_both_or_neither_and_distinct(rk):
+    # host validation only: the pointers are never dereferenced on the host
+    a = rk.RingArgs(pos=1 << 20, page_table=2 << 20, page_logical=3 << 20, n_pages=4 << 20, ring=5 << 20,
+                    window=6 << 20, B=1, Hkv=1, P=16, max_pages=4, src_page_table=7 << 20)
+    assert rk.LIB.rk_ring_advance(ctypes.byref(a), None) == 1          # logical table missing
+    a.src_page_logical = 2 << 20                                       # the destination page table
+    assert rk.LIB.rk_ring_advance(ctypes.byref(a), None) == 1
+    a.src_page_table, a.src_page_logical = 2 << 20, 8 << 20              # source = destination
+    assert rk.LIB.rk_ring_advance(ctypes.byref(a), None) == 1

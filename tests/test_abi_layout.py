@@ -16,7 +16,7 @@ ATTN_FIELDS = ["q", "cu_seqlens_q", "seq_len", "k_pool", "v_pool", "n_pool_pages
 APPEND_FIELDS = ["k_new", "v_new", "pos", "k_pool", "v_pool", "n_pool_pages", "page_table", "page_logical", "n_pages",
                  "B", "Hkv", "d", "P", "max_pages", "status"]
 RING_FIELDS = ["pos", "page_table", "page_logical", "n_pages", "ring", "window", "sink", "B", "Hkv", "P", "max_pages",
-               "status"]
+               "status", "src_page_table", "src_page_logical"]
 ROPE_FIELDS = ["k_src", "n_src_pages", "k_dst", "n_dst_pages", "src_tables", "n_src_entries", "dst_tables",
                "n_dst_entries", "runs", "n_runs", "max_tok", "P", "d", "theta", "style", "status"]
 RUN_FIELDS = ["src_tab_off", "src_tab_len", "dst_tab_off", "dst_tab_len", "pos_off0", "pos_on0", "n_tok", "reserved"]

@@ -381,11 +381,12 @@ def test_decode_workspace_reused_across_shapes(rk):
             assert int(ws[256:28928].count_nonzero().item()) == 0
 
 
-def _ring_decode_steps(rk, w, kp, k_host, check_steps):
+def _ring_decode_steps(rk, w, kp, k_host, check_steps, double_buffered=False):
     """Decode with appended tokens over window-only local heads, as the 128K stack runs it:
     per step rk_ring_advance and rk_segpaged_decode (which stores the new token itself) on
     the GPU, and the oracle's ring and append on the host; the outputs of `check_steps`
-    are compared."""
+    are compared.  Double-buffered: step s decodes on buffer s % 2, and before it the
+    tables of step s + 1 are advanced out of place into the other buffer."""
     a = w.attn
     st = _status()
     dev = {k: to_device(v, "cuda") for k, v in dict(tab=w.dec_page_table, lg=w.dec_page_logical, n=w.dec_n_pages,
@@ -396,14 +397,23 @@ def _ring_decode_steps(rk, w, kp, k_host, check_steps):
     out = torch.empty((a.B, a.Hq, a.d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((a.B, a.Hq), dtype=torch.float32, device="cuda")
     ws = torch.zeros(DEC_WS_BYTES, dtype=torch.uint8, device="cuda")
-    for s in range(max(check_steps) + 1):
+    bufs = [(dev["tab"], dev["lg"]), (dev["tab"].clone(), dev["lg"].clone())]
+    last = max(check_steps)
+    for s in range(last + 1):
         pos = (a.seq_len + s).astype(np.int32)
         pos_d, seq_d = to_device(pos, "cuda"), to_device(pos + 1, "cuda")
-        rk.ring_advance(rk.ring_args(pos_d, dev["tab"], dev["lg"], dev["n"], dev["ring"], dev["window"], dev["sink"],
-                                     Hkv=a.Hkv, P=a.P, status=st))
+        cur = bufs[s % 2] if double_buffered else bufs[0]
+        if not double_buffered or s == 0:
+            rk.ring_advance(rk.ring_args(pos_d, cur[0], cur[1], dev["n"], dev["ring"], dev["window"], dev["sink"],
+                                         Hkv=a.Hkv, P=a.P, status=st))
+        if double_buffered and s < last:
+            nxt = bufs[(s + 1) % 2]
+            rk.ring_advance(rk.ring_args(to_device(pos + 1, "cuda"), nxt[0], nxt[1], dev["n"], dev["ring"],
+                                         dev["window"], dev["sink"], Hkv=a.Hkv, P=a.P, status=st,
+                                         src_page_table=cur[0], src_page_logical=cur[1]))
         q = to_device(w.decode_q[s], "cuda")
         kn, vn = to_device(w.decode_k[s], "cuda"), to_device(w.decode_v[s], "cuda")
-        rk.segpaged_decode(rk.attn_args(q, seq_d, kp, dev["vp"], dev["tab"], dev["lg"], dev["n"], dev["cls"],
+        rk.segpaged_decode(rk.attn_args(q, seq_d, kp, dev["vp"], cur[0], cur[1], dev["n"], dev["cls"],
                                         dev["window"], dev["sink"], out, lse=lse, status=st, total_q=a.B, max_q=1,
                                         flags=rk.RK_ATTN_METADATA_STABLE | rk.RK_ATTN_POOLS_STABLE, k_new=kn,
                                         v_new=vn), workspace=ws)
@@ -413,7 +423,7 @@ def _ring_decode_steps(rk, w, kp, k_host, check_steps):
         if s in check_steps:
             torch.cuda.synchronize()
             assert int(st.item()) == 0
-            assert np.array_equal(dev["tab"].cpu().numpy(), tab) and np.array_equal(dev["lg"].cpu().numpy(), lg)
+            assert np.array_equal(cur[0].cpu().numpy(), tab) and np.array_equal(cur[1].cpu().numpy(), lg)
             gk, gv = bf16_bits(kp), bf16_bits(dev["vp"])
             for h in range(a.Hkv):                   # this step's rows, at the slots the host's tables give
                 e = int(np.searchsorted(lg[h, :int(w.dec_n_pages[h])], int(pos[0]) // a.P))
@@ -425,14 +435,15 @@ def _ring_decode_steps(rk, w, kp, k_host, check_steps):
             _compare(d, out.float().cpu().numpy(), lse.cpu().numpy())
 
 
-def test_stack_small_prefill_then_decode(rk):
+@pytest.mark.parametrize("double_buffered", [False, True], ids=["in_place", "double_buffered"])
+def test_stack_small_prefill_then_decode(rk, double_buffered):
     w = synth.stack_layer(0, n_segments=4, seg_tokens=1024, n_suffix=100, n_decode=40)
     kp = _gpu_rope(rk, w)
     oracle_pool = _check_rope(w, bf16_bits(kp))
     a = dataclasses.replace(w.attn, k_pool=oracle_pool)
     out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
     _compare(a, out, lse)
-    _ring_decode_steps(rk, w, kp, oracle_pool, (0, 17, 39))
+    _ring_decode_steps(rk, w, kp, oracle_pool, (0, 17, 39), double_buffered)
 
 
 def test_stack_small_prestored_decode(rk):
@@ -480,7 +491,7 @@ def test_stack_layer_full_size_sampled(rk):
     a = dataclasses.replace(w.attn, k_pool=oracle_pool)
     out, lse = _gpu_attn(rk, w.attn, k_pool=kp)
     _compare(a, out, lse, rows=_sample_rows(a, 7, per_head=16))
-    _ring_decode_steps(rk, w, kp, oracle_pool, (0, 31, 63))
+    _ring_decode_steps(rk, w, kp, oracle_pool, (0, 31, 63), double_buffered=True)   # as the bench runs it
 
 
 # ------------------------------------------------------------------------- group sizes and pairings
