@@ -968,21 +968,29 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         tc_fence_before();
         mbar_arrive(smem_addr(&sh.s_empty[sb]));
         float x[NG], r[NG];
+        bool over = false;   // a key of this thread exceeds its head's running maximum by 2^8
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           x[g] = (vis && g < G) ? __uint_as_float(sv[g]) * scale : -INFINITY;
           r[g] = x[g];
+          over |= x[g] > m[g] + kRescale;
         }
-        const float wmax = warp_reduce_cols<NG, true>(r);
-        if (lane % LPC == 0) sh.red[gg & 1][warp][my_col] = wmax;
-        if (!named_bar_and(1, 128, got && good)) { ok = false; break; }
+        // The running maxima move only when a key exceeds them by more than 2^8, so the tile's
+        // maxima are needed only when some key does (always on a head's first visible key):
+        // one barrier reduction over the 128 threads settles it.  A failed wait takes the
+        // same branch, whose barrier then stops all of them.
         bool need = false;
         float mt[NG];
+        if (named_bar_or(1, 128, over || !(got && good))) {
+          const float wmax = warp_reduce_cols<NG, true>(r);
+          if (lane % LPC == 0) sh.red[gg & 1][warp][my_col] = wmax;
+          if (!named_bar_and(1, 128, got && good)) { ok = false; break; }
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          mt[g] = fmaxf(fmaxf(sh.red[gg & 1][0][g], sh.red[gg & 1][1][g]),
-                        fmaxf(sh.red[gg & 1][2][g], sh.red[gg & 1][3][g]));
-          need |= mt[g] > m[g] + kRescale;
+          for (int g = 0; g < NG; ++g) {
+            mt[g] = fmaxf(fmaxf(sh.red[gg & 1][0][g], sh.red[gg & 1][1][g]),
+                          fmaxf(sh.red[gg & 1][2][g], sh.red[gg & 1][3][g]));
+            need |= mt[g] > m[g] + kRescale;
+          }
         }
         if (need) {   // uniform across the 128 threads
           float alpha[NG];

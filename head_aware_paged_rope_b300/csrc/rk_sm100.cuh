@@ -223,6 +223,14 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
       : "=r"(out) : "r"(uint32_t(pred)), "r"(id), "r"(nthreads) : "memory");
   return out != 0;
 }
+// Barrier of nthreads threads that also returns whether pred held for any of them.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}"
+      : "=r"(out) : "r"(uint32_t(pred)), "r"(id), "r"(nthreads) : "memory");
+  return out != 0;
+}
 // Programmatic dependent launch: wait for the preceding grid's completion (and its memory),
 // and allow the next grid in the stream to begin launching.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
