@@ -77,7 +77,9 @@ struct DecLayout {
   static constexpr int kV = kP + 2 * 4096;                      // V stages, then K stages: for D = 64
   static constexpr int kK = kV + kStages * kStageBytes;         // V^T's second M half reads past a V stage
   static constexpr int kPlan = kK + kStages * kStageBytes;      // single-launch path: per-segment ranges
-  static constexpr int kBytes = kPlan + kDecFusedSegs * 16;
+  static constexpr int kOrder = kPlan + kDecFusedSegs * 16;     // single-launch path: segment at each sequence
+  static constexpr int kRank = kOrder + kDecFusedSegs * 2;      // position, and the position of each segment
+  static constexpr int kBytes = kRank + kDecFusedSegs * 2;
   static constexpr int kSmem = kBytes + 1024;
 };
 
@@ -111,8 +113,9 @@ struct DecShared {
   uint32_t tmem_slot;
   int abort;
   int T, gs, seg_first, last;   // single-launch path: the schedule, and "this CTA merges the splits"
-  int tb, te, aligned, max_nt;
+  int tb, te, aligned, max_nt, long_first;
   int s_warp[32];
+  unsigned long long s_warp64[32];
 };
 
 __device__ __forceinline__ bool aborted(DecShared& sh) { return *reinterpret_cast<volatile int*>(&sh.abort) != 0; }
@@ -193,6 +196,7 @@ __device__ __forceinline__ float warp_reduce_cols(float (&v)[NG]) {
 constexpr int kMergeFan = 12;   // partials one CTA merges at a time (single-launch path)
 constexpr int kAlignTiles = 8;  // all segments this short and no more of them than CTAs: one segment per CTA
 constexpr int kShortTiles = 8;  // single-launch path: segments this short are never split
+constexpr int kLateShares = 8;  // short segments go last when they fill at most this many shares
 
 // Partial slot of CTA c for a split segment (two per CTA: its first and its last portion):
 // c's portion of the segment is its first one unless c = cta0 and c's share began in an
@@ -206,17 +210,20 @@ __device__ __forceinline__ int split_slot(int c, int cta0, int c0_later) {
 // its start).  Monotone in c, so the shares stay disjoint and cover [0, T).  A tile of a
 // longer segment belongs to the same CTA as without the move: cuts inside it are not
 // moved, and cuts moved within other segments stay on their side of it.  plan[s].w is
-// the first tile of segment s, plan[s].z its visible entries.
-__device__ __forceinline__ int share_cut(int c, long long T, long long gs, const int4* plan, int nseg, int ept) {
+// the first tile of segment s in the sequence, plan[s].z its visible entries, order[i] the
+// segment at sequence position i (or, with order NULL, segment i).
+__device__ __forceinline__ int share_cut(int c, long long T, long long gs, const int4* plan, const int16_t* order,
+                                         int nseg, int ept) {
   if (c <= 0) return 0;
   if (c >= gs) return int(T);
   const int raw = int((long long)c * T / gs);
-  int lo = 0, hi = nseg - 1;   // last segment whose first tile is <= raw
+  int lo = 0, hi = nseg - 1;   // last sequence position whose segment starts at or before raw
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (plan[mid].w <= raw) lo = mid; else hi = mid - 1;
+    if (plan[order ? order[mid] : mid].w <= raw) lo = mid; else hi = mid - 1;
   }
-  const int t0 = plan[lo].w, nt = (plan[lo].z + ept - 1) / ept;
+  const int s = order ? order[lo] : lo;
+  const int t0 = plan[s].w, nt = (plan[s].z + ept - 1) / ept;
   if (raw <= t0 || raw >= t0 + nt || nt > kShortTiles) return raw;
   return raw - t0 <= t0 + nt - raw ? t0 : t0 + nt;
 }
@@ -387,8 +394,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
 
   if constexpr (FUSED) {
     // ---------------------------------------------------------------- plan (every CTA alike)
-    // Thread i takes segments [i*per, i*per + per) (per <= 3), finds their visible ranges in
-    // three interleaved rounds of loads, and a block scan of their tile counts gives each
+    // Thread i takes segments [i*per, i*per + per) (per <= 2), finds their visible ranges in
+    // three interleaved rounds of loads, and block scans of their tile counts give each
     // segment's first tile; the share of this CTA follows as in the separate planner.
     int4* plan = reinterpret_cast<int4*>(smem + LY::kPlan);
     constexpr int kPer = (kDecFusedSegs + kThreads - 1) / kThreads;
@@ -401,38 +408,62 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     for (int i = 0; i < kPer; ++i) if (i < per && s0 + i < nseg) rr[i].load2();
 #pragma unroll
     for (int i = 0; i < kPer; ++i) if (i < per && s0 + i < nseg) rr[i].load3(p);
-    int nt[kPer], sum = 0, mx = 0;
+    // When the short segments (at most kShortTiles tiles: the windows of local heads) fill
+    // only the last few shares, the sequence of tiles holds the longer segments first and the
+    // short ones after them, each class in segment order: the CTAs dispatched last (whose SMs
+    // the preceding call still holds, so they start late) then hold whole short segments,
+    // and the pieces of long segments, which must all be done before their merge, go to CTAs
+    // that start on time.  Otherwise (many windows: they would load the late CTAs with many
+    // portions) the sequence is in segment order.  order[] / rank[] map sequence positions
+    // and segments.  One scan counts, per thread's segments: short tiles (bits 0-12), long
+    // segments (bits 13-22) and long tiles (bits 32-63).
+    int nt[kPer], mx = 0;
+    unsigned long long pk = 0;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
       nt[i] = 0;
       if (i < per && s0 + i < nseg) {
         rr[i].finish();
         nt[i] = (rr[i].n_vis + EPT - 1) / EPT;
+        pk += nt[i] > kShortTiles ? (unsigned long long)nt[i] << 32 | (1ull << 13) : (unsigned long long)nt[i];
       }
-      sum += nt[i];
       mx = max(mx, nt[i]);
     }
     if (mx > 0) atomicMax(&sh.max_nt, mx);   // read after the scan's barriers
-    int T;
-    int t0 = block_exclusive_scan(sum, &T, sh.s_warp);
+    unsigned long long PK;
+    const unsigned long long q0 = block_exclusive_scan64(pk, &PK, sh.s_warp64);
+    const int TL = int(PK >> 32), TS = int(PK & 0x1fff), n_long = int((PK >> 13) & 0x3ff);
+    const int T = TL + TS;
+    const int l0 = int(q0 >> 32), s_tiles0 = int(q0 & 0x1fff), l_segs0 = int((q0 >> 13) & 0x3ff);
+    const bool long_first = (long long)TS * min(int(gridDim.x), max(T, 1)) <= (long long)kLateShares * T;
+    int16_t* order = reinterpret_cast<int16_t*>(smem + LY::kOrder);
+    int16_t* rank = reinterpret_cast<int16_t*>(smem + LY::kRank);
     // Few, short segments (at most kAlignTiles tiles each, no more segments than CTAs): CTA c
     // takes segment c whole, so nothing is split.  Otherwise the equal shares.
     const bool aligned = sh.max_nt <= kAlignTiles && nseg <= int(gridDim.x);
     const int gs = min(int(gridDim.x), T);
     const int c = blockIdx.x;
     {
-      int t1 = t0;
+      // running first tile and sequence position of this thread's next long / short segment
+      // (in segment order: of its next segment)
+      int lt = l0, st = TL + s_tiles0, lr = l_segs0, sr = s0 - l_segs0, it = l0 + s_tiles0;
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         const int seg = s0 + i;
         if (i < per && seg < nseg) {
+          const bool lg = nt[i] > kShortTiles;
+          const int t1 = !long_first ? it : lg ? lt : st;
+          const int r = !long_first ? seg : lg ? lr : n_long + sr;
+          it += nt[i];
           plan[seg] = make_int4(rr[i].e_sink, rr[i].e_w, rr[i].n_vis, t1);
+          order[r] = int16_t(seg);
+          rank[seg] = int16_t(r);
           if (aligned && seg == c) {
             sh.tb = nt[i] > 0 ? t1 : T;
             sh.te = nt[i] > 0 ? t1 + nt[i] : T;
             sh.seg_first = seg;
           }
-          t1 += nt[i];
+          if (lg) { lt += nt[i]; ++lr; } else { st += nt[i]; ++sr; }
         }
       }
     }
@@ -440,20 +471,21 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       sh.T = T;
       sh.gs = gs;
       sh.aligned = aligned;
+      sh.long_first = long_first;
       if (aligned && c >= nseg) sh.tb = sh.te = T;
     }
     __syncthreads();
     if (!aligned) {
       if (tid == 0) {
-        sh.tb = share_cut(c, T, gs, plan, nseg, EPT);
-        sh.te = share_cut(c + 1, T, gs, plan, nseg, EPT);
+        sh.tb = share_cut(c, T, gs, plan, long_first ? order : nullptr, nseg, EPT);
+        sh.te = share_cut(c + 1, T, gs, plan, long_first ? order : nullptr, nseg, EPT);
       }
       __syncthreads();
       const int tb = sh.tb;
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        if (i < per && s0 + i < nseg && nt[i] > 0 && t0 <= tb && tb < t0 + nt[i]) sh.seg_first = s0 + i;
-        t0 += nt[i];
+        const int seg = s0 + i;
+        if (i < per && seg < nseg && nt[i] > 0 && plan[seg].w <= tb && tb < plan[seg].w + nt[i]) sh.seg_first = seg;
       }
     }
     __syncthreads();
@@ -471,6 +503,19 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     }
     int seg = my.seg0, t = my.tile_begin;
     const int t_end = my.tile_end;
+    // the segment after s in the tile sequence (single launch: long segments first)
+    const bool reordered = FUSED && sh.long_first;
+    const int16_t* order = reordered ? reinterpret_cast<const int16_t*>(smem + LY::kOrder) : nullptr;
+    const int16_t* rank = reinterpret_cast<const int16_t*>(smem + LY::kRank);
+    auto next_seg = [&](int s) -> int {
+      if (reordered) {
+        if (s >= nseg) return nseg;
+        const int r = rank[s] + 1;
+        return r < nseg ? int(order[r]) : nseg;
+      } else {
+        return s + 1;
+      }
+    };
     // raw page id / logical page of entry v_begin + grp*32 + lane of segment s (present: listed)
     auto fetch = [&](int s, const DecSeg& sd, int v_begin, int v_end, int grp, int& raw_page, int& raw_lp,
                      int& raw_rot, bool& present) {
@@ -512,7 +557,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           const int c1 = cut ? int((((long long)d.tile0 + d.n_tiles) * gs + T - 1) / T) - 1 : s;
           d.cta0 = c0;
           d.n_splits = c1 - c0 + 1;
-          d.slot0 = (cut && c1 > c0) ? int(share_cut(c0, T, gs, s_plan, nseg, EPT) < d.tile0) : 0;   // c0_later
+          d.slot0 = (cut && c1 > c0) ? int(share_cut(c0, T, gs, s_plan, order, nseg, EPT) < d.tile0) : 0;   // c0_later
         } else {
           d = ws.segs[s];
         }
@@ -530,7 +575,10 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     uint32_t last_q_parity = 0;
     bool ok = true;
     DecSeg cur = load_seg(t < t_end ? seg : nseg);
-    while (t < t_end && cur.n_tiles == 0 && seg < nseg) cur = load_seg(++seg);
+    while (t < t_end && cur.n_tiles == 0 && seg < nseg) {
+      seg = next_seg(seg);
+      cur = load_seg(seg);
+    }
     int raw_page, raw_lp, raw_rot;
     bool present;
     fetch(seg, cur, (t < t_end && seg < nseg) ? (t - cur.tile0) * EPT : 0, cur.n_vis, 0, raw_page, raw_lp, raw_rot,
@@ -582,7 +630,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       if (!live) break;
       // the next segment's record, used when this portion's last group is issued
       const bool more = cur.tile0 + lt1 < t_end;
-      int nseg_idx = seg + 1;
+      int nseg_idx = next_seg(seg);
       DecSeg nxt = load_seg(more ? nseg_idx : nseg);
       bool q_done = false;
       // Q rows of the group -> buffer qn & 1, free once the MMAs of portion qn - 2 are done
@@ -619,7 +667,10 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
         if (grp + 1 < n_grp) {
           fetch(seg, cur, po.v_begin, po.v_end, grp + 1, raw_page_n, raw_lp_n, raw_rot_n, present_n);
         } else if (more) {
-          while (nxt.n_tiles == 0 && nseg_idx < nseg) nxt = load_seg(++nseg_idx);   // segments with nothing visible
+          while (nxt.n_tiles == 0 && nseg_idx < nseg) {   // segments with nothing visible
+            nseg_idx = next_seg(nseg_idx);
+            nxt = load_seg(nseg_idx);
+          }
           fetch(nseg_idx, nxt, 0, nxt.n_vis, 0, raw_page_n, raw_lp_n, raw_rot_n, present_n);
         } else {
           raw_page_n = raw_lp_n = raw_rot_n = -1;

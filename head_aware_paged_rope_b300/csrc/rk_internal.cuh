@@ -321,6 +321,35 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_wa
   return base + x - v;
 }
 
+// The same for one 64-bit value per thread (several counts packed in bit fields, none of
+// which may carry into the next); s_warp holds 32 values.
+__device__ __forceinline__ unsigned long long block_exclusive_scan64(unsigned long long v, unsigned long long* total,
+                                                                     unsigned long long* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = lane < (blockDim.x >> 5) ? s_warp[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;   // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  const unsigned long long base = warp ? s_warp[warp - 1] : 0ull;
+  *total = s_warp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Launch configuration with programmatic dependent launch: the kernel may be scheduled

@@ -18,7 +18,29 @@ def owner(t, T, gs):
     return ((t + 1) * gs + T - 1) // T - 1
 
 
-def share_cut(c, T, gs, tile0, nt):
+LATE_SHARES = 8     # kLateShares
+
+
+def sequence(nt, grid):
+    """The single-launch tile sequence: when the short segments fill at most LATE_SHARES
+    shares, segments of more than SHORT tiles first, then the others, each class in segment
+    order; else segment order.  Returns (order, tile0) -- the segment at each sequence
+    position and the first tile of each segment."""
+    nt = np.asarray(nt, dtype=np.int64)
+    T, TS = int(nt.sum()), int(nt[nt <= SHORT].sum())
+    if TS * min(grid, max(T, 1)) <= LATE_SHARES * T:
+        order = [s for s in range(len(nt)) if nt[s] > SHORT] + [s for s in range(len(nt)) if nt[s] <= SHORT]
+    else:
+        order = list(range(len(nt)))
+    tile0 = np.zeros(len(nt), np.int64)
+    t = 0
+    for s in order:
+        tile0[s] = t
+        t += nt[s]
+    return np.array(order), tile0
+
+
+def share_cut(c, T, gs, tile0, nt, order):
     """First tile of CTA c's share: c*T/gs, moved to the nearer end (ties: its start) of the
     segment it falls in when that segment has at most SHORT tiles."""
     if c <= 0:
@@ -26,7 +48,8 @@ def share_cut(c, T, gs, tile0, nt):
     if c >= gs:
         return T
     raw = c * T // gs
-    s = int(np.searchsorted(tile0, raw, side="right")) - 1        # last segment with tile0 <= raw
+    pos = int(np.searchsorted(tile0[order], raw, side="right")) - 1   # last position starting <= raw
+    s = int(order[pos])
     t0, n = int(tile0[s]), int(nt[s])
     if raw <= t0 or raw >= t0 + n or n > SHORT:
         return raw
@@ -42,10 +65,10 @@ def decode_schedule(nt, grid):
     (segment, CTA) piece of the shares: the slot the producer gives it (2c for the CTA's
     first portion, 2c+1 for a later one)."""
     nt = np.asarray(nt, dtype=np.int64)
-    tile0 = np.concatenate([[0], np.cumsum(nt)[:-1]])
+    order, tile0 = sequence(nt, grid)
     T = int(nt.sum())
     gs = min(grid, T)
-    cuts = [share_cut(c, T, gs, tile0, nt) for c in range(gs + 1)]
+    cuts = [share_cut(c, T, gs, tile0, nt, order) for c in range(gs + 1)]
     segs, pieces = [], {}
     for s, (t0, n) in enumerate(zip(tile0, nt)):
         if n == 0:
@@ -60,7 +83,8 @@ def decode_schedule(nt, grid):
     for c in range(gs):
         tb, te = cuts[c], cuts[c + 1]
         first = True
-        for s, (t0, n) in enumerate(zip(tile0, nt)):
+        for s in order:                                       # the share's segments in sequence order
+            t0, n = tile0[s], nt[s]
             if n == 0 or t0 + n <= tb or t0 >= te:
                 continue
             pieces[(s, c)] = 2 * c + (0 if first else 1)
@@ -87,7 +111,7 @@ def test_decode_shares_slots_and_counters(seed):
     T, gs, cuts, segs, pieces = decode_schedule(nt, grid)
     # the cuts are monotone and the shares tile [0, T)
     assert cuts[0] == 0 and cuts[-1] == T and all(a <= b for a, b in zip(cuts, cuts[1:]))
-    tile0 = np.concatenate([[0], np.cumsum(nt)[:-1]])
+    _, tile0 = sequence(nt, grid)
     for s, (t0, n) in enumerate(zip(tile0, nt)):
         held = [c for c in range(gs) if n and cuts[c] < t0 + n and cuts[c + 1] > t0]
         if n == 0:
@@ -129,6 +153,26 @@ def test_decode_shares_slots_and_counters(seed):
             t0, c0, n, later = rec
             assert sorted(v for (ss, c), v in split_slots.items() if ss == s) == \
                 sorted(split_slot(c, c0, later) for c in range(c0, c0 + n))
+
+
+def test_long_segments_come_first_so_the_last_ctas_hold_only_windows():
+    # a 128K-stack layer with a global head: 1024 tiles of it and seven 5-tile windows over
+    # 148 CTAs; the CTAs dispatched last take windows, never a piece of the global head
+    nt = [5] * 8
+    nt[3] = 1024
+    T, gs, cuts, segs, pieces = decode_schedule(nt, 148)
+    order, tile0 = sequence(nt, 148)
+    assert list(order[:1]) == [3] and tile0[3] == 0
+    last = [c for (s, c) in pieces if s != 3]
+    assert min(last) > max(c for (s, c) in pieces if s == 3) - 1 and max(last) == gs - 1
+
+
+def test_many_windows_keep_segment_order():
+    # the decode microbenchmark: 32 global heads of 64 tiles and 224 windows of 3 -- the
+    # windows would fill 36 shares, so the sequence stays in segment order
+    nt = np.tile([64] + [3] * 7, 32)
+    order, tile0 = sequence(nt, 148)
+    assert list(order) == list(range(len(nt)))
 
 
 def test_short_windows_stay_whole_on_a_local_only_layer():
