@@ -131,6 +131,7 @@ struct GemmShared {
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_slot;
   int abort;
+  int last;   // this CTA holds the last piece of a split tile
 };
 
 __device__ __forceinline__ bool g_aborted(GemmShared& sh) { return *reinterpret_cast<volatile int*>(&sh.abort) != 0; }
@@ -154,6 +155,13 @@ struct GemmParams {
   const int32_t* rows;      // MODE 1: output row of each M row (the kept tokens)
   int ldc;
   int32_t* status;
+  // MODE 1, last wave split along K: tiles [n_full, tiles) are cut into `split` pieces each;
+  // every piece adds its fp32 tile into part[tail tile] (laid out [kDownN / 4][kBM] float4,
+  // zero at the start), and the piece that takes the last ticket of its tile (tickets[tail
+  // tile], zero at the start) converts the sum and scatters the rows
+  int n_full, split;
+  float* part;
+  int32_t* tickets;
 };
 
 __device__ __forceinline__ float silu(float g) {
@@ -178,6 +186,25 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
   constexpr int kLoadBytes = kATile + kMmaN * kBK * 2;
   const int m_tiles = (g.M + kBM - 1) / kBM, n_tiles = g.N / kTileN, k_steps = g.K / kBK;
   const int n_work = m_tiles * n_tiles;
+  const bool split = MODE == 1 && g.split > 1;
+  const int n_units = split ? g.n_full + (n_work - g.n_full) * g.split : n_work;
+  // unit w: output tile `tile` (its row and column blocks m, n), K steps [kb, ke), and its
+  // piece index (-1: the whole tile)
+  auto unit = [&](int w, int& tile, int& m, int& n, int& kb, int& ke, int& piece) {
+    tile = w;
+    piece = -1;
+    kb = 0;
+    ke = k_steps;
+    if (split && w >= g.n_full) {
+      const int q = (w - g.n_full) / g.split;
+      piece = (w - g.n_full) - q * g.split;
+      tile = g.n_full + q;
+      kb = int((long long)piece * k_steps / g.split);
+      ke = int((long long)(piece + 1) * k_steps / g.split);
+    }
+    n = tile / m_tiles;
+    m = tile - n * m_tiles;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -213,9 +240,10 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
       bool ok = true;
       int last = -1;
       uint32_t last_par = 0;
-      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
-        const int n = w / m_tiles, m = w - n * m_tiles;
-        for (int ks = 0; ks < k_steps; ++ks, ++it) {
+      for (int w = blockIdx.x; ok && w < n_units; w += gridDim.x) {
+        int tile, m, n, kb, ke, piece;
+        unit(w, tile, m, n, kb, ke, piece);
+        for (int ks = kb; ks < ke; ++ks, ++it) {
           const int s = it % kStages;
           if (it >= kStages && !g_wait(sh, smem_addr(&sh.empty[s]), ((it / kStages) - 1) & 1)) { ok = false; break; }
           const uint32_t bar = smem_addr(&sh.full[s]);
@@ -240,11 +268,13 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++tcount) {
+      for (int w = blockIdx.x; ok && w < n_units; w += gridDim.x, ++tcount) {
         const int a = tcount & 1;
+        int tile, m, n, kb, ke, piece;
+        unit(w, tile, m, n, kb, ke, piece);
         if (tcount >= 2 && !g_wait(sh, smem_addr(&sh.acc_empty[a]), ((tcount >> 1) - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        for (int ks = 0; ks < k_steps; ++ks, ++it) {
+        for (int ks = kb; ks < ke; ++ks, ++it) {
           const int s = it % kStages;
           if (!g_wait(sh, smem_addr(&sh.full[s]), (it / kStages) & 1)) { ok = false; break; }
           tc_fence_after();
@@ -253,7 +283,7 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t da = desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t db = desc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_f16(tmem + a * kBN, da, db, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_f16(tmem + a * kBN, da, db, kIdesc, (ks > kb || kk > 0) ? 1u : 0u);
           }
           tc_commit(smem_addr(&sh.empty[s]));
         }
@@ -268,8 +298,9 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     uint32_t tcount = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++tcount) {
-      const int n = w / m_tiles, m = w - n * m_tiles;
+    for (int w = blockIdx.x; w < n_units; w += gridDim.x, ++tcount) {
+      int tile, m, n, kb, ke, piece;
+      unit(w, tile, m, n, kb, ke, piece);
       const int a = tcount & 1;
       const bool got = g_wait(sh, smem_addr(&sh.acc_full[a]), (tcount >> 1) & 1);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -300,6 +331,52 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
             }
           }
         }
+      } else if (piece >= 0) {
+        // a piece of a split tile: added into the tile's fp32 sum, column blocks of 4 with the
+        // rows adjacent, so that a warp's 32 rows touch 512 contiguous bytes
+        const int q = tile - g.n_full;
+        float4* acc = reinterpret_cast<float4*>(g.part) + int64_t(q) * (kDownN / 4) * kBM + r;
+#pragma unroll 1
+        for (int c = 0; c < kTileN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + a * kBN + c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            atomicAdd(acc + ((c + i) / 4) * kBM, make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                               __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])));
+        }
+        tc_fence_before();
+        mbar_arrive(smem_addr(&sh.acc_empty[a]));   // the accumulator is free; the sum is in memory
+        __threadfence();                              // the additions are visible before the ticket
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (r == 0) sh.last = atomicAdd(g.tickets + q, 1) == g.split - 1;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (sh.last) {   // every piece is added: convert the sum and scatter the rows
+          __threadfence();
+          if (live) {
+            const int orow = __ldg(g.rows + row);
+            __nv_bfloat16* dst = g.c + int64_t(orow) * g.ldc + n * kTileN;
+#pragma unroll 1
+            for (int c4 = 0; c4 < kTileN / 4; c4 += 16) {   // 16 loads in flight
+              float4 x[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) x[i] = __ldcg(acc + (c4 + i) * kBM);
+#pragma unroll
+              for (int i = 0; i < 16; i += 2) {
+                uint4 o;
+                o.x = pack_bf16(x[i].x, x[i].y);
+                o.y = pack_bf16(x[i].z, x[i].w);
+                o.z = pack_bf16(x[i + 1].x, x[i + 1].y);
+                o.w = pack_bf16(x[i + 1].z, x[i + 1].w);
+                *reinterpret_cast<uint4*>(dst + (c4 + i) * 4) = o;
+              }
+            }
+          }
+          if (r == 0) g.tickets[q] = 0;   // for the next call
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // sh.last is rewritten by the next piece
+        continue;
       } else {
         const int orow = live ? __ldg(g.rows + row) : 0;
         __nv_bfloat16* dst = g.c + int64_t(orow) * g.ldc + n * kTileN;
@@ -335,7 +412,7 @@ __global__ __launch_bounds__(kGThreads, 1) void ffn_gemm_kernel(const __grid_con
 }
 
 template <int MODE>
-cudaError_t launch_gemm(const void* A, int lda_rows, const void* B0, const void* B1, int b_rows, const GemmParams& g,
+cudaError_t launch_gemm(const void* A, int lda_rows, const void* B0, const void* B1, int b_rows, GemmParams g,
                         cudaStream_t stream) {
   CUtensorMap ma, mb0, mb1;
   const cuuint64_t adims[2] = {cuuint64_t(g.K), cuuint64_t(lda_rows)};
@@ -355,7 +432,23 @@ cudaError_t launch_gemm(const void* A, int lda_rows, const void* B0, const void*
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int tiles = ((g.M + kBM - 1) / kBM) * (g.N / (MODE == 0 ? kBN / 2 : kDownN));
-  const int grid = std::max(1, std::min(tiles, device_sm_count()));
+  const int sms = device_sm_count();
+  int units = tiles;
+  g.n_full = tiles;
+  g.split = 0;
+  if (MODE == 1 && g.part) {
+    // the tiles of an incomplete last wave are cut along K so that it fills the SMs (each
+    // piece at least 4 K steps): R tiles x S pieces <= the SMs, partials in part / tickets
+    const int R = tiles % sms, S = R > 0 ? std::min(sms / R, (g.K / kBK) / 4) : 0;
+    if (S >= 2) {
+      g.n_full = tiles - R;
+      g.split = S;
+      units = g.n_full + R * S;
+      const cudaError_t e = cudaMemsetAsync(g.part, 0, size_t(R) * kBM * kDownN * sizeof(float), stream);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  const int grid = std::max(1, std::min(units, sms));
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kGThreads), kGSmem, stream, attr);
   return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<MODE>, ma, mb0, mb1, g);
@@ -363,16 +456,29 @@ cudaError_t launch_gemm(const void* A, int lda_rows, const void* B0, const void*
 
 }  // namespace
 
+// Workspace: gathered rows [keep][d_model] and activation [keep][d_ff] (bf16), then the fp32
+// partial tiles of a split last wave of the down projection (at most one per SM) and their
+// tickets.
 size_t sparse_ffn_ws_bytes(int keep, int d_model, int d_ff) {
-  return align256(size_t(keep) * d_model * 2) + align256(size_t(keep) * d_ff * 2);
+  const size_t sms = size_t(device_sm_count());
+  return align256(size_t(keep) * d_model * 2) + align256(size_t(keep) * d_ff * 2) +
+         align256(sms * kBM * kDownN * sizeof(float)) + align256(sms * sizeof(int32_t));
 }
 
 cudaError_t launch_sparse_ffn(const rk_sparse_ffn_args& a, void* ws, cudaStream_t stream) {
   uint8_t* base = static_cast<uint8_t*>(ws);
+  const size_t sms = size_t(device_sm_count());
+  const size_t off_act = align256(size_t(a.keep) * a.d_model * 2);
+  const size_t off_part = off_act + align256(size_t(a.keep) * a.d_ff * 2);
+  const size_t off_tick = off_part + align256(sms * kBM * kDownN * sizeof(float));
   __nv_bfloat16* x_sel = reinterpret_cast<__nv_bfloat16*>(base);
-  __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(base + align256(size_t(a.keep) * a.d_model * 2));
+  __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(base + off_act);
+  float* part = reinterpret_cast<float*>(base + off_part);
+  int32_t* tickets = reinterpret_cast<int32_t*>(base + off_tick);
   cudaError_t e = cudaMemsetAsync(a.out, 0, size_t(a.T) * a.d_model * 2, stream);   // skipped tokens: zero
   if (e != cudaSuccess || a.keep == 0) return e;
+  e = cudaMemsetAsync(tickets, 0, sms * sizeof(int32_t), stream);
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pdl_config(dim3(1), dim3(kSelThreads), 0, stream, attr);
   e = cudaLaunchKernelEx(&cfg, select_kernel, a.importance, a.T, a.keep, a.kept);
@@ -385,10 +491,11 @@ cudaError_t launch_sparse_ffn(const rk_sparse_ffn_args& a, void* ws, cudaStream_
   e = cudaLaunchKernelEx(&cfg2, gather_kernel, static_cast<const uint4*>(a.x), static_cast<const int32_t*>(a.kept),
                          a.keep, row16, reinterpret_cast<uint4*>(x_sel));
   if (e != cudaSuccess) return e;
-  GemmParams g1{a.keep, a.d_ff, a.d_model, act, nullptr, a.d_ff, a.status};
+  GemmParams g1{a.keep, a.d_ff, a.d_model, act, nullptr, a.d_ff, a.status, 0, 0, nullptr, nullptr};
   e = launch_gemm<0>(x_sel, a.keep, a.w_gate, a.w_up, a.d_ff, g1, stream);
   if (e != cudaSuccess) return e;
-  GemmParams g2{a.keep, a.d_model, a.d_ff, static_cast<__nv_bfloat16*>(a.out), a.kept, a.d_model, a.status};
+  GemmParams g2{a.keep, a.d_model, a.d_ff, static_cast<__nv_bfloat16*>(a.out), a.kept, a.d_model, a.status,
+                0, 0, part, tickets};
   return launch_gemm<1>(act, a.keep, a.w_down, nullptr, a.d_model, g2, stream);
 }
 

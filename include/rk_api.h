@@ -392,7 +392,12 @@ typedef struct rk_sparse_ffn_args {
   int32_t* status;           /* optional device int32 error word, may be NULL */
 } rk_sparse_ffn_args;
 
-/* Workspace bytes: the gathered rows and the activation ([keep][d_model] + [keep][d_ff] bf16). */
+/* Workspace bytes: the gathered rows and the activation ([keep][d_model] + [keep][d_ff] bf16),
+ * then fp32 sums of output tiles (128 x 256, at most one per SM of the current device) for
+ * the down projection, which splits an incomplete last wave of output tiles along K, and
+ * their tickets.  The pieces of a split tile are added with atomic additions, so the bf16
+ * rounding of those rows may differ by one unit between calls.  Query the size on the
+ * device the call will run on. */
 RK_API size_t rk_sparse_ffn_workspace_size(const rk_sparse_ffn_args* args);
 
 /* Errors: RK_ERR_INVALID_ARG (NULL pointers, sizes out of range, pointers not 16-byte
