@@ -66,6 +66,7 @@ constexpr uint32_t kColO = 32;
 constexpr int kHalfBytes = kKeys * 128; // one [128 keys][64 channels] bf16 box column
 constexpr int kGrp = 32;                // list entries whose page ids the producer warp loads at once
 constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr int kMaxTaperGrid = 256;  // tapered shares on grids up to this size
 
 template <int D>
 struct DecLayout {
@@ -114,6 +115,8 @@ struct DecShared {
   int abort;
   int T, gs, seg_first, last;   // single-launch path: the schedule, and "this CTA merges the splits"
   int tb, te, aligned, max_nt, long_first;
+  int taper;                    // tapered shares (0: equal shares); their raw cuts:
+  int cuts[kMaxTaperGrid + 1];
   int s_warp[32];
   unsigned long long s_warp64[32];
 };
@@ -197,6 +200,8 @@ constexpr int kMergeFan = 12;   // partials one CTA merges at a time (single-lau
 constexpr int kAlignTiles = 8;  // all segments this short and no more of them than CTAs: one segment per CTA
 constexpr int kShortTiles = 8;  // single-launch path: segments this short are never split
 constexpr int kLateShares = 8;  // short segments go last when they fill at most this many shares
+constexpr int kTaperDiv = 6;    // with early start the last gs / kTaperDiv shares shrink linearly,
+constexpr int kTaperPct = 40;   // the last one by this many per cent of a full share
 
 // Partial slot of CTA c for a split segment (two per CTA: its first and its last portion):
 // c's portion of the segment is its first one unless c = cta0 and c's share began in an
@@ -205,18 +210,53 @@ __device__ __forceinline__ int split_slot(int c, int cta0, int c0_later) {
   return (c == cta0 && c0_later) ? 2 * c + 1 : 2 * c;
 }
 
-// First tile of CTA c's share on the single-launch path: c*T/gs, moved to the nearer end
-// of the segment it falls in when that segment has at most kShortTiles tiles (ties go to
-// its start).  Monotone in c, so the shares stay disjoint and cover [0, T).  A tile of a
-// longer segment belongs to the same CTA as without the move: cuts inside it are not
-// moved, and cuts moved within other segments stay on their side of it.  plan[s].w is
-// the first tile of segment s in the sequence, plan[s].z its visible entries, order[i] the
-// segment at sequence position i (or, with order NULL, segment i).
-__device__ __forceinline__ int share_cut(int c, long long T, long long gs, const int4* plan, const int16_t* order,
-                                         int nseg, int ept) {
+// Tapered shares.  With early start the CTAs are dispatched in index order as the SMs of
+// the preceding call free up, and the last of them start several microseconds late (their
+// SMs run that call's last CTAs, which also merge).  So the last L shares shrink linearly:
+// share i < gs - L weighs 200 L, share gs - L + k - 1 (k = 1..L) weighs 200 L - 2 kTaperPct k,
+// and share c begins at tile T * W(c) / W(gs), W(c) the weight of the shares before it.
+__device__ __forceinline__ long long share_weight(int c, int gs, int L) {
+  const long long m = max(0, c - (gs - L));
+  return 200LL * L * c - kTaperPct * m * (m + 1);
+}
+// L for a call: none without early start or on a grid above kMaxTaperGrid, and none when the
+// smallest share would hold less than one tile (consecutive cuts must stay distinct: every
+// CTA between the first and the last of a split segment holds a piece of it).
+__device__ __forceinline__ int taper_count(bool early, long long T, int gs) {
+  const int L = early && gs <= kMaxTaperGrid ? gs / kTaperDiv : 0;
+  if (L == 0) return 0;
+  return T * (2LL * L * (100 - kTaperPct)) >= share_weight(gs, gs, L) ? L : 0;
+}
+__device__ __forceinline__ int share_raw(int c, long long T, int gs, int L) {
   if (c <= 0) return 0;
   if (c >= gs) return int(T);
-  const int raw = int((long long)c * T / gs);
+  return L ? int(T * share_weight(c, gs, L) / share_weight(gs, gs, L)) : int((long long)c * T / gs);
+}
+// The CTA whose share holds tile t of a segment longer than kShortTiles: the last c whose
+// raw first tile is at or before t.  cuts[c] = share_raw(c) when the shares are tapered, else
+// NULL (closed form).
+__device__ __forceinline__ int share_owner(long long t, long long T, int gs, const int* cuts) {
+  if (!cuts) return int(((t + 1) * gs + T - 1) / T) - 1;
+  int lo = 0, hi = gs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cuts[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// First tile of CTA c's share on the single-launch path: its raw first tile (c*T/gs, or the
+// tapered cut), moved to the nearer end of the segment it falls in when that segment has at
+// most kShortTiles tiles (ties go to its start).  Monotone in c, so the shares stay disjoint
+// and cover [0, T).  A tile of a longer segment belongs to the same CTA as without the move:
+// cuts inside it are not moved, and cuts moved within other segments stay on their side of
+// it.  plan[s].w is the first tile of segment s in the sequence, plan[s].z its visible
+// entries, order[i] the segment at sequence position i (or, with order NULL, segment i).
+__device__ __forceinline__ int share_cut(int c, long long T, long long gs, const int* cuts, const int4* plan,
+                                         const int16_t* order, int nseg, int ept) {
+  if (c <= 0) return 0;
+  if (c >= gs) return int(T);
+  const int raw = cuts ? cuts[c] : int((long long)c * T / gs);
   int lo = 0, hi = nseg - 1;   // last sequence position whose segment starts at or before raw
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -443,6 +483,9 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const bool aligned = sh.max_nt <= kAlignTiles && nseg <= int(gridDim.x);
     const int gs = min(int(gridDim.x), T);
     const int c = blockIdx.x;
+    const int taper = aligned ? 0 : taper_count(early, T, gs);
+    if (taper)
+      for (int i = tid; i <= gs; i += kThreads) sh.cuts[i] = share_raw(i, T, gs, taper);
     {
       // running first tile and sequence position of this thread's next long / short segment
       // (in segment order: of its next segment)
@@ -472,13 +515,15 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       sh.gs = gs;
       sh.aligned = aligned;
       sh.long_first = long_first;
+      sh.taper = taper;
       if (aligned && c >= nseg) sh.tb = sh.te = T;
     }
     __syncthreads();
     if (!aligned) {
       if (tid == 0) {
-        sh.tb = share_cut(c, T, gs, plan, long_first ? order : nullptr, nseg, EPT);
-        sh.te = share_cut(c + 1, T, gs, plan, long_first ? order : nullptr, nseg, EPT);
+        const int* cuts = taper ? sh.cuts : nullptr;
+        sh.tb = share_cut(c, T, gs, cuts, plan, long_first ? order : nullptr, nseg, EPT);
+        sh.te = share_cut(c + 1, T, gs, cuts, plan, long_first ? order : nullptr, nseg, EPT);
       }
       __syncthreads();
       const int tb = sh.tb;
@@ -550,14 +595,16 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           d.W = local ? __ldg(p.window + s) : 0;
           d.S = local && p.sink ? __ldg(p.sink + s) : 0;
           // only segments longer than kShortTiles are shared; the CTAs holding their tiles are
-          // the ones c*T/gs gives (cuts inside them are not moved)
-          const long long T = sh.T, gs = sh.gs;
+          // the ones the raw cuts give (cuts inside them are not moved)
+          const long long T = sh.T;
+          const int gs = sh.gs;
+          const int* cuts = sh.taper ? sh.cuts : nullptr;
           const bool cut = d.n_tiles > kShortTiles && !sh.aligned;
-          const int c0 = cut ? int((((long long)d.tile0 + 1) * gs + T - 1) / T) - 1 : s;
-          const int c1 = cut ? int((((long long)d.tile0 + d.n_tiles) * gs + T - 1) / T) - 1 : s;
+          const int c0 = cut ? share_owner(d.tile0, T, gs, cuts) : s;
+          const int c1 = cut ? share_owner((long long)d.tile0 + d.n_tiles - 1, T, gs, cuts) : s;
           d.cta0 = c0;
           d.n_splits = c1 - c0 + 1;
-          d.slot0 = (cut && c1 > c0) ? int(share_cut(c0, T, gs, s_plan, order, nseg, EPT) < d.tile0) : 0;   // c0_later
+          d.slot0 = (cut && c1 > c0) ? int(share_cut(c0, T, gs, cuts, s_plan, order, nseg, EPT) < d.tile0) : 0;   // c0_later
         } else {
           d = ws.segs[s];
         }

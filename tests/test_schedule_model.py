@@ -14,8 +14,36 @@ MAX_GRID = 1024     # kDecMaxGrid
 SHORT = 8           # kShortTiles
 
 
-def owner(t, T, gs):
-    return ((t + 1) * gs + T - 1) // T - 1
+TAPER_DIV, TAPER_PCT, MAX_TAPER_GRID = 6, 40, 256    # kTaperDiv, kTaperPct, kMaxTaperGrid
+
+
+def share_weight(c, gs, L):
+    m = max(0, c - (gs - L))
+    return 200 * L * c - TAPER_PCT * m * (m + 1)
+
+
+def taper_count(early, T, gs):
+    """Tapered shares of a call (0: equal shares)."""
+    L = gs // TAPER_DIV if early and gs <= MAX_TAPER_GRID else 0
+    if L == 0:
+        return 0
+    return L if T * (2 * L * (100 - TAPER_PCT)) >= share_weight(gs, gs, L) else 0
+
+
+def share_raw(c, T, gs, L):
+    if c <= 0:
+        return 0
+    if c >= gs:
+        return T
+    return T * share_weight(c, gs, L) // share_weight(gs, gs, L) if L else c * T // gs
+
+
+def owner(t, T, gs, L=0):
+    """The CTA whose share holds tile t of a long segment: closed form for equal shares,
+    else the last c whose raw cut is at or before t."""
+    if not L:
+        return ((t + 1) * gs + T - 1) // T - 1
+    return max(c for c in range(gs) if share_raw(c, T, gs, L) <= t)
 
 
 LATE_SHARES = 8     # kLateShares
@@ -40,14 +68,14 @@ def sequence(nt, grid):
     return np.array(order), tile0
 
 
-def share_cut(c, T, gs, tile0, nt, order):
-    """First tile of CTA c's share: c*T/gs, moved to the nearer end (ties: its start) of the
-    segment it falls in when that segment has at most SHORT tiles."""
+def share_cut(c, T, gs, tile0, nt, order, L=0):
+    """First tile of CTA c's share: its raw cut (c*T/gs, or tapered), moved to the nearer end
+    (ties: its start) of the segment it falls in when that segment has at most SHORT tiles."""
     if c <= 0:
         return 0
     if c >= gs:
         return T
-    raw = c * T // gs
+    raw = share_raw(c, T, gs, L)
     pos = int(np.searchsorted(tile0[order], raw, side="right")) - 1   # last position starting <= raw
     s = int(order[pos])
     t0, n = int(tile0[s]), int(nt[s])
@@ -60,22 +88,23 @@ def split_slot(c, cta0, c0_later):
     return 2 * c + 1 if (c == cta0 and c0_later) else 2 * c
 
 
-def decode_schedule(nt, grid):
+def decode_schedule(nt, grid, early=False):
     """Per head segment: (tile0, cta0, n_splits, c0_later) as the producer derives them; per
     (segment, CTA) piece of the shares: the slot the producer gives it (2c for the CTA's
-    first portion, 2c+1 for a later one)."""
+    first portion, 2c+1 for a later one).  early: shares tapered as with early start."""
     nt = np.asarray(nt, dtype=np.int64)
     order, tile0 = sequence(nt, grid)
     T = int(nt.sum())
     gs = min(grid, T)
-    cuts = [share_cut(c, T, gs, tile0, nt, order) for c in range(gs + 1)]
+    L = taper_count(early, T, gs)
+    cuts = [share_cut(c, T, gs, tile0, nt, order, L) for c in range(gs + 1)]
     segs, pieces = [], {}
     for s, (t0, n) in enumerate(zip(tile0, nt)):
         if n == 0:
             segs.append(None)
             continue
         if n > SHORT:
-            c0, c1 = owner(int(t0), T, gs), owner(int(t0 + n - 1), T, gs)
+            c0, c1 = owner(int(t0), T, gs, L), owner(int(t0 + n - 1), T, gs, L)
         else:
             c0 = c1 = -1
         later = int(c1 > c0 and cuts[c0] < t0)
@@ -89,11 +118,12 @@ def decode_schedule(nt, grid):
                 continue
             pieces[(s, c)] = 2 * c + (0 if first else 1)
             first = False
-    return T, gs, cuts, segs, pieces
+    return T, gs, cuts, segs, pieces, L
 
 
+@pytest.mark.parametrize("early", [False, True])
 @pytest.mark.parametrize("seed", range(60))
-def test_decode_shares_slots_and_counters(seed):
+def test_decode_shares_slots_and_counters(seed, early):
     rng = np.random.default_rng(seed)
     grid = int(rng.choice([1, 3, 8, 40, 148]))
     nseg = int(rng.integers(1, 400))
@@ -108,7 +138,7 @@ def test_decode_shares_slots_and_counters(seed):
         nt = np.zeros(nseg, np.int64); nt[rng.integers(nseg)] = int(rng.integers(1, 3000))
     else:                                                   # windows of 5 tiles and a few long heads
         nt = np.full(nseg, 5, np.int64); nt[rng.integers(nseg, size=3)] = rng.integers(9, 1100, 3)
-    T, gs, cuts, segs, pieces = decode_schedule(nt, grid)
+    T, gs, cuts, segs, pieces, L = decode_schedule(nt, grid, early)
     # the cuts are monotone and the shares tile [0, T)
     assert cuts[0] == 0 and cuts[-1] == T and all(a <= b for a, b in zip(cuts, cuts[1:]))
     _, tile0 = sequence(nt, grid)
@@ -122,7 +152,7 @@ def test_decode_shares_slots_and_counters(seed):
             t0_, c0, k, _ = segs[s]
             assert held == list(range(c0, c0 + k))
             for t in range(int(t0), int(t0 + n)):
-                c = owner(t, T, gs)
+                c = owner(t, T, gs, L)
                 assert cuts[c] <= t < cuts[c + 1]
     # slots: the kernel's split_slot formula gives the producer's slot; all distinct, < 2*grid
     split_slots = {}
@@ -160,7 +190,7 @@ def test_long_segments_come_first_so_the_last_ctas_hold_only_windows():
     # 148 CTAs; the CTAs dispatched last take windows, never a piece of the global head
     nt = [5] * 8
     nt[3] = 1024
-    T, gs, cuts, segs, pieces = decode_schedule(nt, 148)
+    T, gs, cuts, segs, pieces, _ = decode_schedule(nt, 148)
     order, tile0 = sequence(nt, 148)
     assert list(order[:1]) == [3] and tile0[3] == 0
     last = [c for (s, c) in pieces if s != 3]
@@ -177,7 +207,7 @@ def test_many_windows_keep_segment_order():
 
 def test_short_windows_stay_whole_on_a_local_only_layer():
     # eight local heads of five key tiles each over 148 CTAs: eight CTAs take one window each
-    T, gs, cuts, segs, pieces = decode_schedule([5] * 8, 148)
+    T, gs, cuts, segs, pieces, _ = decode_schedule([5] * 8, 148)
     assert all(rec[2] == 1 for rec in segs)
     assert sorted(cuts[c + 1] - cuts[c] for c in range(gs) if cuts[c + 1] > cuts[c]) == [5] * 8
 
@@ -209,3 +239,19 @@ def test_prefill_items_cover_each_unit_once(seed):
         assert all(e - b <= chunk + chunk // 2 for b, e in mine)         # merged remainder at most 1.5 chunks
         if len(mine) > 1:
             assert all(e - b >= chunk // 2 for b, e in mine)             # no slivers
+
+
+def test_tapered_shares_shrink_towards_the_last_cta():
+    # the decode microbenchmark's 2720 tiles over 148 CTAs with early start: the first
+    # 124 shares are equal, the last 24 shrink step by step to 60 % of a full share
+    nt = np.tile([64] + [3] * 7, 32)
+    T, gs, cuts, segs, pieces, L = decode_schedule(nt, 148, early=True)
+    assert L == 24
+    raw = [share_raw(c, T, gs, L) for c in range(gs + 1)]
+    w = np.diff(raw)
+    full = T * 200 * L / share_weight(gs, gs, L)
+    assert abs(w[:gs - L].mean() - full) < 1 and abs(w[-1] - 0.6 * full) <= 1
+    assert all(w[i] >= w[i + 1] - 1 for i in range(gs - L - 1, gs - 1))
+    assert sum(w) == T and min(w) >= 1
+    # no taper without early start, or when a share would hold less than a tile
+    assert taper_count(False, T, gs) == 0 and taper_count(True, 150, 148) == 0
