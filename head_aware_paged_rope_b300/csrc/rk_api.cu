@@ -34,7 +34,7 @@ struct AttnLayout {
   int tok_per_unit;
   int max_units;
   int max_items;
-  size_t off_units, off_items, off_lse, off_o, off_prefix, total;
+  size_t off_units, off_items, off_lse, off_o, off_prefix, off_done, off_split, total;
 };
 
 rk_status check_attn(const rk_attn_args* a, bool decode) {
@@ -95,6 +95,10 @@ AttnLayout attn_layout(const rk_attn_args* a) {
   off += sizeof(float) * size_t(l.max_items) * l.rows * a->d;   // tile prefix follows directly
   l.off_prefix = off;
   off += align256(sizeof(int32_t) * size_t(a->B + 1));
+  l.off_done = off;
+  off += align256(sizeof(int32_t) * size_t(l.max_units));
+  l.off_split = off;
+  off += align256(sizeof(int32_t) * size_t(l.max_units));
   l.total = off;
   return l;
 }
@@ -140,6 +144,8 @@ AttnWorkspace make_ws(void* base, const AttnLayout& l) {
   ws.items = reinterpret_cast<Item*>(b + l.off_items);
   ws.part_lse = reinterpret_cast<float*>(b + l.off_lse);
   ws.part_o = reinterpret_cast<float*>(b + l.off_o);
+  ws.unit_done = reinterpret_cast<int32_t*>(b + l.off_done);
+  ws.split_list = reinterpret_cast<int32_t*>(b + l.off_split);
   ws.max_units = l.max_units;
   ws.max_items = l.max_items;
   ws.rows = l.rows;
@@ -238,7 +244,6 @@ rk_status run_attention(const rk_attn_args* a, void* workspace, size_t bytes, cu
   const int ept = prefill_tc_keys() / a->P;
   cudaError_t e = launch_plan(p, ws, l.tok_per_unit, ept, std::min(kTargetItems, grid * kItemsPerCta), kMinChunkTiles, stream);
   if (e == cudaSuccess) e = launch_prefill_tc(p, ws, grid, stream);
-  if (e == cudaSuccess) e = launch_combine(p, ws, stream);
   return e == cudaSuccess ? RK_OK : RK_ERR_CUDA;
 }
 

@@ -73,8 +73,8 @@ struct Unit {
   int32_t n_splits;   // items of this unit
   int32_t first_item; // index of its first full-size item (they are consecutive)
   int32_t b;          // sequence
-  int32_t n_full;     // full-size items
-  int32_t rem_item;   // index of its shorter last item, or -1
+  int32_t n_full;     // full-size chunks
+  int32_t rem_item;   // planner scratch (-1 once planned)
 };
 
 struct Item {
@@ -89,14 +89,13 @@ struct PlanHeader {
   int32_t n_items;
   int32_t chunk;      // entries per split
   int32_t counter;    // dynamic work counter (reset by the planner)
-  int32_t pad[60];
+  int32_t n_split;    // units with more than one item (listed in split_list)
+  int32_t merge_counter;   // merge jobs taken (reset by the planner)
+  int32_t pad[58];
 };
 
-// Item index of split s of a unit (items are emitted longest first: every unit's full-size
-// chunks, then the shorter remainders).
-__device__ __forceinline__ int32_t unit_item(const Unit& u, int32_t s) {
-  return s < u.n_full ? u.first_item + s : u.rem_item;
-}
+// Item index of split s of a unit (the items of a unit are consecutive).
+__device__ __forceinline__ int32_t unit_item(const Unit& u, int32_t s) { return u.first_item + s; }
 
 __device__ __forceinline__ int32_t unit_entry(const Unit& u, int32_t v) {
   return v < u.e_sink ? v : u.e_w + (v - u.e_sink);
@@ -139,6 +138,8 @@ struct AttnWorkspace {
   Item* items;
   float* part_lse;     // [max_items][rows]
   float* part_o;       // [max_items][rows][d]
+  int32_t* unit_done;  // [max_units] softmax warps that stored their rows of a partial (8 per item)
+  int32_t* split_list; // [max_units] the units with more than one item, in unit order
   int32_t max_units;
   int32_t max_items;
   int32_t rows;        // rows per unit (query tile rows)
@@ -372,7 +373,6 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
 // Launchers implemented in the .cu files.
 cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int rows_per_unit,
                         int entries_per_tile, int target_items, int min_chunk_tiles, cudaStream_t stream);
-cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, cudaStream_t stream);
 cudaError_t launch_plan_decode(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream);
 cudaError_t launch_decode_tc(const AttnParams& p, const DecWorkspace& ws, cudaStream_t stream);
 // bf16 2-D / 3-D tensor map with 128-byte swizzle (rk_prefill_tc.cu)

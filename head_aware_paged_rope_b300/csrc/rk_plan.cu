@@ -1,4 +1,4 @@
-// Work planning and split-KV combine for SegPagedAttention.
+// Work planning for SegPagedAttention.
 //
 // The visible key set of a query tile against one KV head is read straight off that
 // head's page list ("RedKnot" article, SegPagedAttention paragraph: the table records
@@ -6,7 +6,7 @@
 // at most two ranges of list entries -- sink pages and the causal / window pages -- by
 // binary search on the ascending logical page numbers, then cuts the units into items
 // of about equal size so that a persistent grid stays busy whatever the mix of head
-// classes.  Items of one unit are merged afterwards with the usual log-sum-exp rule.
+// classes.  The attention kernel merges the items of a unit with the usual log-sum-exp rule.
 #include "rk_internal.cuh"
 #include "rk_sm100.cuh"
 
@@ -150,36 +150,49 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
   __syncthreads();
   const int chunk = s_chunk;
 
-  // 4. items, longest first: the full-size chunks of every unit, then each unit's shorter
-  //    last chunk (or its only, empty, item).  A remainder of at most half a chunk joins
-  //    the unit's last full chunk instead of becoming an item of its own.
-  int carry_full = 0, carry_rem = 0;
+  // 4. items: a unit's entries are cut into full-size chunks, a remainder of more than half
+  //    a chunk becoming an item of its own and a smaller one joining the last chunk.  The
+  //    items of a unit are consecutive, and the units come in three classes: single items
+  //    of at least a chunk (the longest, first), then the units cut into several items in
+  //    unit order -- so that they complete one after another and the attention kernel can
+  //    merge each while later ones run -- then the single items shorter than a chunk.  The
+  //    split units are listed for that merge; their completion counters start at zero.
+  int cls_items[3] = {0, 0, 0}, carry_split = 0;
   for (int base = 0; base < n_units; base += kPlanThreads) {
     const int u = base + tid;
-    int nf = 0, rm = 0;
+    int ns = 0, cls = 0;
     if (u < n_units) {
       const int nv = ws.units[u].n_vis;
-      const int r = nv % chunk;
-      nf = nv / chunk;
-      rm = (nv == 0 || (r != 0 && (nf == 0 || 2 * r > chunk))) ? 1 : 0;
-    }
-    int tot_f, tot_r;
-    const int pre_f = block_exclusive_scan(nf, &tot_f, s_warp);
-    const int pre_r = block_exclusive_scan(rm, &tot_r, s_warp);
-    if (u < n_units) {
+      const int r = nv % chunk, nf = nv / chunk;
+      const int rm = (nv == 0 || (r != 0 && (nf == 0 || 2 * r > chunk))) ? 1 : 0;
+      ns = nf + rm;
+      cls = ns > 1 ? 1 : nf >= 1 ? 0 : 2;
       ws.units[u].n_full = nf;
-      ws.units[u].n_splits = nf + rm;
-      ws.units[u].first_item = carry_full + pre_f;
-      ws.units[u].rem_item = rm ? carry_rem + pre_r : -1;   // made absolute below
+      ws.units[u].n_splits = ns;
+      ws.unit_done[u] = 0;
     }
-    carry_full += tot_f;
-    carry_rem += tot_r;
+    int tot[3], pre[3];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) pre[c] = block_exclusive_scan(cls == c ? ns : 0, &tot[c], s_warp);
+    int tot_s;
+    const int pre_s = block_exclusive_scan(cls == 1 ? 1 : 0, &tot_s, s_warp);
+    if (u < n_units) {
+      const int base_c = cls == 0 ? cls_items[0] + pre[0] : cls == 1 ? cls_items[1] + pre[1] : cls_items[2] + pre[2];
+      ws.units[u].first_item = base_c;   // within its class, made absolute below
+      ws.units[u].rem_item = cls;
+      if (cls == 1) ws.split_list[carry_split + pre_s] = u;
+    }
+#pragma unroll
+    for (int c = 0; c < 3; ++c) cls_items[c] += tot[c];
+    carry_split += tot_s;
   }
   __syncthreads();
-  const int n_items_all = carry_full + carry_rem;
+  const int n_items_all = cls_items[0] + cls_items[1] + cls_items[2];
   for (int u = tid; u < n_units; u += kPlanThreads) {
     Unit& un = ws.units[u];
-    if (un.rem_item >= 0) un.rem_item += carry_full;
+    const int cls = un.rem_item;
+    un.first_item += cls == 0 ? 0 : cls == 1 ? cls_items[0] : cls_items[0] + cls_items[1];
+    un.rem_item = -1;
     const int nv = un.n_vis;
     for (int s = 0; s < un.n_splits; ++s) {
       const int it = unit_item(un, s);
@@ -197,80 +210,8 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
     ws.header->n_items = min(n_items_all, ws.max_items);
     ws.header->chunk = chunk;
     ws.header->counter = 0;
-  }
-}
-
-// Merge the split partials of each unit: lse = log sum_s e^{lse_s}, o = sum_s e^{lse_s - lse} o_s.
-// Work is (unit, block of 8 rows): warp w of a block merges row 8*blk + w in one pass over
-// the unit's splits with a running maximum, four splits' loads in flight at a time; lane l
-// holds channels [l*C, l*C + C).
-template <int D>
-__global__ __launch_bounds__(256) void combine_kernel(AttnParams p, AttnWorkspace ws) {
-  sm100::grid_dependency_wait();   // the attention kernel is complete
-  constexpr int C = D / 32;        // 4 or 2 channels per lane
-  const int n_units = ws.header->n_units;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = p.G;
-  const int rb = (ws.rows + 7) / 8;
-  const long long n_blk = (long long)n_units * rb;
-  for (long long blk = blockIdx.x; blk < n_blk; blk += gridDim.x) {
-    const int u = int(blk / rb);
-    const int ns = ws.units[u].n_splits;
-    if (ns <= 1) continue;
-    const Unit un = ws.units[u];
-    const int r = int(blk - (long long)u * rb) * 8 + warp;
-    if (r >= un.ntok * G) continue;
-    float M = -INFINITY, den = 0.f, acc[C];
-#pragma unroll
-    for (int c = 0; c < C; ++c) acc[c] = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += 4) {
-      float lv[4], ov[4][C];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        lv[k] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < C; ++c) ov[k][c] = 0.f;
-        if (s0 + k < ns) {
-          const int64_t it = unit_item(un, s0 + k);
-          lv[k] = ws.part_lse[it * ws.rows + r];
-          const float* po = ws.part_o + (it * ws.rows + r) * D + lane * C;
-          if constexpr (C == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(po);
-            ov[k][0] = v.x; ov[k][1] = v.y; ov[k][2] = v.z; ov[k][3] = v.w;
-          } else {
-            const float2 v = *reinterpret_cast<const float2*>(po);
-            ov[k][0] = v.x; ov[k][1] = v.y;
-          }
-        }
-      }
-      const float mc = fmaxf(fmaxf(M, fmaxf(lv[0], lv[1])), fmaxf(lv[2], lv[3]));
-      if (mc == -INFINITY) continue;
-      const float f = M == -INFINITY ? 0.f : expf(M - mc);
-      den *= f;
-#pragma unroll
-      for (int c = 0; c < C; ++c) acc[c] *= f;
-      M = mc;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float w = lv[k] == -INFINITY ? 0.f : expf(lv[k] - M);
-        den += w;
-#pragma unroll
-        for (int c = 0; c < C; ++c) acc[c] = fmaf(w, ov[k][c], acc[c]);
-      }
-    }
-    const int t = un.tok0 + r / G;
-    const int hq = (un.seg % p.Hkv) * G + (r % G);
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    __nv_bfloat16* o = p.out + (int64_t(t) * p.Hq + hq) * D + lane * C;
-    if constexpr (C == 4) {
-      uint2 w;
-      w.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-      w.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<uint2*>(o) = w;
-    } else {
-      *reinterpret_cast<uint32_t*>(o) = pack_bf16(acc[0] * inv, acc[1] * inv);
-    }
-    if (p.lse && lane == 0) p.lse[int64_t(t) * p.Hq + hq] = den > 0.f ? M + logf(den) : -INFINITY;
+    ws.header->n_split = carry_split;
+    ws.header->merge_counter = 0;
   }
 }
 
@@ -430,13 +371,5 @@ cudaError_t launch_plan(const AttnParams& p, const AttnWorkspace& ws, int tok_pe
                             min_chunk_tiles, tile_prefix);
 }
 
-cudaError_t launch_combine(const AttnParams& p, const AttnWorkspace& ws, cudaStream_t stream) {
-  const long long blocks = (long long)ws.max_units * ((ws.rows + 7) / 8);
-  const int grid = int(std::max(1LL, std::min(blocks, (long long)device_sm_count() * 8)));
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(256), 0, stream, attr);
-  return p.d == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p, ws)
-                    : cudaLaunchKernelEx(&cfg, combine_kernel<64>, p, ws);
-}
 
 }  // namespace rk

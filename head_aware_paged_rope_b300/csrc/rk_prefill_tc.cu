@@ -16,7 +16,8 @@
 //            and V rings (a K stage is freed as soon as both S tiles are computed);
 //   warp 9   MMA issuer (one thread): S_A = Q_A K^T and S_B = Q_B K^T into TMEM, then
 //            O_A += P_A V and O_B += P_B V with P read straight from TMEM;
-//   warps 10-11 idle (they complete the third warpgroup, whose registers go to the softmax);
+//   warps 10-11 merge the units cut into several items as they complete (the softmax warps
+//            join them once the item queue is empty), so no separate combine kernel runs;
 //   warps 0-3 / 4-7  softmax of tile A / B: thread r owns row r (TMEM lane r), loads its S
 //            row once into registers, masks the edge, keeps a running maximum that moves
 //            only when it grows by more than 2^8 (then the row of O is rescaled in TMEM),
@@ -72,6 +73,7 @@ struct TcBarriers {
   uint64_t o_done[2];
   uint64_t iq_full[2], iq_empty[2];   // item ring: producer -> MMA issuer and softmax warps
   int ring[2];
+  int job[2][2];                      // merge jobs of the two workers (softmax warps, warps 10-11)
   uint32_t tmem_slot;
   int abort;
 };
@@ -89,6 +91,150 @@ __device__ __forceinline__ bool wait_or_abort(TcBarriers& b, uint32_t bar, uint3
     if (mbar_try_wait(bar, parity)) return true;
     if (aborted(b)) return false;
     if (globaltimer() - t0 > kWaitNs) return false;
+  }
+}
+
+// Wait (acquire) until a unit's completion counter reaches `target`.  Gives up after 1 s in
+// which neither that counter nor the item counter moved, or when another role aborted.
+__device__ __forceinline__ bool wait_count(TcBarriers& b, const int32_t* c, int target, const int32_t* items) {
+  int v;
+  asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+  if (v >= target) return true;
+  int last = v, last_items = -1;
+  uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(128);
+    asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= target) return true;
+    const int it = *reinterpret_cast<const volatile int32_t*>(items);
+    const uint64_t now = globaltimer();
+    if (v != last || it != last_items) {
+      last = v;
+      last_items = it;
+      t0 = now;
+    } else if (now - t0 > kWaitNs || aborted(b)) {
+      return false;
+    }
+  }
+}
+
+// Merge of the units cut into several items.  Two workers in each CTA take jobs -- one split
+// unit and kJobRows of its rows -- from a common counter, in the order the planner lists the
+// split units, which is the order their items are handed out, so units complete one after
+// another and most merges run while later items are computed:
+//  - warps 10-11 (BACKGROUND), from the start, but only while items remain and only a job
+//    whose unit is already complete (they look at the next job and claim it with a
+//    compare-and-swap), so that they never hold a merge the tail waits for;
+//  - the eight softmax warps once their items are done: they claim the next job outright and
+//    wait until its unit is complete (each item of it is held by a running CTA whose softmax
+//    warps take no job before their items are done).
+// A unit is complete when the 8 softmax warps of every item of it have stored their rows of
+// the partial.  The merge is the log-sum-exp rule: lse = log sum_s e^(lse_s),
+// o = sum_s e^(lse_s - lse) o_s.  Warp w of the worker takes rows w, w + nwarps, ... of the
+// job; lane l channels [l C, l C + C), with 8 items' partials of the row in flight.
+template <int D, bool BACKGROUND>
+__device__ __forceinline__ bool merge_split_units(const AttnParams& p, const AttnWorkspace& ws, TcBarriers& b,
+                                                  int* job_slot, uint32_t bar, int nthreads, int wtid, int n_items) {
+  constexpr int kJobRows = 8, C = D / 32, SPL = 8;
+  const int wl = wtid >> 5, lane = wtid & 31, nwarps = nthreads >> 5;
+  const int rb = ws.rows / kJobRows;
+  const int n_jobs = ws.header->n_split * rb;
+  const int G = p.G;
+  volatile int32_t* vcounter = &ws.header->merge_counter;
+  for (int k = 0;; ++k) {
+    if (wtid == 0) {
+      int job;
+      if constexpr (BACKGROUND) {
+        // the next job, if its unit is complete and items remain; else -1 (stop)
+        job = -1;
+        uint64_t t0 = globaltimer();
+        int last_items = -1;
+        while (true) {
+          const int items = *reinterpret_cast<volatile int32_t*>(&ws.header->counter);
+          if (items + int(gridDim.x) >= n_items || aborted(b)) break;
+          const int j = *vcounter;
+          if (j >= n_jobs) break;
+          const int u = ws.split_list[j / rb];
+          int done;
+          asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(done) : "l"(ws.unit_done + u) : "memory");
+          if (done >= 8 * ws.units[u].n_splits) {
+            if (atomicCAS(&ws.header->merge_counter, j, j + 1) == j) { job = j; break; }
+            continue;
+          }
+          const uint64_t now = globaltimer();
+          if (items != last_items) { last_items = items; t0 = now; }
+          else if (now - t0 > kWaitNs) break;   // no item taken for 1 s: leave it to the tail
+          __nanosleep(256);
+        }
+      } else {
+        job = atomicAdd(&ws.header->merge_counter, 1);
+      }
+      job_slot[k & 1] = job;
+    }
+    named_bar_sync(bar, nthreads);
+    const int job = job_slot[k & 1];
+    if (job < 0 || job >= n_jobs) return true;
+    const int u = ws.split_list[job / rb];
+    const Unit un = ws.units[u];
+    const bool got = (BACKGROUND || wtid != 0) ? true : wait_count(b, ws.unit_done + u, 8 * un.n_splits, &ws.header->counter);
+    if (!named_bar_and(bar, nthreads, got)) return false;
+    const int ns = un.n_splits;
+    for (int r = (job % rb) * kJobRows + wl; r < (job % rb + 1) * kJobRows; r += nwarps) {
+      float M = -INFINITY, den = 0.f, acc[C];
+#pragma unroll
+      for (int c = 0; c < C; ++c) acc[c] = 0.f;
+      for (int s0 = 0; s0 < ns; s0 += SPL) {
+        float lv[SPL], ov[SPL][C];
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) {
+          lv[q] = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < C; ++c) ov[q][c] = 0.f;
+          if (s0 + q < ns) {
+            const int64_t row = int64_t(unit_item(un, s0 + q)) * ws.rows + r;
+            lv[q] = __ldcg(ws.part_lse + row);
+            const float* po = ws.part_o + row * D + lane * C;
+            if constexpr (C == 4) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+              ov[q][0] = v.x; ov[q][1] = v.y; ov[q][2] = v.z; ov[q][3] = v.w;
+            } else {
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+              ov[q][0] = v.x; ov[q][1] = v.y;
+            }
+          }
+        }
+        float mc = M;
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) mc = fmaxf(mc, lv[q]);
+        if (mc == -INFINITY) continue;
+        const float f = M == -INFINITY ? 0.f : expf(M - mc);
+        den *= f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[c] *= f;
+        M = mc;
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) {
+          const float w = lv[q] == -INFINITY ? 0.f : expf(lv[q] - mc);
+          den += w;
+#pragma unroll
+          for (int c = 0; c < C; ++c) acc[c] = fmaf(w, ov[q][c], acc[c]);
+        }
+      }
+      if (r >= un.ntok * G) continue;
+      const int t = un.tok0 + r / G;
+      const int hq = (un.seg % p.Hkv) * G + (r % G);
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      __nv_bfloat16* o = p.out + (int64_t(t) * p.Hq + hq) * D + lane * C;
+      if constexpr (C == 4) {
+        uint2 w;
+        w.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+        w.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(o) = w;
+      } else {
+        *reinterpret_cast<uint32_t*>(o) = pack_bf16(acc[0] * inv, acc[1] * inv);
+      }
+      if (p.lse && lane == 0) p.lse[int64_t(t) * p.Hq + hq] = den > 0.f ? M + logf(den) : -INFINITY;
+    }
   }
 }
 
@@ -148,7 +294,7 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = bars.tmem_slot;
   grid_dependency_wait();      // the plan (and everything before it in the stream) is complete
-  grid_launch_dependents();    // the combine kernel may be scheduled as CTAs of this one finish
+  grid_launch_dependents();    // the next kernel may be scheduled as CTAs of this one finish
 
   const int G = p.G;
   const int n_items = ws.header->n_items;
@@ -334,6 +480,10 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
         if (!ok) fail(bars, p.status);
         if (pending && aborted(bars)) mbar_wait(pend_bar, pend_par);
       }
+    } else if (ws.header->n_split > 0) {
+      // ---------------------------------------------------------------- warps 10-11: merges
+      if (!merge_split_units<D, true>(p, ws, bars, bars.job[1], 4, 64, tid - 320, n_items) && (tid & 31) == 0)
+        fail(bars, p.status);
     }
   } else {
     regs_increase<kRegsHigh>();
@@ -538,8 +688,17 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
           ws.part_lse[int64_t(it) * ws.rows + R] = lse;
         }
       }
+      if (split) {   // this warp's rows of the partial are stored: count them for the merge
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(ws.unit_done + item.unit, 1);
+      }
     }
     if (!ok && lane == 0) fail(bars, p.status);
+    // every softmax warp gets here (all waits above are bounded); merge only if all are well
+    if (named_bar_and(3, 256, ok) && ws.header->n_split > 0 &&
+        !merge_split_units<D, false>(p, ws, bars, bars.job[0], 3, 256, tid, n_items) && lane == 0)
+      fail(bars, p.status);
   }
 
   __syncthreads();

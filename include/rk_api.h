@@ -242,7 +242,10 @@ typedef struct rk_attn_args {
 RK_API size_t rk_segpaged_prefill_workspace_size(const rk_attn_args* args);
 RK_API size_t rk_segpaged_decode_workspace_size(const rk_attn_args* args);
 
-/* Prefill: any number of queries per sequence (a suffix at the end of the context).
+/* Prefill: any number of queries per sequence (a suffix at the end of the context).  A query
+ * tile whose key list is cut into several pieces is merged (log-sum-exp) inside the same
+ * kernel, by CTAs that have run out of pieces; a merge that waits longer than 1 s for its
+ * pieces sets RK_ERR_TIMEOUT in the status word.
  * Errors: RK_ERR_INVALID_ARG (NULL pointers, k_new or v_new set, q / k_pool / v_pool / out not 16-byte aligned,
  * B/Hq/Hkv/max_pages/total_q < 0, Hq % Hkv,
  * max_q > total_q), RK_ERR_UNSUPPORTED (d, P, Hq/Hkv > 16), RK_ERR_WORKSPACE, RK_ERR_CUDA. */

@@ -212,17 +212,30 @@ def test_short_windows_stay_whole_on_a_local_only_layer():
     assert sorted(cuts[c + 1] - cuts[c] for c in range(gs) if cuts[c + 1] > cuts[c]) == [5] * 8
 
 
-def prefill_items(n_vis, chunk):
-    """Items of each unit as the planner emits them: full chunks, and a remainder that
-    joins the last full chunk when it is at most half a chunk."""
-    items = []
+def prefill_plan(n_vis, chunk):
+    """Items as the planner emits them, in item order: full chunks, a remainder that joins the
+    last full chunk when it is at most half a chunk; the units in three classes -- single
+    items of at least a chunk, then the units of several items (unit order, each unit's items
+    consecutive), then single items shorter than a chunk.  Also returns each unit's first
+    item (the kernel's unit_item(u, s) = first_item + s) and the split-unit list."""
+    per_unit, cls = [], []
     for u, nv in enumerate(n_vis):
         r, nf = nv % chunk, nv // chunk
         rm = 1 if (nv == 0 or (r != 0 and (nf == 0 or 2 * r > chunk))) else 0
         ns = nf + rm
-        for s in range(ns):
-            items.append((u, s * chunk, nv if s == ns - 1 else (s + 1) * chunk))
-    return items
+        per_unit.append([(u, s * chunk, nv if s == ns - 1 else (s + 1) * chunk) for s in range(ns)])
+        cls.append(1 if ns > 1 else 0 if nf >= 1 else 2)
+    items, first = [], [0] * len(n_vis)
+    for c in (0, 1, 2):
+        for u in range(len(n_vis)):
+            if cls[u] == c:
+                first[u] = len(items)
+                items += per_unit[u]
+    return items, first, [u for u in range(len(n_vis)) if cls[u] == 1]
+
+
+def prefill_items(n_vis, chunk):
+    return prefill_plan(n_vis, chunk)[0]
 
 
 @pytest.mark.parametrize("seed", range(20))
@@ -239,6 +252,16 @@ def test_prefill_items_cover_each_unit_once(seed):
         assert all(e - b <= chunk + chunk // 2 for b, e in mine)         # merged remainder at most 1.5 chunks
         if len(mine) > 1:
             assert all(e - b >= chunk // 2 for b, e in mine)             # no slivers
+    # the kernel finds split s of unit u at first_item + s; split units are listed in the
+    # order their items are handed out, and come after the long single items
+    items, first, split = prefill_plan(n_vis, chunk)
+    for u, nv in enumerate(n_vis):
+        mine = [i for i, it in enumerate(items) if it[0] == u]
+        assert mine == list(range(first[u], first[u] + len(mine)))
+        assert (len(mine) > 1) == (u in split)
+    assert [first[u] for u in split] == sorted(first[u] for u in split)
+    singles_long = [u for u in range(len(n_vis)) if u not in split and n_vis[u] >= chunk]
+    assert all(first[a] < first[b] for a in singles_long for b in split)
 
 
 def test_tapered_shares_shrink_towards_the_last_cta():
