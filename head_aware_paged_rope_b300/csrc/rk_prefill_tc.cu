@@ -432,8 +432,11 @@ __global__ __launch_bounds__(kTcThreads, 1) void prefill_tc_kernel(const __grid_
           // order per tile j: S_A(j), O_B += P_B V (j-1), S_B(j), O_A += P_A V (j): the softmax of
           // one tile runs while the tensor core works for the other
           auto qk = [&](int x, uint32_t g1, uint32_t kb) -> bool {
-            // S_x holds P_x of the previous tile until its value product has completed
-            if (g1 >= 1 && !wait_or_abort(bars, smem_addr(&bars.o_done[x]), (g1 - 1) & 1)) return false;
+            // S_x holds P_x of the previous tile, which that tile's value product reads.  That
+            // product was issued before this one (after P_x was written), and the tensor pipe
+            // runs the MMAs one thread issues in that order, so P_x is read before this S_x
+            // overwrites it: no wait for the value product to complete.  (The softmax still
+            // finds O_x complete when S_x arrives: the commit of S_x tracks every earlier MMA.)
             tc_fence_after();
             const uint32_t qb = sQ + x * LY::kTile;
   #pragma unroll
