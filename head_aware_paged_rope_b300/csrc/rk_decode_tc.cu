@@ -115,6 +115,7 @@ struct DecShared {
   int abort;
   int T, gs, seg_first, last;   // single-launch path: the schedule, and "this CTA merges the splits"
   int tb, te, aligned, max_nt, long_first;
+  int short_lim;                // segments of at most this many tiles are never split
   int taper;                    // tapered shares (0: equal shares); their raw cuts:
   int cuts[kMaxTaperGrid + 1];
   int s_warp[32];
@@ -136,14 +137,6 @@ __device__ __forceinline__ bool wait_or_abort(DecShared& sh, uint32_t bar, uint3
     if (aborted(sh)) return false;
     if (globaltimer() - t0 > kWaitNs) return false;
   }
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
 }
 
 __device__ __forceinline__ int seg_entry(const DecSeg& s, int v) { return v < s.e_sink ? v : s.e_w + (v - s.e_sink); }
@@ -198,7 +191,8 @@ __device__ __forceinline__ float warp_reduce_cols(float (&v)[NG]) {
 
 constexpr int kMergeFan = 12;   // partials one CTA merges at a time (single-launch path)
 constexpr int kAlignTiles = 8;  // all segments this short and no more of them than CTAs: one segment per CTA
-constexpr int kShortTiles = 8;  // single-launch path: segments this short are never split
+constexpr int kShortTiles = 8;  // single-launch path: segments this short are never split, unless
+constexpr bool kSpread = true;  // there are no more tiles than CTAs: then every tile gets a CTA
 constexpr int kLateShares = 8;  // short segments go last when they fill at most this many shares
 constexpr int kTaperDiv = 6;    // with early start the last gs / kTaperDiv shares shrink linearly,
 constexpr int kTaperPct = 40;   // the last one by this many per cent of a full share
@@ -253,7 +247,7 @@ __device__ __forceinline__ int share_owner(long long t, long long T, int gs, con
 // it.  plan[s].w is the first tile of segment s in the sequence, plan[s].z its visible
 // entries, order[i] the segment at sequence position i (or, with order NULL, segment i).
 __device__ __forceinline__ int share_cut(int c, long long T, long long gs, const int* cuts, const int4* plan,
-                                         const int16_t* order, int nseg, int ept) {
+                                         const int16_t* order, int nseg, int ept, int short_lim) {
   if (c <= 0) return 0;
   if (c >= gs) return int(T);
   const int raw = cuts ? cuts[c] : int((long long)c * T / gs);
@@ -264,7 +258,7 @@ __device__ __forceinline__ int share_cut(int c, long long T, long long gs, const
   }
   const int s = order ? order[lo] : lo;
   const int t0 = plan[s].w, nt = (plan[s].z + ept - 1) / ept;
-  if (raw <= t0 || raw >= t0 + nt || nt > kShortTiles) return raw;
+  if (raw <= t0 || raw >= t0 + nt || nt > short_lim) return raw;
   return raw - t0 <= t0 + nt - raw ? t0 : t0 + nt;
 }
 
@@ -480,7 +474,11 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     int16_t* rank = reinterpret_cast<int16_t*>(smem + LY::kRank);
     // Few, short segments (at most kAlignTiles tiles each, no more segments than CTAs): CTA c
     // takes segment c whole, so nothing is split.  Otherwise the equal shares.
-    const bool aligned = sh.max_nt <= kAlignTiles && nseg <= int(gridDim.x);
+    // No more tiles than CTAs: every tile its own CTA, windows split too (their pieces all
+    // load at once, and a merge of a few partials costs less than a second round of copies).
+    const bool spread = kSpread && T <= int(gridDim.x);
+    const bool aligned = !spread && sh.max_nt <= kAlignTiles && nseg <= int(gridDim.x);
+    const int short_lim = spread ? 0 : kShortTiles;
     const int gs = min(int(gridDim.x), T);
     const int c = blockIdx.x;
     const int taper = aligned ? 0 : taper_count(early, T, gs);
@@ -514,6 +512,7 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
       sh.T = T;
       sh.gs = gs;
       sh.aligned = aligned;
+      sh.short_lim = short_lim;
       sh.long_first = long_first;
       sh.taper = taper;
       if (aligned && c >= nseg) sh.tb = sh.te = T;
@@ -522,8 +521,8 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     if (!aligned) {
       if (tid == 0) {
         const int* cuts = taper ? sh.cuts : nullptr;
-        sh.tb = share_cut(c, T, gs, cuts, plan, long_first ? order : nullptr, nseg, EPT);
-        sh.te = share_cut(c + 1, T, gs, cuts, plan, long_first ? order : nullptr, nseg, EPT);
+        sh.tb = share_cut(c, T, gs, cuts, plan, long_first ? order : nullptr, nseg, EPT, short_lim);
+        sh.te = share_cut(c + 1, T, gs, cuts, plan, long_first ? order : nullptr, nseg, EPT, short_lim);
       }
       __syncthreads();
       const int tb = sh.tb;
@@ -599,12 +598,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
           const long long T = sh.T;
           const int gs = sh.gs;
           const int* cuts = sh.taper ? sh.cuts : nullptr;
-          const bool cut = d.n_tiles > kShortTiles && !sh.aligned;
+          const bool cut = d.n_tiles > sh.short_lim && !sh.aligned;
           const int c0 = cut ? share_owner(d.tile0, T, gs, cuts) : s;
           const int c1 = cut ? share_owner((long long)d.tile0 + d.n_tiles - 1, T, gs, cuts) : s;
           d.cta0 = c0;
           d.n_splits = c1 - c0 + 1;
-          d.slot0 = (cut && c1 > c0) ? int(share_cut(c0, T, gs, cuts, s_plan, order, nseg, EPT) < d.tile0) : 0;   // c0_later
+          d.slot0 = (cut && c1 > c0) ? int(share_cut(c0, T, gs, cuts, s_plan, order, nseg, EPT, sh.short_lim) < d.tile0) : 0;   // c0_later
         } else {
           d = ws.segs[s];
         }

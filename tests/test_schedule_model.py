@@ -68,9 +68,15 @@ def sequence(nt, grid):
     return np.array(order), tile0
 
 
-def share_cut(c, T, gs, tile0, nt, order, L=0):
+def short_limit(T, grid):
+    """Segments of at most this many tiles are never split: SHORT, or 0 (every tile its own
+    CTA) when there are no more tiles than CTAs."""
+    return 0 if T <= grid else SHORT
+
+
+def share_cut(c, T, gs, tile0, nt, order, L=0, short=SHORT):
     """First tile of CTA c's share: its raw cut (c*T/gs, or tapered), moved to the nearer end
-    (ties: its start) of the segment it falls in when that segment has at most SHORT tiles."""
+    (ties: its start) of the segment it falls in when that segment has at most `short` tiles."""
     if c <= 0:
         return 0
     if c >= gs:
@@ -79,7 +85,7 @@ def share_cut(c, T, gs, tile0, nt, order, L=0):
     pos = int(np.searchsorted(tile0[order], raw, side="right")) - 1   # last position starting <= raw
     s = int(order[pos])
     t0, n = int(tile0[s]), int(nt[s])
-    if raw <= t0 or raw >= t0 + n or n > SHORT:
+    if raw <= t0 or raw >= t0 + n or n > short:
         return raw
     return t0 if raw - t0 <= t0 + n - raw else t0 + n
 
@@ -97,13 +103,14 @@ def decode_schedule(nt, grid, early=False):
     T = int(nt.sum())
     gs = min(grid, T)
     L = taper_count(early, T, gs)
-    cuts = [share_cut(c, T, gs, tile0, nt, order, L) for c in range(gs + 1)]
+    short = short_limit(T, grid)
+    cuts = [share_cut(c, T, gs, tile0, nt, order, L, short) for c in range(gs + 1)]
     segs, pieces = [], {}
     for s, (t0, n) in enumerate(zip(tile0, nt)):
         if n == 0:
             segs.append(None)
             continue
-        if n > SHORT:
+        if n > short:
             c0, c1 = owner(int(t0), T, gs, L), owner(int(t0 + n - 1), T, gs, L)
         else:
             c0 = c1 = -1
@@ -146,7 +153,7 @@ def test_decode_shares_slots_and_counters(seed, early):
         held = [c for c in range(gs) if n and cuts[c] < t0 + n and cuts[c + 1] > t0]
         if n == 0:
             continue
-        if n <= SHORT:                                      # short segments: one CTA, no split
+        if n <= short_limit(T, grid):                       # short segments: one CTA, no split
             assert len(held) == 1 and segs[s][2] == 1
         else:                                               # long ones: the CTAs c*T/gs gives
             t0_, c0, k, _ = segs[s]
@@ -205,11 +212,15 @@ def test_many_windows_keep_segment_order():
     assert list(order) == list(range(len(nt)))
 
 
-def test_short_windows_stay_whole_on_a_local_only_layer():
-    # eight local heads of five key tiles each over 148 CTAs: eight CTAs take one window each
+def test_windows_spread_one_tile_per_cta_on_a_local_only_layer():
+    # eight local heads of five key tiles each over 148 CTAs: 40 tiles, no more than CTAs, so
+    # every tile gets its own CTA and each window is merged from five pieces
     T, gs, cuts, segs, pieces, _ = decode_schedule([5] * 8, 148)
+    assert gs == 40 and all(cuts[c + 1] - cuts[c] == 1 for c in range(gs))
+    assert all(rec[2] == 5 for rec in segs)
+    # more tiles than CTAs: windows stay whole
+    T, gs, cuts, segs, pieces, _ = decode_schedule([5] * 40, 148)
     assert all(rec[2] == 1 for rec in segs)
-    assert sorted(cuts[c + 1] - cuts[c] for c in range(gs) if cuts[c + 1] > cuts[c]) == [5] * 8
 
 
 def prefill_plan(n_vis, chunk):
