@@ -194,8 +194,10 @@ constexpr int kAlignTiles = 8;  // all segments this short and no more of them t
 constexpr int kShortTiles = 8;  // single-launch path: segments this short are never split, unless
 constexpr bool kSpread = true;  // there are no more tiles than CTAs: then every tile gets a CTA
 constexpr int kLateShares = 8;  // short segments go last when they fill at most this many shares
-constexpr int kTaperDiv = 6;    // with early start the last gs / kTaperDiv shares shrink linearly,
-constexpr int kTaperPct = 40;   // the last one by this many per cent of a full share
+// With early start the last gs / div shares shrink linearly, the last one by pct per cent of a
+// full share: the strong setting when some segment spans more CTAs than one merge group.
+constexpr int kTaperStrongDiv = 3, kTaperStrongPct = 60;
+constexpr int kTaperMildDiv = 6, kTaperMildPct = 40;
 
 // Partial slot of CTA c for a split segment (two per CTA: its first and its last portion):
 // c's portion of the segment is its first one unless c = cta0 and c's share began in an
@@ -207,24 +209,26 @@ __device__ __forceinline__ int split_slot(int c, int cta0, int c0_later) {
 // Tapered shares.  With early start the CTAs are dispatched in index order as the SMs of
 // the preceding call free up, and the last of them start several microseconds late (their
 // SMs run that call's last CTAs, which also merge).  So the last L shares shrink linearly:
-// share i < gs - L weighs 200 L, share gs - L + k - 1 (k = 1..L) weighs 200 L - 2 kTaperPct k,
+// share i < gs - L weighs 200 L, share gs - L + k - 1 (k = 1..L) weighs 200 L - 2 pct k,
 // and share c begins at tile T * W(c) / W(gs), W(c) the weight of the shares before it.
-__device__ __forceinline__ long long share_weight(int c, int gs, int L) {
+// A segment spread over more CTAs than one merge group waits, for its final merge, for the
+// latest of them, so such a call tapers more (kTaperStrongDiv / kTaperStrongPct).
+__device__ __forceinline__ long long share_weight(int c, int gs, int L, int pct) {
   const long long m = max(0, c - (gs - L));
-  return 200LL * L * c - kTaperPct * m * (m + 1);
+  return 200LL * L * c - pct * m * (m + 1);
 }
 // L for a call: none without early start or on a grid above kMaxTaperGrid, and none when the
 // smallest share would hold less than one tile (consecutive cuts must stay distinct: every
 // CTA between the first and the last of a split segment holds a piece of it).
-__device__ __forceinline__ int taper_count(bool early, long long T, int gs) {
-  const int L = early && gs <= kMaxTaperGrid ? gs / kTaperDiv : 0;
+__device__ __forceinline__ int taper_count(bool early, long long T, int gs, int div, int pct) {
+  const int L = early && gs <= kMaxTaperGrid ? gs / div : 0;
   if (L == 0) return 0;
-  return T * (2LL * L * (100 - kTaperPct)) >= share_weight(gs, gs, L) ? L : 0;
+  return T * (2LL * L * (100 - pct)) >= share_weight(gs, gs, L, pct) ? L : 0;
 }
-__device__ __forceinline__ int share_raw(int c, long long T, int gs, int L) {
+__device__ __forceinline__ int share_raw(int c, long long T, int gs, int L, int pct) {
   if (c <= 0) return 0;
   if (c >= gs) return int(T);
-  return L ? int(T * share_weight(c, gs, L) / share_weight(gs, gs, L)) : int((long long)c * T / gs);
+  return L ? int(T * share_weight(c, gs, L, pct) / share_weight(gs, gs, L, pct)) : int((long long)c * T / gs);
 }
 // The CTA whose share holds tile t of a segment longer than kShortTiles: the last c whose
 // raw first tile is at or before t.  cuts[c] = share_raw(c) when the shares are tapered, else
@@ -481,9 +485,12 @@ __global__ __launch_bounds__(kThreads, 1) void decode_tc_kernel(const __grid_con
     const int short_lim = spread ? 0 : kShortTiles;
     const int gs = min(int(gridDim.x), T);
     const int c = blockIdx.x;
-    const int taper = aligned ? 0 : taper_count(early, T, gs);
+    // the longest segment spans about max_nt * gs / T CTAs
+    const bool strong = (long long)sh.max_nt * gs > (long long)kMergeFan * T;
+    const int tdiv = strong ? kTaperStrongDiv : kTaperMildDiv, tpct = strong ? kTaperStrongPct : kTaperMildPct;
+    const int taper = aligned ? 0 : taper_count(early, T, gs, tdiv, tpct);
     if (taper)
-      for (int i = tid; i <= gs; i += kThreads) sh.cuts[i] = share_raw(i, T, gs, taper);
+      for (int i = tid; i <= gs; i += kThreads) sh.cuts[i] = share_raw(i, T, gs, taper, tpct);
     {
       // running first tile and sequence position of this thread's next long / short segment
       // (in segment order: of its next segment)

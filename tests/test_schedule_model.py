@@ -14,36 +14,41 @@ MAX_GRID = 1024     # kDecMaxGrid
 SHORT = 8           # kShortTiles
 
 
-TAPER_DIV, TAPER_PCT, MAX_TAPER_GRID = 6, 40, 256    # kTaperDiv, kTaperPct, kMaxTaperGrid
+TAPER_STRONG, TAPER_MILD, MAX_TAPER_GRID = (3, 60), (6, 40), 256   # kTaperStrong*, kTaperMild*, kMaxTaperGrid
 
 
-def share_weight(c, gs, L):
+def taper_setting(max_nt, T, gs):
+    """(div, pct): strong when the longest segment spans more CTAs than one merge group."""
+    return TAPER_STRONG if max_nt * gs > MERGE_FAN * T else TAPER_MILD
+
+
+def share_weight(c, gs, L, pct):
     m = max(0, c - (gs - L))
-    return 200 * L * c - TAPER_PCT * m * (m + 1)
+    return 200 * L * c - pct * m * (m + 1)
 
 
-def taper_count(early, T, gs):
+def taper_count(early, T, gs, div=TAPER_MILD[0], pct=TAPER_MILD[1]):
     """Tapered shares of a call (0: equal shares)."""
-    L = gs // TAPER_DIV if early and gs <= MAX_TAPER_GRID else 0
+    L = gs // div if early and gs <= MAX_TAPER_GRID else 0
     if L == 0:
         return 0
-    return L if T * (2 * L * (100 - TAPER_PCT)) >= share_weight(gs, gs, L) else 0
+    return L if T * (2 * L * (100 - pct)) >= share_weight(gs, gs, L, pct) else 0
 
 
-def share_raw(c, T, gs, L):
+def share_raw(c, T, gs, L, pct=TAPER_MILD[1]):
     if c <= 0:
         return 0
     if c >= gs:
         return T
-    return T * share_weight(c, gs, L) // share_weight(gs, gs, L) if L else c * T // gs
+    return T * share_weight(c, gs, L, pct) // share_weight(gs, gs, L, pct) if L else c * T // gs
 
 
-def owner(t, T, gs, L=0):
+def owner(t, T, gs, L=0, pct=TAPER_MILD[1]):
     """The CTA whose share holds tile t of a long segment: closed form for equal shares,
     else the last c whose raw cut is at or before t."""
     if not L:
         return ((t + 1) * gs + T - 1) // T - 1
-    return max(c for c in range(gs) if share_raw(c, T, gs, L) <= t)
+    return max(c for c in range(gs) if share_raw(c, T, gs, L, pct) <= t)
 
 
 LATE_SHARES = 8     # kLateShares
@@ -74,14 +79,14 @@ def short_limit(T, grid):
     return 0 if T <= grid else SHORT
 
 
-def share_cut(c, T, gs, tile0, nt, order, L=0, short=SHORT):
+def share_cut(c, T, gs, tile0, nt, order, L=0, short=SHORT, pct=TAPER_MILD[1]):
     """First tile of CTA c's share: its raw cut (c*T/gs, or tapered), moved to the nearer end
     (ties: its start) of the segment it falls in when that segment has at most `short` tiles."""
     if c <= 0:
         return 0
     if c >= gs:
         return T
-    raw = share_raw(c, T, gs, L)
+    raw = share_raw(c, T, gs, L, pct)
     pos = int(np.searchsorted(tile0[order], raw, side="right")) - 1   # last position starting <= raw
     s = int(order[pos])
     t0, n = int(tile0[s]), int(nt[s])
@@ -102,16 +107,17 @@ def decode_schedule(nt, grid, early=False):
     order, tile0 = sequence(nt, grid)
     T = int(nt.sum())
     gs = min(grid, T)
-    L = taper_count(early, T, gs)
     short = short_limit(T, grid)
-    cuts = [share_cut(c, T, gs, tile0, nt, order, L, short) for c in range(gs + 1)]
+    div, pct = taper_setting(int(nt.max()) if len(nt) else 0, T, gs)
+    L = taper_count(early, T, gs, div, pct)
+    cuts = [share_cut(c, T, gs, tile0, nt, order, L, short, pct) for c in range(gs + 1)]
     segs, pieces = [], {}
     for s, (t0, n) in enumerate(zip(tile0, nt)):
         if n == 0:
             segs.append(None)
             continue
         if n > short:
-            c0, c1 = owner(int(t0), T, gs, L), owner(int(t0 + n - 1), T, gs, L)
+            c0, c1 = owner(int(t0), T, gs, L, pct), owner(int(t0 + n - 1), T, gs, L, pct)
         else:
             c0 = c1 = -1
         later = int(c1 > c0 and cuts[c0] < t0)
@@ -125,7 +131,7 @@ def decode_schedule(nt, grid, early=False):
                 continue
             pieces[(s, c)] = 2 * c + (0 if first else 1)
             first = False
-    return T, gs, cuts, segs, pieces, L
+    return T, gs, cuts, segs, pieces, (L, pct)
 
 
 @pytest.mark.parametrize("early", [False, True])
@@ -145,7 +151,7 @@ def test_decode_shares_slots_and_counters(seed, early):
         nt = np.zeros(nseg, np.int64); nt[rng.integers(nseg)] = int(rng.integers(1, 3000))
     else:                                                   # windows of 5 tiles and a few long heads
         nt = np.full(nseg, 5, np.int64); nt[rng.integers(nseg, size=3)] = rng.integers(9, 1100, 3)
-    T, gs, cuts, segs, pieces, L = decode_schedule(nt, grid, early)
+    T, gs, cuts, segs, pieces, (L, pct) = decode_schedule(nt, grid, early)
     # the cuts are monotone and the shares tile [0, T)
     assert cuts[0] == 0 and cuts[-1] == T and all(a <= b for a, b in zip(cuts, cuts[1:]))
     _, tile0 = sequence(nt, grid)
@@ -159,7 +165,7 @@ def test_decode_shares_slots_and_counters(seed, early):
             t0_, c0, k, _ = segs[s]
             assert held == list(range(c0, c0 + k))
             for t in range(int(t0), int(t0 + n)):
-                c = owner(t, T, gs, L)
+                c = owner(t, T, gs, L, pct)
                 assert cuts[c] <= t < cuts[c + 1]
     # slots: the kernel's split_slot formula gives the producer's slot; all distinct, < 2*grid
     split_slots = {}
@@ -276,16 +282,23 @@ def test_prefill_items_cover_each_unit_once(seed):
 
 
 def test_tapered_shares_shrink_towards_the_last_cta():
-    # the decode microbenchmark's 2720 tiles over 148 CTAs with early start: the first
-    # 124 shares are equal, the last 24 shrink step by step to 60 % of a full share
+    # the decode microbenchmark's 2720 tiles over 148 CTAs with early start: its long
+    # segments span ~3.5 CTAs, so the mild taper -- the first 124 shares equal, the last 24
+    # shrinking step by step to 60 % of a full share
     nt = np.tile([64] + [3] * 7, 32)
-    T, gs, cuts, segs, pieces, L = decode_schedule(nt, 148, early=True)
-    assert L == 24
-    raw = [share_raw(c, T, gs, L) for c in range(gs + 1)]
+    T, gs, cuts, segs, pieces, (L, pct) = decode_schedule(nt, 148, early=True)
+    assert (L, pct) == (24, 40)
+    raw = [share_raw(c, T, gs, L, pct) for c in range(gs + 1)]
     w = np.diff(raw)
-    full = T * 200 * L / share_weight(gs, gs, L)
+    full = T * 200 * L / share_weight(gs, gs, L, pct)
     assert abs(w[:gs - L].mean() - full) < 1 and abs(w[-1] - 0.6 * full) <= 1
     assert all(w[i] >= w[i + 1] - 1 for i in range(gs - L - 1, gs - 1))
     assert sum(w) == T and min(w) >= 1
+    # a 128K-stack layer with a global head spans ~143 CTAs: the strong taper, the last 49
+    # shares down to 40 %
+    nt = [5] * 8
+    nt[3] = 1032
+    T, gs, cuts, segs, pieces, (L, pct) = decode_schedule(nt, 148, early=True)
+    assert (L, pct) == (49, 60)
     # no taper without early start, or when a share would hold less than a tile
     assert taper_count(False, T, gs) == 0 and taper_count(True, 150, 148) == 0
