@@ -668,7 +668,7 @@ def ours_main(args, world, rank, local):
 
     dom = max(("rope", "prefill", "decode"), key=lambda k: parts[k]["ms"])
     if dom == "prefill":
-        roof = {"kernel": "prefill_tc_kernel (with its planner and combine)", "bound": "tensor",
+        roof = {"kernel": "prefill_tc_kernel (with its planner)", "bound": "tensor",
                 "achieved": parts["prefill"]["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
         roof["traffic"] = None
     elif dom == "decode":

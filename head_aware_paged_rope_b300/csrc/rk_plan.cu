@@ -224,7 +224,7 @@ __global__ __launch_bounds__(kPlanThreads) void plan_kernel(AttnParams p, AttnWo
 //     the decode grid takes tiles [c*T/gs, (c+1)*T/gs), so tile t belongs to CTA
 //     ((t+1)*gs + T - 1) / T - 1 (the others get no tiles);
 //  3. per segment the CTAs its tiles fall to; segments with more than one get consecutive
-//     partial slots and are listed for the combine kernel;
+//     partial slots and are listed for combine_decode_tc_kernel;
 //  4. per CTA the segment holding its first tile.
 // Per-segment tile counts and prefixes stay in shared memory (8 bytes per segment).
 __global__ __launch_bounds__(kPlanThreads) void plan_decode_kernel(AttnParams p, DecWorkspace ws) {

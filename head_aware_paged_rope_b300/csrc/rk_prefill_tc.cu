@@ -141,6 +141,8 @@ __device__ __forceinline__ bool merge_split_units(const AttnParams& p, const Att
   const int n_jobs = ws.header->n_split * rb;
   const int G = p.G;
   volatile int32_t* vcounter = &ws.header->merge_counter;
+  // diagnostic: wait for one stored piece more than there are, so that the bounded wait runs out
+  const int extra = (p.flags & RK_ATTN_DIAG_EXPIRE_WAIT) ? 1 : 0;
   for (int k = 0;; ++k) {
     if (wtid == 0) {
       int job;
@@ -157,7 +159,7 @@ __device__ __forceinline__ bool merge_split_units(const AttnParams& p, const Att
           const int u = ws.split_list[j / rb];
           int done;
           asm volatile("ld.acquire.gpu.s32 %0, [%1];" : "=r"(done) : "l"(ws.unit_done + u) : "memory");
-          if (done >= 8 * ws.units[u].n_splits) {
+          if (done >= 8 * ws.units[u].n_splits + extra) {
             if (atomicCAS(&ws.header->merge_counter, j, j + 1) == j) { job = j; break; }
             continue;
           }
@@ -176,7 +178,8 @@ __device__ __forceinline__ bool merge_split_units(const AttnParams& p, const Att
     if (job < 0 || job >= n_jobs) return true;
     const int u = ws.split_list[job / rb];
     const Unit un = ws.units[u];
-    const bool got = (BACKGROUND || wtid != 0) ? true : wait_count(b, ws.unit_done + u, 8 * un.n_splits, &ws.header->counter);
+    const bool got =
+        (BACKGROUND || wtid != 0) ? true : wait_count(b, ws.unit_done + u, 8 * un.n_splits + extra, &ws.header->counter);
     if (!named_bar_and(bar, nthreads, got)) return false;
     const int ns = un.n_splits;
     for (int r = (job % rb) * kJobRows + wl; r < (job % rb + 1) * kJobRows; r += nwarps) {

@@ -230,11 +230,15 @@ typedef struct rk_attn_args {
  * calls of the layers after rk_ring_advance satisfy this. */
 #define RK_ATTN_POOLS_STABLE 2
 
-/* Diagnostic, decode only: the first CTA of the decode kernel also waits for a word of the
- * workspace header that nothing sets, so that its bounded wait (1 s) runs out.  The call
- * then ends with RK_ERR_TIMEOUT in the status word, the way a wait that never completes
- * would end it, without any fault; every role of the kernel leaves.  For testing that error
- * path only.  Zero the workspace again before its next use. */
+/* Diagnostic: a bounded wait is made to run out, and the call ends with RK_ERR_TIMEOUT in
+ * the status word, the way a wait that never completes would end it, without any fault;
+ * every role of the kernel leaves.  For testing that error path only.
+ *  - Decode: the first CTA also waits for a word of the workspace header that nothing sets
+ *    (1 s).  Zero the workspace again before its next use.
+ *  - Prefill: the merge of query tiles cut into several pieces waits for one piece more
+ *    than there are; it gives up 1 s after the last piece was taken (the outputs of those
+ *    tiles are then undefined).  Calls without a split tile wait for nothing.  The next
+ *    call needs no reset: the planner re-initialises the workspace. */
 #define RK_ATTN_DIAG_EXPIRE_WAIT (1 << 30)
 
 /* Bytes of workspace rk_segpaged_prefill / rk_segpaged_decode need for these sizes

@@ -554,6 +554,30 @@ def test_decode_bounded_wait_runs_out_and_the_workspace_recovers(rk):
         assert int(ws[256:28928].count_nonzero().item()) == 0
 
 
+def test_prefill_merge_wait_runs_out_and_the_next_call_is_correct(rk):
+    """With RK_ATTN_DIAG_EXPIRE_WAIT the prefill kernel's merge of split query tiles waits for
+    one stored piece more than a tile has: its bounded wait runs out (1 s after the last
+    piece was taken), the call reports RK_ERR_TIMEOUT and the kernel ends -- no fault, no
+    hang.  The next call on the same workspace, without the flag, is correct."""
+    import time
+    w = synth.rag_prefill(n_segments=3, seg_tokens=1000, n_suffix=77)
+    da = attn_to_device(w.attn, "cuda")
+    st = _status()
+    base = da.args(rk, decode=False, status=st)
+    ws = torch.zeros(rk.segpaged_prefill_workspace_size(base), dtype=torch.uint8, device="cuda")
+    t0 = time.time()
+    rk.segpaged_prefill(da.args(rk, decode=False, status=st, flags=rk.RK_ATTN_DIAG_EXPIRE_WAIT), workspace=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5                       # RK_ERR_TIMEOUT
+    assert time.time() - t0 < 20
+    st.zero_()
+    da.out.fill_(float("nan"))
+    rk.segpaged_prefill(da.args(rk, decode=False, status=st), workspace=ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _compare(w.attn, da.out.float().cpu().numpy(), da.lse.cpu().numpy())
+
+
 def test_non_ascending_logical_list_is_reported(rk):
     """A page list whose logical pages do not ascend (here: last entry below the span its
     length needs) is reported as RK_ERR_DEVICE_ORDER by prefill and decode."""
