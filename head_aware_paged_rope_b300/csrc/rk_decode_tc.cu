@@ -13,11 +13,13 @@
 //
 // Schedule: the 128-key tiles of all head segments form one sequence of T tiles and CTA c
 // takes the share [cut(c), cut(c+1)) of it, cut(c) = c*T/gs (gs = the smaller of the grid,
-// one CTA per SM, and T); when no segment has more than kAlignTiles tiles and there are no
-// more segments than CTAs, CTA c takes segment c whole instead.  On the single-launch path
-// a cut that falls inside a segment of at most kShortTiles tiles moves to the nearer end
-// of that segment, so short segments (the windows of local heads) are never split and need
-// no merge; only long segments are shared by several CTAs.  Up to kDecFusedSegs head
+// one CTA per SM, and T).  On the single-launch path, with early start the last shares are
+// tapered (the CTAs dispatched last start late), and a cut that falls inside a segment of at
+// most kShortTiles tiles moves to the nearer end of that segment, so short segments (the
+// windows of local heads) are never split and need no merge; only long segments are shared
+// by several CTAs.  Two exceptions: with no more tiles than CTAs every tile gets its own CTA
+// (windows split too), and when no segment has more than kAlignTiles tiles and there are no
+// more segments than CTAs, CTA c takes segment c whole.  Up to kDecFusedSegs head
 // segments every CTA plans this itself (visible ranges in three interleaved rounds of
 // loads, a block scan of the tile counts) and a segment shared by several CTAs is merged
 // inside the kernel; beyond that, plan_decode_kernel (rk_plan.cu) plans and
