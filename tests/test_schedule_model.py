@@ -302,3 +302,101 @@ def test_tapered_shares_shrink_towards_the_last_cta():
     assert (L, pct) == (49, 60)
     # no taper without early start, or when a share would hold less than a tile
     assert taper_count(False, T, gs) == 0 and taper_count(True, 150, 148) == 0
+
+
+def simulate_prefill_merges(n_vis, chunk, grid, rng):
+    """Discrete-event model of the prefill kernel's merge protocol: per CTA a producer takes
+    items (its blockIdx first, then tickets from a counter), its softmax warps finish them in
+    order and count them on their unit; a background worker (warps 10-11) claims the next
+    merge job only while items remain and only when that job's unit is complete (a
+    compare-and-swap on the job counter); once a CTA's items are done its softmax warps claim
+    jobs outright and wait for the unit.  Returns the merge log [(job, unit, time,
+    worker kind)] and the time every unit completed."""
+    items, first, split = prefill_plan(n_vis, chunk)
+    rb = 32                                        # jobs per split unit (256 rows / 8)
+    n_jobs = len(split) * rb
+    ns = {u: 0 for u in range(len(n_vis))}
+    for (u, _, _) in items:
+        ns[u] += 1
+    done = {u: 0 for u in range(len(n_vis))}
+    complete_at = {}
+    counter = 0                                    # item tickets taken
+    job_counter = 0
+    log = []
+    # per CTA: queue of (finish time) items; time advances in events
+    t = 0.0
+    cta_items = {c: [] for c in range(grid)}
+    busy_until = {c: 0.0 for c in range(grid)}
+    next_item = {c: (c if c < len(items) else None) for c in range(grid)}
+    fast_state = {c: None for c in range(grid)}    # job a CTA's softmax warps wait on
+    bg_free_at = {c: 0.0 for c in range(grid)}
+    finished = {c: False for c in range(grid)}
+    for _ in range(100000):
+        progressed = False
+        for c in range(grid):
+            # producer + softmax: process the next item when free
+            if next_item[c] is not None and busy_until[c] <= t:
+                it = next_item[c]
+                u = items[it][0]
+                dur = 1.0 + (items[it][2] - items[it][1]) * rng.uniform(0.8, 1.2) / max(chunk, 1)
+                busy_until[c] = t + dur
+                cta_items[c].append((t + dur, u))
+                tk = counter
+                counter += 1
+                nxt = grid + tk
+                next_item[c] = nxt if nxt < len(items) else None
+                progressed = True
+            # completions
+            for (ft, u) in list(cta_items[c]):
+                if ft <= t:
+                    cta_items[c].remove((ft, u))
+                    done[u] += 1
+                    if done[u] == ns[u]:
+                        complete_at[u] = ft
+                    progressed = True
+            items_left = counter + grid < len(items)
+            # background worker: claims only completed units while items remain
+            if bg_free_at[c] <= t and items_left and job_counter < n_jobs:
+                u = split[job_counter // rb]
+                if done[u] == ns[u]:
+                    log.append((job_counter, u, t, "bg"))
+                    job_counter += 1
+                    bg_free_at[c] = t + 0.3
+                    progressed = True
+            # softmax warps after their items: claim outright, wait for the unit
+            if next_item[c] is None and not cta_items[c] and busy_until[c] <= t and not finished[c]:
+                if fast_state[c] is None:
+                    if job_counter >= n_jobs:
+                        finished[c] = True
+                    else:
+                        fast_state[c] = job_counter
+                        job_counter += 1
+                    progressed = True
+                else:
+                    j = fast_state[c]
+                    u = split[j // rb]
+                    if done[u] == ns[u]:
+                        log.append((j, u, t, "tail"))
+                        fast_state[c] = None
+                        busy_until[c] = t + 0.1
+                        progressed = True
+        if all(finished.values()):
+            return log, complete_at, n_jobs
+        if not progressed:
+            t += 0.05
+    raise AssertionError("the merge protocol did not terminate")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_prefill_merge_jobs_run_once_each_after_their_unit(seed):
+    rng = np.random.default_rng(500 + seed)
+    chunk = int(rng.choice([12, 24, 96]))
+    grid = int(rng.choice([4, 16, 40]))
+    n_vis = np.concatenate([rng.integers(1, chunk, int(rng.integers(5, 60))),          # short singles
+                            rng.integers(2 * chunk, 8 * chunk, int(rng.integers(1, 8)))])  # split units
+    rng.shuffle(n_vis)
+    log, complete_at, n_jobs = simulate_prefill_merges(n_vis, chunk, grid, rng)
+    jobs = [j for (j, _, _, _) in log]
+    assert sorted(jobs) == list(range(n_jobs))                       # every job, once
+    for (j, u, t, kind) in log:
+        assert t >= complete_at[u]                                   # only after its unit completed
